@@ -1,0 +1,180 @@
+/*
+ * pkv.h -- C ABI of libpkv.so: paged KV cache decode attention on GB300
+ * (sm_103a).
+ *
+ * What the operations are (page title, section):
+ *   - "How does TensorRT-LLM work?", "The paged KV cache": KV memory is one
+ *     pool of equal fixed-size blocks handed out on demand; a small per-request
+ *     table lists the request's blocks in order; decode attends over every
+ *     earlier token, whose keys and values are kept in that cache.
+ *   - "Introduction to TensorRT-LLM", "2. Paged KV Cache": fixed-size token
+ *     blocks, virtual-to-physical block tables; section "4. Optimized
+ *     Attention Kernels" names FlashAttention and Flash-Decoding (fused
+ *     kernels, split over the key/value length).
+ *   - "TensorRT-LLM, in depth", "First principles": kv_bytes_per_token =
+ *     2 * layers * kv_heads * head_dim * bytes_per_elem; grouped-query
+ *     attention (Llama-3-8B: 32 query heads share 8 KV heads).
+ *   - "TensorRT-LLM, in depth", "Quantization": an FP8 KV cache halves the
+ *     cache bytes.
+ *
+ * Conventions for every entry point:
+ *   - Device buffers are plain device pointers owned by the caller (e.g. torch
+ *     tensors).  The library never allocates or frees device memory and never
+ *     synchronises the stream; work is enqueued on `stream` (a cudaStream_t,
+ *     NULL = legacy default stream).
+ *   - Every dense tensor is C-contiguous.  q, out, k, v, the pool bases and the
+ *     workspace must be 16-byte aligned; int32/int64 arrays naturally aligned.
+ *   - Host-checkable faults return an error before anything is enqueued.
+ *     Index faults that only the device can see (a block id outside the pool,
+ *     a slot outside the pool, a length beyond the block table) never touch
+ *     memory out of bounds: the offending access is skipped and, when the pool
+ *     has an error word, a bit is OR-ed into it (PKV_ERRBIT_*).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or index */
+    PKV_ERR_UNSUPPORTED = 2,   /* geometry or dtype this build has no kernel for */
+    PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    PKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    PKV_ERR_DEVICE_BOUNDS = 5  /* reserved for callers decoding the error word */
+} pkv_status;
+
+/* Element types.  PKV_FP8_E4M3 is OCP E4M3 (bias 7, max 448, no infinities). */
+typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
+
+/* Bits OR-ed into the pool's error word by the kernels. */
+#define PKV_ERRBIT_BLOCK_ID 1 /* block table entry outside [0, num_blocks) */
+#define PKV_ERRBIT_SLOT 2     /* slot_mapping entry outside [-1, num_blocks*block_size) */
+#define PKV_ERRBIT_SEQ_LEN 4  /* seq_lens entry < 0 or > max_blocks_per_seq*block_size */
+
+/* Kernel design used by paged_decode_attention. */
+typedef enum pkv_algo {
+    PKV_ALGO_AUTO = 0, /* best available for the pool's dtype and geometry */
+    PKV_ALGO_SIMT = 1, /* CUDA-core dot products (every dtype) */
+    PKV_ALGO_MMA = 2   /* tensor-core QK^T and PV (BF16 / FP8 pools) */
+} pkv_algo;
+
+/*
+ * Pool geometry.  The K pool and the V pool are each one device tensor laid
+ * out [num_layers][num_blocks][num_kv_heads][block_size][head_dim] in
+ * kv_dtype, so that one (block, kv head) is a contiguous run of
+ * block_size*head_dim elements.  A slot is block_id*block_size + offset.
+ * k_scale / v_scale are the per-tensor dequantisation scales of an FP8 pool
+ * (value = e4m3 * scale; appends store e4m3(x * (1/scale)), with 1/scale
+ * rounded once to binary32); they are ignored for other dtypes.
+ * error_word: optional device int32 the kernels OR PKV_ERRBIT_* into; may be
+ * NULL.  Supported: block_size in {16, 32, 64}, head_dim in {64, 128}.
+ */
+typedef struct pkv_pool_desc {
+    int32_t num_layers;
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    pkv_dtype kv_dtype;
+    float k_scale;
+    float v_scale;
+    void* k_base;        /* device */
+    void* v_base;        /* device */
+    int32_t* error_word; /* device, optional */
+} pkv_pool_desc;
+
+/* Opaque host handle: a validated copy of the descriptor.  It owns no device
+ * memory; destroying it leaves the caller's tensors untouched. */
+typedef struct pkv_pool pkv_pool;
+
+/* Validate `desc` and create a handle.  INVALID_ARG / UNSUPPORTED on a bad
+ * descriptor ("TensorRT-LLM, in depth", "The paged KV cache and block reuse":
+ * the KV cache manager splits reserved memory into fixed-size blocks). */
+pkv_status kv_pool_create(const pkv_pool_desc* desc, pkv_pool** out);
+void kv_pool_destroy(pkv_pool* pool);
+
+/* Bytes of one pool tensor (K or V) for the descriptor's geometry. */
+size_t kv_pool_tensor_bytes(const pkv_pool_desc* desc);
+
+/* "TensorRT-LLM, in depth", "First principles": bytes of K and V that one
+ * token occupies across all layers: 2 * layers * kv_heads * head_dim * size. */
+int64_t kv_bytes_per_token(int32_t num_layers, int32_t num_kv_heads, int32_t head_dim,
+                           pkv_dtype dtype);
+
+/*
+ * KV append ("How does TensorRT-LLM work?", "The paged KV cache": every new
+ * token adds one more set of keys/values, written into the request's blocks).
+ *   k, v          device [num_tokens][num_kv_heads][head_dim] in in_dtype
+ *                 (PKV_F32 or PKV_BF16; an F32 pool takes F32 only).
+ *   slot_mapping  device int64 [num_tokens]; token t goes to slot
+ *                 slot_mapping[t] of layer `layer`; -1 skips the token.
+ * Conversion: same dtype copies bits; F32->BF16 rounds to nearest even;
+ * ->FP8 stores e4m3_rn_satfinite(fp32(x) * fp32(1/scale)).  Two tokens that
+ * name the same slot race (undefined which one lands).
+ */
+pkv_status kv_append(const pkv_pool* pool, int32_t layer, const void* k, const void* v,
+                     pkv_dtype in_dtype, const int64_t* slot_mapping, int32_t num_tokens,
+                     void* stream);
+
+/*
+ * Split planning for paged_decode_attention.  Flash-decoding splits each
+ * sequence's tokens into chunks of `split_tokens` (0 = choose automatically
+ * from the batch shape and the GPU's SM count), attends to each chunk in its
+ * own CTA and merges the partial results by their log-sum-exp.  Outputs (any
+ * may be NULL): the split size actually used, the number of splits of the
+ * longest sequence, and the workspace bytes the call needs (0 when a single
+ * split covers max_seq_len).  split_tokens, when given, must be a positive
+ * multiple of 64 and of block_size.
+ */
+pkv_status paged_decode_plan(const pkv_pool* pool, int32_t num_seqs, int32_t num_q_heads,
+                             int32_t max_seq_len, int32_t split_tokens, int32_t* split_tokens_out,
+                             int32_t* num_splits_out, size_t* workspace_bytes_out);
+
+/*
+ * Paged decode attention ("How does TensorRT-LLM work?", "Custom attention
+ * kernels" and "The paged KV cache"): for every sequence b and query head hq,
+ *     out[b][hq][:] = softmax_t(scale * q[b][hq] . K_t) V_t,
+ *     t = 0 .. seq_lens[b]-1,
+ * where K_t / V_t are row t % block_size of block block_tables[b][t /
+ * block_size] of the pool's layer `layer`, KV head hq / (num_q_heads /
+ * num_kv_heads) (grouped-query attention), times k_scale / v_scale for FP8.
+ *   q             device [num_seqs][num_q_heads][head_dim], q_dtype = F32 for
+ *                 an F32 pool, BF16 otherwise.
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]; only the first
+ *                 ceil(seq_lens[b]/block_size) entries of row b are read.
+ *   seq_lens      device int32 [num_seqs].  A length of 0 gives a zero row.
+ *   max_seq_len   host upper bound of seq_lens (sizes the grid); must be
+ *                 <= max_blocks_per_seq * block_size.  Longer device lengths
+ *                 are clamped to it and flagged PKV_ERRBIT_SEQ_LEN.
+ *   workspace     device scratch of at least the planned bytes (may be NULL
+ *                 when the plan needs none); its contents on entry do not
+ *                 matter.  Calls that share a workspace must be stream-ordered.
+ *   out           device [num_seqs][num_q_heads][head_dim] in q_dtype.
+ *   algo          PKV_ALGO_AUTO, or a specific kernel design.
+ * Softmax and accumulation are fp32; the output is rounded to q_dtype (RN).
+ */
+pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_pool* pool,
+                                  int32_t layer, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                  int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
+                                  float scale, int32_t split_tokens, pkv_algo algo,
+                                  void* workspace, size_t workspace_bytes, void* out,
+                                  void* stream);
+
+/* Human-readable name of a status. */
+const char* pkv_status_string(pkv_status status);
+
+/* Message of the last CUDA error seen by this thread's calls ("" if none). */
+const char* pkv_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,232 @@
+// C ABI of libpkv.so: argument validation, split planning and launches.
+// Everything here runs on the host; it allocates no device memory and never
+// synchronises a stream.
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+thread_local char g_last_cuda_error[256] = "";
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool valid_dtype(pkv_dtype t) { return t == PKV_F32 || t == PKV_BF16 || t == PKV_FP8_E4M3; }
+
+pkv_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return PKV_OK;
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    set_last_error(e);
+    return PKV_ERR_CUDA;
+}
+
+int g_sms[64] = {0};
+}  // namespace
+
+void set_last_error(cudaError_t e) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+}
+
+int dtype_bytes(pkv_dtype t) {
+    switch (t) {
+        case PKV_F32: return 4;
+        case PKV_BF16: return 2;
+        case PKV_FP8_E4M3: return 1;
+    }
+    return 0;
+}
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64 && g_sms[dev] > 0) return g_sms[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) g_sms[dev] = n;
+    return n;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported geometry or dtype";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PKV_ERR_CUDA: return "CUDA error";
+        case PKV_ERR_DEVICE_BOUNDS: return "device-side index out of bounds";
+    }
+    return "unknown status";
+}
+
+const char* pkv_last_cuda_error(void) { return g_last_cuda_error; }
+
+int64_t kv_bytes_per_token(int32_t num_layers, int32_t num_kv_heads, int32_t head_dim, pkv_dtype dtype) {
+    return 2LL * num_layers * num_kv_heads * head_dim * dtype_bytes(dtype);
+}
+
+size_t kv_pool_tensor_bytes(const pkv_pool_desc* d) {
+    if (!d || !valid_dtype(d->kv_dtype)) return 0;
+    return static_cast<size_t>(d->num_layers) * d->num_blocks * d->num_kv_heads * d->block_size *
+           d->head_dim * dtype_bytes(d->kv_dtype);
+}
+
+pkv_status kv_pool_create(const pkv_pool_desc* d, pkv_pool** out) {
+    if (!d || !out) return PKV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!valid_dtype(d->kv_dtype)) return PKV_ERR_INVALID_ARG;
+    if (d->num_layers < 1 || d->num_blocks < 1 || d->num_kv_heads < 1) return PKV_ERR_INVALID_ARG;
+    if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return PKV_ERR_UNSUPPORTED;
+    if (d->head_dim != 64 && d->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (!d->k_base || !d->v_base || !aligned(d->k_base, 16) || !aligned(d->v_base, 16))
+        return PKV_ERR_INVALID_ARG;
+    if (d->error_word && !aligned(d->error_word, 4)) return PKV_ERR_INVALID_ARG;
+    // slots and element offsets are int64; keep one layer's slot count in int32
+    if (static_cast<int64_t>(d->num_blocks) * d->block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    float ks = 1.f, vs = 1.f;
+    if (d->kv_dtype == PKV_FP8_E4M3) {
+        if (!(std::isfinite(d->k_scale) && d->k_scale > 0.f && std::isfinite(d->v_scale) && d->v_scale > 0.f))
+            return PKV_ERR_INVALID_ARG;
+        ks = d->k_scale;
+        vs = d->v_scale;
+    }
+    pkv_pool* p = static_cast<pkv_pool*>(std::malloc(sizeof(pkv_pool)));
+    if (!p) return PKV_ERR_INVALID_ARG;
+    p->d = *d;
+    p->d.k_scale = ks;
+    p->d.v_scale = vs;
+    p->elem_bytes = dtype_bytes(d->kv_dtype);
+    p->layer_bytes = static_cast<size_t>(d->num_blocks) * d->num_kv_heads * d->block_size * d->head_dim *
+                     p->elem_bytes;
+    volatile float one = 1.f;  // one binary32 division each, on the host
+    p->k_inv_scale = one / ks;
+    p->v_inv_scale = one / vs;
+    *out = p;
+    return PKV_OK;
+}
+
+void kv_pool_destroy(pkv_pool* p) { std::free(p); }
+
+pkv_status kv_append(const pkv_pool* p, int32_t layer, const void* k, const void* v, pkv_dtype in_dtype,
+                     const int64_t* slot_mapping, int32_t num_tokens, void* stream) {
+    if (!p || layer < 0 || layer >= p->d.num_layers || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (in_dtype != PKV_F32 && in_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (p->d.kv_dtype == PKV_F32 && in_dtype != PKV_F32) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    return cuda_status(launch_kv_append(p, layer, k, v, in_dtype, slot_mapping, num_tokens,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status paged_decode_plan(const pkv_pool* p, int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
+                             int32_t split_tokens, int32_t* split_out, int32_t* nsplit_out, size_t* ws_out) {
+    if (!p || num_seqs < 0 || num_q_heads < 1 || max_seq_len < 0 || split_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % p->d.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    int S = split_tokens;
+    if (S > 0) {
+        if (S % kTileTokens != 0 || S % p->d.block_size != 0) return PKV_ERR_INVALID_ARG;
+    } else {
+        // Auto: 512-token splits, halved (down to one tile) while the batch
+        // would give fewer than two CTAs per SM.
+        const int sms = num_sms() > 0 ? num_sms() : 148;
+        const int64_t pairs = static_cast<int64_t>(num_seqs) * p->d.num_kv_heads;
+        S = 512;
+        while (S > kTileTokens && pairs * ((max_seq_len + S - 1) / S) < 2LL * sms) S /= 2;
+        if (S % p->d.block_size != 0) S = p->d.block_size > kTileTokens ? p->d.block_size : kTileTokens;
+    }
+    int64_t ns = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + S - 1) / S : 1;
+    if (ns < 1) ns = 1;
+    if (ns > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    size_t ws = 0;
+    if (ns > 1) {
+        const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * ns;
+        ws = round_up(rows * p->d.head_dim * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+    }
+    if (split_out) *split_out = S;
+    if (nsplit_out) *nsplit_out = static_cast<int32_t>(ns);
+    if (ws_out) *ws_out = ws;
+    return PKV_OK;
+}
+
+pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_seq_len, float scale, int32_t split_tokens, pkv_algo algo,
+                                  void* workspace, size_t workspace_bytes, void* out, void* stream) {
+    if (!p || layer < 0 || layer >= p->d.num_layers) return PKV_ERR_INVALID_ARG;
+    if (num_seqs < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 || max_seq_len < 0) return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % p->d.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * p->d.block_size)
+        return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    const pkv_dtype want_q = p->d.kv_dtype == PKV_F32 ? PKV_F32 : PKV_BF16;
+    if (q_dtype != want_q) return PKV_ERR_UNSUPPORTED;
+    if (algo != PKV_ALGO_AUTO && algo != PKV_ALGO_SIMT && algo != PKV_ALGO_MMA) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+    if (!q || !out || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+    const int G = num_q_heads / p->d.num_kv_heads;
+
+    bool use_mma = false;
+    if (algo == PKV_ALGO_MMA) {
+        if (!decode_mma_supported(p->d.kv_dtype, p->d.head_dim, G, p->d.block_size)) return PKV_ERR_UNSUPPORTED;
+        use_mma = true;
+    } else if (algo == PKV_ALGO_AUTO) {
+        use_mma = decode_mma_supported(p->d.kv_dtype, p->d.head_dim, G, p->d.block_size);
+    }
+    if (!use_mma && !decode_simt_supported(p->d.kv_dtype, p->d.head_dim, G)) return PKV_ERR_UNSUPPORTED;
+
+    int32_t S = 0, NS = 0;
+    size_t need = 0;
+    pkv_status st = paged_decode_plan(p, num_seqs, num_q_heads, max_seq_len, split_tokens, &S, &NS, &need);
+    if (st != PKV_OK) return st;
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return PKV_ERR_WORKSPACE;
+
+    DecodeArgs a{};
+    a.q = q;
+    a.out = out;
+    a.k_layer = static_cast<const uint8_t*>(p->d.k_base) + static_cast<size_t>(layer) * p->layer_bytes;
+    a.v_layer = static_cast<const uint8_t*>(p->d.v_base) + static_cast<size_t>(layer) * p->layer_bytes;
+    a.tables = block_tables;
+    a.lens = seq_lens;
+    a.err = p->d.error_word;
+    a.max_blocks = max_blocks_per_seq;
+    a.max_len = max_seq_len;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = p->d.num_kv_heads;
+    a.head_dim = p->d.head_dim;
+    a.block_size = p->d.block_size;
+    a.num_blocks = p->d.num_blocks;
+    a.split_tokens = S;
+    a.num_splits = NS;
+    const float log2e = 1.4426950408889634f;
+    a.qk_scale_log2 = scale * p->d.k_scale * log2e;
+    a.v_scale = p->d.v_scale;
+    if (NS > 1) {
+        const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * NS;
+        a.o_part = static_cast<float*>(workspace);
+        a.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                              round_up(rows * p->d.head_dim * sizeof(float), 256));
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = use_mma ? launch_decode_mma(p->d.kv_dtype, a, s) : launch_decode_simt(p->d.kv_dtype, a, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (NS > 1) return cuda_status(launch_combine(q_dtype, a, s));
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// Internal declarations shared by the translation units of libpkv.so.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "pkv.h"
+
+// The validated pool handle behind the opaque pkv_pool type.
+struct pkv_pool {
+    pkv_pool_desc d;
+    int elem_bytes;          // bytes per stored element
+    size_t layer_bytes;      // bytes of one layer of one pool tensor
+    float k_inv_scale;       // binary32 1/k_scale (FP8 pools), else 1
+    float v_inv_scale;
+};
+
+namespace pkv {
+
+constexpr int kTileTokens = 64;  // tokens one decode CTA stages per pipeline step
+
+int dtype_bytes(pkv_dtype t);
+int num_sms();  // SM count of the current device (cached)
+void set_last_error(cudaError_t e);
+
+// ---------------------------------------------------------------- append
+cudaError_t launch_kv_append(const pkv_pool* pool, int layer, const void* k, const void* v,
+                             pkv_dtype in_dtype, const int64_t* slots, int num_tokens,
+                             cudaStream_t stream);
+
+// ---------------------------------------------------------------- decode
+struct DecodeArgs {
+    const void* q;
+    void* out;
+    const uint8_t* k_layer;   // base of the layer in the K pool
+    const uint8_t* v_layer;
+    const int32_t* tables;
+    const int32_t* lens;
+    float* o_part;            // [B][Hq][num_splits][D] fp32 (split partials)
+    float* lse_part;          // [B][Hq][num_splits] log2-domain log-sum-exp
+    int32_t* err;             // optional error word
+    int max_blocks;
+    int max_len;              // host bound of seq_lens (<= max_blocks * block_size)
+    int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
+    int split_tokens, num_splits;
+    float qk_scale_log2;      // scale * k_scale * log2(e)
+    float v_scale;            // v_scale (FP8) or 1
+};
+
+// Returns cudaErrorNotSupported when no kernel matches (dtype, D, G).
+cudaError_t launch_decode_simt(pkv_dtype kv, const DecodeArgs& a, cudaStream_t stream);
+bool decode_simt_supported(pkv_dtype kv, int head_dim, int group);
+cudaError_t launch_decode_mma(pkv_dtype kv, const DecodeArgs& a, cudaStream_t stream);
+bool decode_mma_supported(pkv_dtype kv, int head_dim, int group, int block_size);
+cudaError_t launch_combine(pkv_dtype q_dtype, const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases compare every output element; they span several 64-token tiles,
+several splits and ragged tails.  Full-size workloads run in the benchmark's
+launch configuration and compare sampled sequences (all heads) one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_194_gb300 import binding as pk
+from paged_kv_cache_194_gb300 import workloads as wl
+from paged_kv_cache_194_gb300.decode import DecodeBatch
+
+from parity import TOL, compare, oracle_reference
+
+pytestmark = pytest.mark.gpu
+
+EDGE_LENS = (1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 300, 1000)
+
+
+def _w(name, G, Hkv, D, bs, kv, ind, lens, dist="normal", seed=21):
+    return wl.Workload(name, seed, len(lens), G * Hkv, Hkv, D, bs, kv, ind, 1.0 / math.sqrt(D),
+                       lens="fixed", fixed_lens=tuple(lens), dist=dist)
+
+
+SMALL = [
+    wl.WORKLOADS["tiny"],
+    _w("bf16_g4_d128_bs16", 4, 2, 128, 16, "bf16", "bf16", EDGE_LENS),
+    _w("bf16_g1_d128_bs32", 1, 3, 128, 32, "bf16", "bf16", (5, 64, 200, 33)),
+    _w("bf16_g2_d64_bs64", 2, 2, 64, 64, "bf16", "bf16", (1, 64, 65, 500)),
+    _w("bf16_g8_d128_bs16", 8, 1, 128, 16, "bf16", "bf16", (7, 130, 257)),
+    _w("bf16_g8_d64_bs32", 8, 2, 64, 32, "bf16", "bf16", (31, 32, 96)),
+    _w("fp8_g4_d128_bs64", 4, 2, 128, 64, "fp8", "bf16", EDGE_LENS),
+    _w("fp8_g2_d64_bs16", 2, 2, 64, 16, "fp8", "bf16", (3, 80, 129)),
+    _w("fp8_from_f32_g4", 4, 1, 128, 32, "fp8", "f32", (40, 100)),
+    _w("bf16_from_f32_g4", 4, 1, 128, 16, "bf16", "f32", (40, 100)),
+    _w("f32_g4_d128_bs32", 4, 2, 128, 32, "f32", "f32", (1, 70, 190), dist="uniform"),
+    _w("f32_g16_d64_bs16", 16, 1, 64, 16, "f32", "f32", (17, 99), dist="uniform"),
+    _w("with_empty_seq", 4, 2, 128, 16, "bf16", "bf16", (0, 5, 0, 77)),
+]
+
+
+def _run_step(batch, layer=0, split=0, algo="auto", step=0):
+    """One decode step through the C ABI: append the new token, attend."""
+    slots = batch.next_token_slots()
+    q, kn, vn = batch.step_inputs(layer, step)
+    pk.kv_append(batch.pool, layer, kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda())
+    tables, lens = batch.tables(), batch.seq_lens()
+    out = pk.paged_decode_attention(q.cuda(), batch.pool, layer, tables.cuda(), lens.cuda(),
+                                    int(lens.max()), batch.w.scale, split_tokens=split, algo=algo)
+    torch.cuda.synchronize()
+    return q, tables, lens, out
+
+
+def _algos(w):
+    return ["simt"] if w.kv_dtype == "f32" else ["simt", "auto"]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("split", [0, 64, 128])
+def test_small_parity(w, split):
+    if split % w.block_size:
+        pytest.skip("split must be a multiple of the block size")
+    inst = wl.instance(w)
+    for algo in _algos(w):
+        batch = DecodeBatch(inst)
+        q, tables, lens, out = _run_step(batch, split=split, algo=algo)
+        ref, _ = oracle_reference(w, inst.k_scale, inst.v_scale, 0, q, tables, lens.tolist(),
+                                  list(range(w.num_seqs)))
+        compare(out, ref, TOL[w.kv_dtype], "%s split=%d algo=%s" % (w.name, split, algo))
+        assert batch.pool.errors() == 0
+
+
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[6], SMALL[10], SMALL[0]], ids=lambda w: w.name)
+def test_append_bitexact_whole_pool(w):
+    """The GPU pool after prefill + one step equals the oracle's pool byte for
+    byte, including blocks no token touched (sentinel fill)."""
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst, fill_byte=0x5A)
+    slots = batch.next_token_slots()
+    q, kn, vn = batch.step_inputs(0)
+    pk.kv_append(batch.pool, 0, kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    tables = batch.tables().numpy()
+    opool = oracle.OraclePool(1, inst.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype,
+                              inst.k_scale, inst.v_scale, fill=0x5A)
+    for b in range(w.num_seqs):
+        L = int(inst.lens[b])
+        if L == 0:
+            continue
+        k, v = wl.seq_kv(w, 0, b, L)
+        oracle.kv_append(opool, 0, k, v, w.in_dtype, oracle.slot_mapping(tables, w.block_size, np.full(L, b), np.arange(L)))
+    gk = batch.pool.k.view(torch.uint8).cpu().numpy().ravel()
+    gv = batch.pool.v.view(torch.uint8).cpu().numpy().ravel()
+    assert np.array_equal(gk, opool.k.view(np.uint8).ravel())
+    assert np.array_equal(gv, opool.v.view(np.uint8).ravel())
+
+
+def test_append_skip_slot_and_bad_slot_flag():
+    w = SMALL[1]
+    inst = wl.instance(w)
+    pool = pk.KVPool(1, 8, 16, 2, 128, "bf16", fill=0)
+    k = torch.randn(3, 2, 128, dtype=torch.bfloat16, device="cuda")
+    before = pool.k.clone()
+    slots = torch.tensor([-1, 8 * 16, 5], dtype=torch.int64, device="cuda")  # skip, out of range, ok
+    pk.kv_append(pool, 0, k, k, slots)
+    torch.cuda.synchronize()
+    assert pool.errors() & pk.ERRBIT_SLOT
+    after = pool.k.view(8, 2, 16, 128)
+    assert torch.equal(after[0, :, 5], k[2])
+    mask = torch.ones(8, 2, 16, dtype=torch.bool, device="cuda")
+    mask[0, :, 5] = False
+    assert torch.equal(after[mask], before.view(8, 2, 16, 128)[mask])
+
+
+def test_single_token_is_exact():
+    w = _w("len1", 4, 2, 128, 16, "bf16", "bf16", (1, 1, 1, 1))
+    inst = wl.instance(w)
+    for algo in ("simt", "auto"):
+        batch = DecodeBatch(inst)
+        q, tables, lens, out = _run_step(batch, algo=algo)
+        _, kn, vn = batch.step_inputs(0)
+        want = vn.cuda().repeat_interleave(w.group, dim=1)  # [B, Hq, D]
+        assert torch.equal(out, want), algo
+
+
+def test_block_permutation_gives_identical_output():
+    w = SMALL[1]
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    q, tables, lens, out = _run_step(batch)
+    perm = torch.randperm(inst.num_blocks, generator=torch.Generator().manual_seed(5))
+    pool2 = pk.KVPool(1, inst.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype)
+    pool2.k[:, perm.cuda()] = batch.pool.k
+    pool2.v[:, perm.cuda()] = batch.pool.v
+    t2 = torch.where(tables >= 0, perm[tables.clamp(min=0).long()].to(torch.int32), tables)
+    out2 = pk.paged_decode_attention(q.cuda(), pool2, 0, t2.cuda(), lens.cuda(), int(lens.max()), w.scale)
+    assert torch.equal(out, out2)
+
+
+def test_split_equals_no_split():
+    w = _w("splits", 4, 2, 128, 16, "bf16", "bf16", (3000, 1234, 64, 4096))
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    q, tables, lens, out_split = _run_step(batch, split=64)
+    out_one = pk.paged_decode_attention(q.cuda(), batch.pool, 0, tables.cuda(), lens.cuda(), int(lens.max()),
+                                        w.scale, split_tokens=4096)
+    np.testing.assert_allclose(out_split.float().cpu().numpy(), out_one.float().cpu().numpy(), rtol=8e-3, atol=2e-3)
+
+
+def test_device_index_faults_are_flagged_not_fatal():
+    w = _w("faults", 4, 2, 128, 16, "bf16", "bf16", (40, 50))
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    q, tables, lens, out = _run_step(batch)
+    assert batch.pool.errors() == 0
+    bad = tables.clone()
+    bad[1, 1] = inst.num_blocks  # one past the pool
+    pk.paged_decode_attention(q.cuda(), batch.pool, 0, bad.cuda(), lens.cuda(), int(lens.max()), w.scale)
+    torch.cuda.synchronize()
+    assert batch.pool.errors() & pk.ERRBIT_BLOCK_ID
+    batch.pool.clear_errors()
+    long_lens = lens.clone()
+    long_lens[0] = int(lens.max()) + 5  # beyond max_seq_len given to the call
+    o3 = pk.paged_decode_attention(q.cuda(), batch.pool, 0, tables.cuda(), long_lens.cuda(), int(lens.max()), w.scale)
+    torch.cuda.synchronize()
+    assert batch.pool.errors() & pk.ERRBIT_SEQ_LEN
+    assert torch.isfinite(o3.float()).all()
+
+
+# ------------------------------------------------------------- full sizes
+
+def _sampled(B, k=4):
+    return sorted(set([0, B - 1] + list(np.random.default_rng(B).choice(B, size=min(k, B), replace=False))))
+
+
+@pytest.mark.parametrize("name", ["llama", "fp8"])
+def test_full_size_sampled(name):
+    w = wl.WORKLOADS[name]
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    q, tables, lens, out = _run_step(batch)  # auto split, as the benchmark runs it
+    seqs = _sampled(w.num_seqs)
+    ref, _ = oracle_reference(w, inst.k_scale, inst.v_scale, 0, q, tables, lens.tolist(), seqs)
+    compare(out[seqs], ref, TOL[w.kv_dtype], name)
+    assert batch.pool.errors() == 0
+
+
+def test_ragged_in_flight_steps():
+    w = wl.WORKLOADS["ragged"]
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    seqs = _sampled(w.num_seqs)
+    for step in range(w.steps):
+        q, tables, lens, out = _run_step(batch, step=step)
+        if step in (0, w.steps - 1):
+            ref, _ = oracle_reference(w, 1.0, 1.0, 0, q, tables, lens.tolist(), seqs)
+            compare(out[seqs], ref, TOL["bf16"], "ragged step %d" % step)
+        batch.bm.check()
+    assert batch.pool.errors() == 0
+    assert lens.tolist() == [int(x) + w.steps - 1 for x in inst.lens]
+
+
+def test_long_context_layers():
+    w = wl.WORKLOADS["long"]
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst, cpu_layers=[0, 31])
+    slots = batch.next_token_slots()
+    tables, lens = batch.tables(), batch.seq_lens()
+    for layer in (0, 31):
+        q, kn, vn = batch.step_inputs(layer)
+        pk.kv_append(batch.pool, layer, kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda())
+        out = pk.paged_decode_attention(q.cuda(), batch.pool, layer, tables.cuda(), lens.cuda(),
+                                        int(lens.max()), w.scale, split_tokens=w.split_tokens)
+        torch.cuda.synchronize()
+        ref, _ = oracle_reference(w, 1.0, 1.0, layer, q, tables, lens.tolist(), [0, 3])
+        compare(out[[0, 3]], ref, TOL["bf16"], "long layer %d" % layer)
+    assert batch.pool.errors() == 0
