@@ -68,13 +68,17 @@ def _profile_traffic(kernel_tag: str, src_hash: str):
     return None
 
 
-def _kernel_hash():
+KERNEL_SOURCES = {"simt": ("decode_simt.cu", "device_common.cuh", "pkv_internal.h"),
+                  "mma": ("decode_mma.cu", "device_common.cuh", "pkv_internal.h")}
+
+
+def kernel_hash(algo: str) -> str:
+    """sha256 (first 16 hex digits) of the sources of one kernel design."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_194_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+    for fn in KERNEL_SOURCES[algo]:
+        h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -138,7 +142,7 @@ class Clocks:
 def workload_bytes(w, lens):
     import torch
     kvb = {"f32": 4, "bf16": 2, "fp8": 1}[w.kv_dtype]
-    qb = 4 if w.in_dtype == "f32" else 2
+    qb = 4 if w.query_dtype == "f32" else 2
     sum_len = int(lens.sum())
     kv = sum_len * w.num_kv_heads * w.head_dim * 2 * kvb
     return sum_len, kv, qb, kvb
@@ -172,6 +176,7 @@ def run_ours(args):
     tables, lens = tables_h.to(dev), lens_h.to(dev)
     out = torch.empty_like(q)
     S, NS, wsb = pk.decode_plan(batch.pool, w.num_seqs, w.num_q_heads, max_len, args.split)
+    algo = pk.decode_algo(batch.pool, w.num_q_heads, args.algo)
     work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -230,7 +235,7 @@ def run_ours(args):
     value = ws * kv_bytes / (ms_step * 1e-3) / 1e9
     achieved = att_bytes / (att_ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
-    traffic = _profile_traffic("%s/%s/%s" % (args.workload, args.algo, w.kv_dtype), _kernel_hash())
+    traffic = _profile_traffic("%s/%s/%s" % (args.workload, algo, w.kv_dtype), kernel_hash(algo))
     launches = args.steps * (2 + (1 if NS > 1 else 0))
 
     # ---- end to end through the public API: pinned host buffers in, result out
@@ -271,11 +276,11 @@ def run_ours(args):
         "config": {"workload": "%s: %d seqs, lens %s, %dq/%dkv heads, head_dim %d, block %d, %s KV"
                    % (w.name, B, _lens_desc(w), Hq, Hkv, D, w.block_size, w.kv_dtype),
                    "sum_seq_len": sum_len, "kv_bytes_per_step": kv_bytes, "split_tokens": S,
-                   "num_splits": NS, "algo": args.algo, "parallelism": "replica per GPU" if ws > 1 else "1 GPU",
+                   "num_splits": NS, "algo": algo, "parallelism": "replica per GPU" if ws > 1 else "1 GPU",
                    "l2": "inputs exceed L2 (%.0f MB KV per step vs 129 MB L2); no flush" % (kv_bytes / 1e6)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "paged_decode_attention call (split kernel%s)" % (" + combine" if NS > 1 else ""),
+                     "kernel": "paged_decode_attention call (decode_%s_kernel%s)" % (algo, " + combine" if NS > 1 else ""),
                      "ms_per_launch": round(att_ms, 5), "bytes_per_launch": att_bytes,
                      "peak_kind": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
@@ -331,7 +336,7 @@ def cpu_baseline(w, inst, budget_s=15.0):
     reps, spent, threads = 0, 0.0, 0
     while spent < budget_s and reps < 50:
         t0 = time.perf_counter()
-        _, _, threads = oracle.paged_attention(q, w.in_dtype, pool, 0, t, l, w.scale, return_threads=True)
+        _, _, threads = oracle.paged_attention(q, w.query_dtype, pool, 0, t, l, w.scale, return_threads=True)
         spent += time.perf_counter() - t0
         reps += 1
     return {"value": round(reps * kv_bytes / spent / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
@@ -354,7 +359,7 @@ def run_reference(args):
     # calibrate on sequence 0
     pool, q, t, l = _oracle_sample(w, inst, [0])
     t0 = time.perf_counter()
-    oracle.paged_attention(q, w.in_dtype, pool, 0, t, l, w.scale)
+    oracle.paged_attention(q, w.query_dtype, pool, 0, t, l, w.scale)
     per_token = (time.perf_counter() - t0) / max(1, lens[0])
     want = max(16, int(args.ref_budget / (args.steps + args.warmup) / per_token))
     seqs, window, acc = [], 2**31 - 1, 0
@@ -368,11 +373,11 @@ def run_reference(args):
     pool, q, t, l = _oracle_sample(w, inst, seqs)
     kv_bytes = _kv_bytes(w, acc)
     for _ in range(args.warmup):
-        oracle.paged_attention(q, w.in_dtype, pool, 0, t, l, w.scale, window=(0, window))
+        oracle.paged_attention(q, w.query_dtype, pool, 0, t, l, w.scale, window=(0, window))
     threads = 0
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _, _, threads = oracle.paged_attention(q, w.in_dtype, pool, 0, t, l, w.scale, window=(0, window),
+        _, _, threads = oracle.paged_attention(q, w.query_dtype, pool, 0, t, l, w.scale, window=(0, window),
                                                return_threads=True)
     dt = (time.perf_counter() - t0) / max(1, args.steps)
     value = kv_bytes / dt / 1e9

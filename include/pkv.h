@@ -55,7 +55,8 @@ typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype
 /* Bits OR-ed into the pool's error word by the kernels. */
 #define PKV_ERRBIT_BLOCK_ID 1 /* block table entry outside [0, num_blocks) */
 #define PKV_ERRBIT_SLOT 2     /* slot_mapping entry outside [-1, num_blocks*block_size) */
-#define PKV_ERRBIT_SEQ_LEN 4  /* seq_lens entry < 0 or > max_blocks_per_seq*block_size */
+#define PKV_ERRBIT_SEQ_LEN 4  /* seq_lens entry < 0 or > max_seq_len of the call */
+#define PKV_ERRBIT_TIMEOUT 8  /* a bounded pipeline wait expired; that CTA skipped its output */
 
 /* Kernel design used by paged_decode_attention. */
 typedef enum pkv_algo {
@@ -166,6 +167,13 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
                                   float scale, int32_t split_tokens, pkv_algo algo,
                                   void* workspace, size_t workspace_bytes, void* out,
                                   void* stream);
+
+/* The kernel design paged_decode_attention would run for this pool, group
+ * size (num_q_heads / num_kv_heads) and request: PKV_ALGO_SIMT or
+ * PKV_ALGO_MMA, or -1 when the request cannot be served.  PKV_ALGO_AUTO picks
+ * MMA for BF16/FP8 pools with head_dim 128 and G in {1, 2, 4, 8} (when the
+ * driver provides TMA descriptors), SIMT otherwise. */
+int32_t paged_decode_algo(const pkv_pool* pool, int32_t group, pkv_algo requested);
 
 /* Human-readable name of a status. */
 const char* pkv_status_string(pkv_status status);

@@ -20,12 +20,13 @@ PKV_F32, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 ALGOS = {"auto": 0, "simt": 1, "mma": 2}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda error",
           5: "device bounds"}
-ERRBIT_BLOCK_ID, ERRBIT_SLOT, ERRBIT_SEQ_LEN = 1, 2, 4
+ERRBIT_BLOCK_ID, ERRBIT_SLOT, ERRBIT_SEQ_LEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("kv_pool_create", "kv_pool_destroy", "kv_pool_tensor_bytes", "kv_bytes_per_token",
-           "kv_append", "paged_decode_plan", "paged_decode_attention", "pkv_status_string",
-           "pkv_last_cuda_error")
+           "kv_append", "paged_decode_plan", "paged_decode_algo", "paged_decode_attention",
+           "pkv_status_string", "pkv_last_cuda_error")
+ALGO_NAMES = {1: "simt", 2: "mma"}
 
 
 class PkvError(RuntimeError):
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
     L.paged_decode_attention.argtypes = [P, c.c_int, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                          c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int, P,
                                          c.c_size_t, P, P]
+    L.paged_decode_algo.restype = c.c_int32
+    L.paged_decode_algo.argtypes = [P, c.c_int32, c.c_int]
     L.pkv_status_string.restype = c.c_char_p
     L.pkv_status_string.argtypes = [c.c_int]
     L.pkv_last_cuda_error.restype = c.c_char_p
@@ -191,6 +194,14 @@ def decode_plan(pool: KVPool, num_seqs: int, num_q_heads: int, max_seq_len: int,
                                    ctypes.byref(S), ctypes.byref(NS), ctypes.byref(ws)),
            "paged_decode_plan")
     return S.value, NS.value, ws.value
+
+
+def decode_algo(pool: KVPool, num_q_heads: int, algo: str = "auto") -> str:
+    """Name of the kernel design a call with this request would run."""
+    r = lib().paged_decode_algo(pool.handle, num_q_heads // pool.num_kv_heads, ALGOS[algo])
+    if r < 0:
+        raise PkvError(2, "paged_decode_algo")
+    return ALGO_NAMES[r]
 
 
 def workspace_for(pool: KVPool, num_seqs: int, num_q_heads: int, max_seq_len: int,

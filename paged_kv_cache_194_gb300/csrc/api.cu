@@ -25,6 +25,53 @@ pkv_status cuda_status(cudaError_t e) {
 }
 
 int g_sms[64] = {0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// TMA descriptors over the whole K and V pools, viewed as 2D tensors
+// [rows = layers*blocks*kv_heads*block_size][head_dim]; one box is one
+// (block, kv head) chunk of 64 BF16 or 128 E4M3 columns, 128-byte swizzled.
+bool ensure_tmaps(pkv_pool* p) {
+    if (p->tmap_state != 0) return p->tmap_state == 1;
+    p->tmap_state = -1;
+    const pkv_pool_desc& d = p->d;
+    if (d.kv_dtype != PKV_BF16 && d.kv_dtype != PKV_FP8_E4M3) return false;
+    const uint64_t rows = static_cast<uint64_t>(d.num_layers) * d.num_blocks * d.num_kv_heads * d.block_size;
+    if (rows > static_cast<uint64_t>(INT32_MAX)) return false;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const bool bf16 = d.kv_dtype == PKV_BF16;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim), rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * p->elem_bytes};
+    const cuuint32_t box[2] = {bf16 ? 64u : 128u, static_cast<cuuint32_t>(d.block_size)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    for (int i = 0; i < 2; ++i) {
+        CUresult r = enc(i == 0 ? &p->tmap_k : &p->tmap_v, dt, 2, i == 0 ? d.k_base : d.v_base, dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return false;
+    }
+    p->tmap_state = 1;
+    return true;
+}
 }  // namespace
 
 void set_last_error(cudaError_t e) {
@@ -100,8 +147,10 @@ pkv_status kv_pool_create(const pkv_pool_desc* d, pkv_pool** out) {
         ks = d->k_scale;
         vs = d->v_scale;
     }
-    pkv_pool* p = static_cast<pkv_pool*>(std::malloc(sizeof(pkv_pool)));
+    // CUtensorMap needs 64-byte alignment
+    pkv_pool* p = static_cast<pkv_pool*>(std::aligned_alloc(64, round_up(sizeof(pkv_pool), 64)));
     if (!p) return PKV_ERR_INVALID_ARG;
+    std::memset(p, 0, sizeof(pkv_pool));
     p->d = *d;
     p->d.k_scale = ks;
     p->d.v_scale = vs;
@@ -159,6 +208,18 @@ pkv_status paged_decode_plan(const pkv_pool* p, int32_t num_seqs, int32_t num_q_
     return PKV_OK;
 }
 
+int32_t paged_decode_algo(const pkv_pool* p, int32_t G, pkv_algo algo) {
+    if (!p || G < 1) return -1;
+    pkv_pool* mp = const_cast<pkv_pool*>(p);
+    const bool mma_ok = decode_mma_supported(p->d.kv_dtype, p->d.head_dim, G, p->d.block_size);
+    const bool simt_ok = decode_simt_supported(p->d.kv_dtype, p->d.head_dim, G);
+    if (algo == PKV_ALGO_MMA) return (mma_ok && ensure_tmaps(mp)) ? PKV_ALGO_MMA : -1;
+    if (algo == PKV_ALGO_SIMT) return simt_ok ? PKV_ALGO_SIMT : -1;
+    if (algo != PKV_ALGO_AUTO) return -1;
+    if (mma_ok && ensure_tmaps(mp)) return PKV_ALGO_MMA;
+    return simt_ok ? PKV_ALGO_SIMT : -1;
+}
+
 pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,
                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
                                   const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
@@ -181,11 +242,13 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
     const int G = num_q_heads / p->d.num_kv_heads;
 
     bool use_mma = false;
+    pkv_pool* mp = const_cast<pkv_pool*>(p);  // the handle caches its TMA descriptors
     if (algo == PKV_ALGO_MMA) {
         if (!decode_mma_supported(p->d.kv_dtype, p->d.head_dim, G, p->d.block_size)) return PKV_ERR_UNSUPPORTED;
+        if (!ensure_tmaps(mp)) return PKV_ERR_UNSUPPORTED;
         use_mma = true;
     } else if (algo == PKV_ALGO_AUTO) {
-        use_mma = decode_mma_supported(p->d.kv_dtype, p->d.head_dim, G, p->d.block_size);
+        use_mma = decode_mma_supported(p->d.kv_dtype, p->d.head_dim, G, p->d.block_size) && ensure_tmaps(mp);
     }
     if (!use_mma && !decode_simt_supported(p->d.kv_dtype, p->d.head_dim, G)) return PKV_ERR_UNSUPPORTED;
 
@@ -203,6 +266,7 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
     a.tables = block_tables;
     a.lens = seq_lens;
     a.err = p->d.error_word;
+    a.layer = layer;
     a.max_blocks = max_blocks_per_seq;
     a.max_len = max_seq_len;
     a.num_seqs = num_seqs;
@@ -223,7 +287,8 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
                                               round_up(rows * p->d.head_dim * sizeof(float), 256));
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = use_mma ? launch_decode_mma(p->d.kv_dtype, a, s) : launch_decode_simt(p->d.kv_dtype, a, s);
+    cudaError_t e = use_mma ? launch_decode_mma(p->d.kv_dtype, a, &p->tmap_k, &p->tmap_v, s)
+                            : launch_decode_simt(p->d.kv_dtype, a, s);
     if (e != cudaSuccess) return cuda_status(e);
     if (NS > 1) return cuda_status(launch_combine(q_dtype, a, s));
     return PKV_OK;

@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libpkv.so.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only; the driver is reached through the runtime)
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -15,6 +16,9 @@ struct pkv_pool {
     size_t layer_bytes;      // bytes of one layer of one pool tensor
     float k_inv_scale;       // binary32 1/k_scale (FP8 pools), else 1
     float v_inv_scale;
+    int tmap_state;          // 0: not encoded yet, 1: ready, -1: unavailable
+    CUtensorMap tmap_k;      // TMA descriptors of the whole K / V pool (2D: head_dim x rows)
+    CUtensorMap tmap_v;
 };
 
 namespace pkv {
@@ -41,6 +45,7 @@ struct DecodeArgs {
     float* o_part;            // [B][Hq][num_splits][D] fp32 (split partials)
     float* lse_part;          // [B][Hq][num_splits] log2-domain log-sum-exp
     int32_t* err;             // optional error word
+    int layer;
     int max_blocks;
     int max_len;              // host bound of seq_lens (<= max_blocks * block_size)
     int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
@@ -52,7 +57,8 @@ struct DecodeArgs {
 // Returns cudaErrorNotSupported when no kernel matches (dtype, D, G).
 cudaError_t launch_decode_simt(pkv_dtype kv, const DecodeArgs& a, cudaStream_t stream);
 bool decode_simt_supported(pkv_dtype kv, int head_dim, int group);
-cudaError_t launch_decode_mma(pkv_dtype kv, const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_mma(pkv_dtype kv, const DecodeArgs& a, const void* tmap_k, const void* tmap_v,
+                              cudaStream_t stream);
 bool decode_mma_supported(pkv_dtype kv, int head_dim, int group, int block_size);
 cudaError_t launch_combine(pkv_dtype q_dtype, const DecodeArgs& a, cudaStream_t stream);
 

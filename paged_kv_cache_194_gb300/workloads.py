@@ -54,7 +54,7 @@ class Workload:
     head_dim: int
     block_size: int
     kv_dtype: str            # pool storage: "f32" | "bf16" | "fp8"
-    in_dtype: str            # q and appended k/v: "f32" | "bf16"
+    in_dtype: str            # appended k/v (and q unless q_dtype is set): "f32" | "bf16"
     scale: float
     num_layers: int = 1
     lens: str = "fixed"      # "fixed" | "uniform" | "lognormal"
@@ -67,6 +67,11 @@ class Workload:
     pool_blocks: int = 0     # 0: 1.25x the blocks the batch needs over all steps
     split_tokens: int = 0    # 0: let the library choose
     steps: int = 1           # decode steps (each appends one token per sequence)
+    q_dtype: str = ""        # query dtype when it differs from in_dtype
+
+    @property
+    def query_dtype(self) -> str:
+        return self.q_dtype or self.in_dtype
 
     @property
     def group(self) -> int:
@@ -153,15 +158,15 @@ def query(w: Workload, layer: int = 0, step: int = 0) -> torch.Tensor:
     """q [B, Hq, D] in the workload's input dtype (CPU)."""
     g = _gen(w.seed, 3, layer, step)
     shape = (w.num_seqs, w.num_q_heads, w.head_dim)
-    return _draw(w, shape, g)
+    return _draw(w, shape, g, w.query_dtype)
 
 
-def _draw(w: Workload, shape, g: torch.Generator) -> torch.Tensor:
+def _draw(w: Workload, shape, g: torch.Generator, dtype: str = "") -> torch.Tensor:
     if w.dist == "uniform":
         x = torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0
     else:
         x = torch.randn(shape, generator=g, dtype=torch.float32)
-    return x.to(DTYPES[w.in_dtype])
+    return x.to(DTYPES[dtype or w.in_dtype])
 
 
 def seq_kv(w: Workload, layer: int, b: int, n_tokens: int, start: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:

@@ -46,7 +46,7 @@ def oracle_reference(w: wl.Workload, k_scale: float, v_scale: float, layer: int,
         oracle.kv_append(pool, 0, k, v, w.in_dtype, slots)
     qs = q[list(seqs)]
     sl = np.array([int(lens[b]) for b in seqs], dtype=np.int32)
-    out, lse = oracle.paged_attention(qs, w.in_dtype, pool, 0, sub, sl, w.scale)
+    out, lse = oracle.paged_attention(qs, w.query_dtype, pool, 0, sub, sl, w.scale)
     return out, lse
 
 

@@ -22,9 +22,9 @@ pytestmark = pytest.mark.gpu
 EDGE_LENS = (1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 300, 1000)
 
 
-def _w(name, G, Hkv, D, bs, kv, ind, lens, dist="normal", seed=21):
+def _w(name, G, Hkv, D, bs, kv, ind, lens, dist="normal", seed=21, qd=""):
     return wl.Workload(name, seed, len(lens), G * Hkv, Hkv, D, bs, kv, ind, 1.0 / math.sqrt(D),
-                       lens="fixed", fixed_lens=tuple(lens), dist=dist)
+                       lens="fixed", fixed_lens=tuple(lens), dist=dist, q_dtype=qd)
 
 
 SMALL = [
@@ -36,8 +36,8 @@ SMALL = [
     _w("bf16_g8_d64_bs32", 8, 2, 64, 32, "bf16", "bf16", (31, 32, 96)),
     _w("fp8_g4_d128_bs64", 4, 2, 128, 64, "fp8", "bf16", EDGE_LENS),
     _w("fp8_g2_d64_bs16", 2, 2, 64, 16, "fp8", "bf16", (3, 80, 129)),
-    _w("fp8_from_f32_g4", 4, 1, 128, 32, "fp8", "f32", (40, 100)),
-    _w("bf16_from_f32_g4", 4, 1, 128, 16, "bf16", "f32", (40, 100)),
+    _w("fp8_from_f32_g4", 4, 1, 128, 32, "fp8", "f32", (40, 100), qd="bf16"),
+    _w("bf16_from_f32_g4", 4, 1, 128, 16, "bf16", "f32", (40, 100), qd="bf16"),
     _w("f32_g4_d128_bs32", 4, 2, 128, 32, "f32", "f32", (1, 70, 190), dist="uniform"),
     _w("f32_g16_d64_bs16", 16, 1, 64, 16, "f32", "f32", (17, 99), dist="uniform"),
     _w("with_empty_seq", 4, 2, 128, 16, "bf16", "bf16", (0, 5, 0, 77)),
@@ -57,7 +57,10 @@ def _run_step(batch, layer=0, split=0, algo="auto", step=0):
 
 
 def _algos(w):
-    return ["simt"] if w.kv_dtype == "f32" else ["simt", "auto"]
+    """Every kernel design that serves the workload."""
+    if w.kv_dtype != "f32" and w.head_dim == 128 and w.group in (1, 2, 4, 8):
+        return ["simt", "mma"]
+    return ["simt"]
 
 
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
@@ -120,7 +123,7 @@ def test_append_skip_slot_and_bad_slot_flag():
 def test_single_token_is_exact():
     w = _w("len1", 4, 2, 128, 16, "bf16", "bf16", (1, 1, 1, 1))
     inst = wl.instance(w)
-    for algo in ("simt", "auto"):
+    for algo in ("simt", "mma"):
         batch = DecodeBatch(inst)
         q, tables, lens, out = _run_step(batch, algo=algo)
         _, kn, vn = batch.step_inputs(0)
@@ -128,45 +131,60 @@ def test_single_token_is_exact():
         assert torch.equal(out, want), algo
 
 
-def test_block_permutation_gives_identical_output():
-    w = SMALL[1]
+@pytest.mark.parametrize("algo", ["simt", "mma"])
+@pytest.mark.parametrize("idx", [1, 6], ids=["bf16", "fp8"])
+def test_block_permutation_gives_identical_output(idx, algo):
+    w = SMALL[idx]
     inst = wl.instance(w)
     batch = DecodeBatch(inst)
-    q, tables, lens, out = _run_step(batch)
+    q, tables, lens, out = _run_step(batch, algo=algo)
     perm = torch.randperm(inst.num_blocks, generator=torch.Generator().manual_seed(5))
-    pool2 = pk.KVPool(1, inst.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype)
+    pool2 = pk.KVPool(1, inst.num_blocks, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype,
+                      inst.k_scale, inst.v_scale)
     pool2.k[:, perm.cuda()] = batch.pool.k
     pool2.v[:, perm.cuda()] = batch.pool.v
     t2 = torch.where(tables >= 0, perm[tables.clamp(min=0).long()].to(torch.int32), tables)
-    out2 = pk.paged_decode_attention(q.cuda(), pool2, 0, t2.cuda(), lens.cuda(), int(lens.max()), w.scale)
+    out2 = pk.paged_decode_attention(q.cuda(), pool2, 0, t2.cuda(), lens.cuda(), int(lens.max()), w.scale,
+                                     algo=algo)
     assert torch.equal(out, out2)
 
 
-def test_split_equals_no_split():
+def test_auto_picks_tensor_cores_for_bf16_and_fp8():
+    for idx, want in ((1, "mma"), (6, "mma"), (3, "simt"), (0, "simt")):
+        w = SMALL[idx]
+        inst = wl.instance(w)
+        pool = pk.KVPool(1, 4, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype, inst.k_scale, inst.v_scale)
+        assert pk.decode_algo(pool, w.num_q_heads) == want, w.name
+
+
+@pytest.mark.parametrize("algo", ["simt", "mma"])
+def test_split_equals_no_split(algo):
     w = _w("splits", 4, 2, 128, 16, "bf16", "bf16", (3000, 1234, 64, 4096))
     inst = wl.instance(w)
     batch = DecodeBatch(inst)
-    q, tables, lens, out_split = _run_step(batch, split=64)
+    q, tables, lens, out_split = _run_step(batch, split=64, algo=algo)
     out_one = pk.paged_decode_attention(q.cuda(), batch.pool, 0, tables.cuda(), lens.cuda(), int(lens.max()),
-                                        w.scale, split_tokens=4096)
+                                        w.scale, split_tokens=4096, algo=algo)
     np.testing.assert_allclose(out_split.float().cpu().numpy(), out_one.float().cpu().numpy(), rtol=8e-3, atol=2e-3)
 
 
-def test_device_index_faults_are_flagged_not_fatal():
+@pytest.mark.parametrize("algo", ["simt", "mma"])
+def test_device_index_faults_are_flagged_not_fatal(algo):
     w = _w("faults", 4, 2, 128, 16, "bf16", "bf16", (40, 50))
     inst = wl.instance(w)
     batch = DecodeBatch(inst)
-    q, tables, lens, out = _run_step(batch)
+    q, tables, lens, out = _run_step(batch, algo=algo)
     assert batch.pool.errors() == 0
     bad = tables.clone()
     bad[1, 1] = inst.num_blocks  # one past the pool
-    pk.paged_decode_attention(q.cuda(), batch.pool, 0, bad.cuda(), lens.cuda(), int(lens.max()), w.scale)
+    pk.paged_decode_attention(q.cuda(), batch.pool, 0, bad.cuda(), lens.cuda(), int(lens.max()), w.scale, algo=algo)
     torch.cuda.synchronize()
     assert batch.pool.errors() & pk.ERRBIT_BLOCK_ID
     batch.pool.clear_errors()
     long_lens = lens.clone()
     long_lens[0] = int(lens.max()) + 5  # beyond max_seq_len given to the call
-    o3 = pk.paged_decode_attention(q.cuda(), batch.pool, 0, tables.cuda(), long_lens.cuda(), int(lens.max()), w.scale)
+    o3 = pk.paged_decode_attention(q.cuda(), batch.pool, 0, tables.cuda(), long_lens.cuda(), int(lens.max()), w.scale,
+                                   algo=algo)
     torch.cuda.synchronize()
     assert batch.pool.errors() & pk.ERRBIT_SEQ_LEN
     assert torch.isfinite(o3.float()).all()
