@@ -153,6 +153,7 @@ def run_ours(args):
     import torch.distributed as dist
 
     from paged_kv_cache_194_gb300 import binding as pk
+    from paged_kv_cache_194_gb300 import replicas
     from paged_kv_cache_194_gb300 import workloads as wl
     from paged_kv_cache_194_gb300.decode import DecodeBatch
 
@@ -161,7 +162,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     pk.lib()
-    w = wl.WORKLOADS[args.workload]
+    w = replicas.rank_workload(wl.WORKLOADS[args.workload], rank)
     if w.num_layers > 1:
         raise SystemExit("multi-layer workloads are parity cases, not bench lines")
     inst = wl.instance(w)
@@ -215,15 +216,13 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     clk = clocks.stop(t_begin, t_end)
-    ms_total = ev0.elapsed_time(ev1)
+    ms_total = replicas.max_over_ranks(ev0.elapsed_time(ev1), dev)
     att_ms = sum(a.elapsed_time(b) for a, b in att) / args.steps
-    if ws > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
     ms_step = ms_total / args.steps
 
     sum_len, kv_bytes, qb, kvb = workload_bytes(w, inst.lens)
+    all_kv_bytes = replicas.sum_over_ranks(kv_bytes, dev)
+    all_len = replicas.sum_over_ranks(sum_len, dev)
     B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     # algorithmic bytes of one attention call (split kernel + combine)
     blocks_read = int(((inst.lens.long() + w.block_size - 1) // w.block_size).sum())
@@ -232,7 +231,7 @@ def run_ours(args):
         nsplit = int(((inst.lens.long() + S - 1) // S).sum())
         part = 2 * nsplit * Hq * (D + 1) * 4  # partials written then read
     att_bytes = kv_bytes + B * Hq * D * qb * 2 + blocks_read * 4 + B * 4 + part
-    value = ws * kv_bytes / (ms_step * 1e-3) / 1e9
+    value = all_kv_bytes / (ms_step * 1e-3) / 1e9
     achieved = att_bytes / (att_ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
     traffic = _profile_traffic("%s/%s/%s" % (args.workload, algo, w.kv_dtype), kernel_hash(algo))
@@ -260,18 +259,14 @@ def run_ours(args):
         step()
         hout.copy_(out, non_blocking=True)
         stream.synchronize()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if ws > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = ws * kv_bytes / e2e_s / 1e9
+    e2e_s = replicas.max_over_ranks((time.perf_counter() - t0) / e2e_steps, dev)
+    e2e_value = all_kv_bytes / e2e_s / 1e9
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
-        "tokens_per_s": round(ws * sum_len / (ms_step * 1e-3), 1),
+        "tokens_per_s": round(all_len / (ms_step * 1e-3), 1),
         "decode_tokens_per_s_32_layers": round(ws * B / (ms_step * 1e-3 * LAYERS), 1),
         "config": {"workload": "%s: %d seqs, lens %s, %dq/%dkv heads, head_dim %d, block %d, %s KV"
                    % (w.name, B, _lens_desc(w), Hq, Hkv, D, w.block_size, w.kv_dtype),
