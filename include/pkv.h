@@ -168,6 +168,32 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
                                   void* workspace, size_t workspace_bytes, void* out,
                                   void* stream);
 
+/*
+ * paged_decode_attention without a caller-provided workspace, for callers that
+ * may not allocate device memory where they run decode attention (plug-ins
+ * whose device memory the host application plans once up front, loops that
+ * must never enter an allocator, fixed memory budgets).  The pages have no
+ * counterpart to this entry point; it is an interface convenience.
+ *
+ * Same arguments and results as paged_decode_attention, minus the workspace:
+ * the split-K partials go to a fixed device array owned by the library
+ * (PKV_STATIC_SCRATCH_BYTES; every GPU that loads the library holds it until
+ * the process exits).  Allocates nothing.  The first call that needs scratch
+ * on a device looks up the array's device address with that device current;
+ * make that first call before any stream capture.  A call whose plan needs
+ * more than PKV_STATIC_SCRATCH_BYTES (see paged_decode_plan) returns
+ * PKV_ERR_WORKSPACE before enqueuing anything.  All calls share the one
+ * array: calls that overlap on the GPU race and must be ordered by the
+ * caller.  No contents need clearing between calls.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (16 * 1024 * 1024)
+pkv_status paged_decode_attention_static_ws(const void* q, pkv_dtype q_dtype, const pkv_pool* pool,
+                                            int32_t layer, const int32_t* block_tables,
+                                            int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                            int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
+                                            float scale, int32_t split_tokens, pkv_algo algo, void* out,
+                                            void* stream);
+
 /* The kernel design paged_decode_attention would run for this pool, group
  * size (num_q_heads / num_kv_heads) and request: PKV_ALGO_SIMT or
  * PKV_ALGO_MMA, or -1 when the request cannot be served.  PKV_ALGO_AUTO picks

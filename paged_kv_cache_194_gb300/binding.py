@@ -25,7 +25,8 @@ ERRBIT_BLOCK_ID, ERRBIT_SLOT, ERRBIT_SEQ_LEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
 # Every symbol include/pkv.h declares.
 EXPORTS = ("kv_pool_create", "kv_pool_destroy", "kv_pool_tensor_bytes", "kv_bytes_per_token",
            "kv_append", "paged_decode_plan", "paged_decode_algo", "paged_decode_attention",
-           "pkv_status_string", "pkv_last_cuda_error")
+           "paged_decode_attention_static_ws", "pkv_status_string", "pkv_last_cuda_error")
+STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 ALGO_NAMES = {1: "simt", 2: "mma"}
 
 
@@ -76,6 +77,9 @@ def lib() -> ctypes.CDLL:
     L.paged_decode_attention.argtypes = [P, c.c_int, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                          c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int, P,
                                          c.c_size_t, P, P]
+    L.paged_decode_attention_static_ws.restype = c.c_int
+    L.paged_decode_attention_static_ws.argtypes = [P, c.c_int, P, c.c_int32, P, c.c_int32, P, c.c_int32,
+                                                   c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int, P, P]
     L.paged_decode_algo.restype = c.c_int32
     L.paged_decode_algo.argtypes = [P, c.c_int32, c.c_int]
     L.pkv_status_string.restype = c.c_char_p
@@ -230,4 +234,23 @@ def paged_decode_attention(q: torch.Tensor, pool: KVPool, layer: int, block_tabl
         block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Hq, max_seq_len, float(scale),
         split_tokens, ALGOS[algo], ws_ptr, ws_bytes, _dev(out, "out", q.dtype), _stream_ptr(stream))
     _check(rc, "paged_decode_attention")
+    return out
+
+
+def paged_decode_attention_static_ws(q: torch.Tensor, pool: KVPool, layer: int, block_tables: torch.Tensor,
+                                     seq_lens: torch.Tensor, max_seq_len: int, scale: float,
+                                     out: Optional[torch.Tensor] = None, split_tokens: int = 0,
+                                     algo: str = "auto", stream=None) -> torch.Tensor:
+    """paged_decode_attention whose split partials live in the library's own
+    fixed device array (no workspace argument; the call allocates nothing on
+    the device beyond `out` when `out` is not given).  Calls that overlap on
+    the GPU share that array and race."""
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib().paged_decode_attention_static_ws(
+        _dev(q, "q"), _dtype_code(q.dtype), pool.handle, layer, _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Hq, max_seq_len, float(scale),
+        split_tokens, ALGOS[algo], _dev(out, "out", q.dtype), _stream_ptr(stream))
+    _check(rc, "paged_decode_attention_static_ws")
     return out
