@@ -58,6 +58,29 @@ bool ensure_tmaps(pkv_pool* p) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const bool bf16 = d.kv_dtype == PKV_BF16;
+    if (bf16 && d.head_dim == 128) {
+        // One box per (block, kv head): dims {64 columns, rows, 2 halves} with
+        // the half stride (128 B) inside the row stride (256 B), so the box
+        // lands as [half][bs rows][128 B].
+        const cuuint64_t dims3[3] = {64, rows, 2};
+        const cuuint64_t strides3[2] = {256, 128};
+        const cuuint32_t box3[3] = {64, static_cast<cuuint32_t>(d.block_size), 2};
+        const cuuint32_t estr3[3] = {1, 1, 1};
+        bool ok3 = true;
+        for (int i = 0; i < 2 && ok3; ++i) {
+            CUresult r = enc(i == 0 ? &p->tmap_k : &p->tmap_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                             i == 0 ? d.k_base : d.v_base, dims3, strides3, box3, estr3,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            ok3 = r == CUDA_SUCCESS;
+        }
+        if (ok3) {
+            p->tmap_3d = 1;
+            p->tmap_state = 1;
+            return true;
+        }
+    }
+    p->tmap_3d = 0;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim), rows};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * p->elem_bytes};
     const cuuint32_t box[2] = {bf16 ? 64u : 128u, static_cast<cuuint32_t>(d.block_size)};
@@ -186,11 +209,11 @@ pkv_status paged_decode_plan(const pkv_pool* p, int32_t num_seqs, int32_t num_q_
     if (S > 0) {
         if (S % kTileTokens != 0 || S % p->d.block_size != 0) return PKV_ERR_INVALID_ARG;
     } else {
-        // Auto: 512-token splits, halved (down to one tile) while the batch
+        // Auto: 1024-token splits, halved (down to one tile) while the batch
         // would give fewer than two CTAs per SM.
         const int sms = num_sms() > 0 ? num_sms() : 148;
         const int64_t pairs = static_cast<int64_t>(num_seqs) * p->d.num_kv_heads;
-        S = 512;
+        S = 1024;
         while (S > kTileTokens && pairs * ((max_seq_len + S - 1) / S) < 2LL * sms) S /= 2;
         if (S % p->d.block_size != 0) S = p->d.block_size > kTileTokens ? p->d.block_size : kTileTokens;
     }
@@ -267,6 +290,7 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
     a.lens = seq_lens;
     a.err = p->d.error_word;
     a.layer = layer;
+    a.tma_3d = p->tmap_3d;
     a.max_blocks = max_blocks_per_seq;
     a.max_len = max_seq_len;
     a.num_seqs = num_seqs;

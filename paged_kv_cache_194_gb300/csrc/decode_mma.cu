@@ -9,9 +9,11 @@
 //
 // CTA = one (split, KV head, sequence); 4 consumer warps + 1 producer warp.
 //  * Producer: one lane walks the block table and issues, per 64-token stage,
-//    one TMA tile load (cp.async.bulk.tensor, 128-byte swizzle) per
-//    (block, 64-column half) of K and of V into the stage; a full mbarrier
-//    counts the bytes, an empty mbarrier (4 arrivals) frees the stage.
+//    one TMA tile load (cp.async.bulk.tensor, 128-byte swizzle) per block of
+//    K and of V into the stage: for BF16 a 3D box {64 columns, bs rows,
+//    2 halves} fetches the block's whole 256-byte rows at once (two 2D boxes
+//    if the driver refuses that descriptor); a full mbarrier counts the
+//    bytes, an empty mbarrier (4 arrivals) frees the stage.
 //    Every KV byte crosses HBM once; the G query heads of the KV head share it.
 //  * Consumer warp w owns tokens [16w, 16w+16) of each stage:
 //      S^T[16 tok x 8] = K[16 x 128] . Q^T[128 x 8]   8 x mma.m16n8k16
@@ -58,6 +60,10 @@ struct MmaCfg<PKV_FP8_E4M3> {
     static constexpr int kStages = 5;
 };
 
+// Stage layout of one tensor (K or V): [block of the tile][half][bs rows][128 B].
+// A block's two halves (head_dim 0-63 and 64-127 for BF16) are bs*128 bytes
+// apart; both start on 1024-byte boundaries (bs >= 16), so the 128-byte
+// swizzle phase of a row is its row index within the block, mod 8.
 constexpr int kHalfBytes = kTT * kBoxRowBytes;  // 8 KB: 64 rows x 128 B
 template <int DT>
 constexpr int tensor_stage_bytes() { return MmaCfg<DT>::kHalves * kHalfBytes; }
@@ -108,6 +114,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
@@ -172,10 +184,11 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
     return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
 }
 
-// Byte offset of 16-byte chunk `chunk` of row `row` in a 128B-swizzled box
-// whose base is 1024-byte aligned.
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return static_cast<uint32_t>(row * kBoxRowBytes + ((chunk ^ (row & 7)) << 4));
+// Byte offset of 16-byte chunk `chunk` of row `lr` inside a 128B-swizzled run
+// of rows whose first row sits on a 1024-byte boundary (and is a multiple of 8
+// rows into the run).
+__device__ __forceinline__ uint32_t swz(int lr, int chunk) {
+    return static_cast<uint32_t>(lr * kBoxRowBytes + ((chunk ^ (lr & 7)) << 4));
 }
 
 // Head-dim index held by O^T accumulator row `m` (0..15) of m-tile `mt`.
@@ -271,11 +284,16 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 }
                 if (lane == 0) {
                     const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + h) * bs);
-                    for (int hf = 0; hf < kHalves; ++hf) {
-                        const uint32_t off = hf * kHalfBytes + k * bs * kBoxRowBytes;
-                        const int x = hf * (DT == PKV_BF16 ? 64 : 128);
-                        tma_load_2d(smem_u32(kst + off), &tmk, x, y, smem_u32(&full[s]));
-                        tma_load_2d(smem_u32(vst + off), &tmv, x, y, smem_u32(&full[s]));
+                    const uint32_t off = k * kHalves * bs * kBoxRowBytes;
+                    if (kHalves == 2 && a.tma_3d) {  // one box: both 128-byte halves of every row
+                        tma_load_3d(smem_u32(kst + off), &tmk, 0, y, 0, smem_u32(&full[s]));
+                        tma_load_3d(smem_u32(vst + off), &tmv, 0, y, 0, smem_u32(&full[s]));
+                    } else {
+                        for (int hf = 0; hf < kHalves; ++hf) {
+                            const uint32_t o2 = off + hf * bs * kBoxRowBytes;
+                            tma_load_2d(smem_u32(kst + o2), &tmk, hf * 64, y, smem_u32(&full[s]));
+                            tma_load_2d(smem_u32(vst + o2), &tmv, hf * 64, y, smem_u32(&full[s]));
+                        }
                     }
                 }
             }
@@ -323,6 +341,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     const int row0 = warp * 16;
     const float qk = a.qk_scale_log2;
+    const int bsz = a.block_size;
+    const uint32_t half_stride = static_cast<uint32_t>(bsz * kBoxRowBytes);
+    // this warp's 16 rows: block row0/bs of the tile, rows row0%bs.. of it
+    const uint32_t warp_base = static_cast<uint32_t>((row0 / bsz) * kHalves * bsz * kBoxRowBytes +
+                                                     (row0 % bsz) * kBoxRowBytes);
     bool aborted = false;
 
     for (int tile = 0; tile < num_tiles; ++tile) {
@@ -341,25 +364,25 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (row0 < n) {
             if (n < row0 + 16) {  // zero this warp's V rows past the end
                 for (int i = lane; i < 16 * kHalves * 8; i += 32) {
-                    const int row = row0 + i / (kHalves * 8);
+                    const int lr = i / (kHalves * 8);
                     const int rest = i % (kHalves * 8);
-                    if (row >= n)
-                        *reinterpret_cast<uint4*>(vst + (rest >> 3) * kHalfBytes + row * kBoxRowBytes + (rest & 7) * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
+                    if (row0 + lr >= n)
+                        *reinterpret_cast<uint4*>(vst + warp_base + (rest >> 3) * half_stride + lr * kBoxRowBytes +
+                                                  (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async();
                 __syncwarp();
             }
             // ---- S^T = K Q^T
             float sc[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint32_t kb = smem_u32(kst);
-            const int lrow = row0 + (lane & 7) + ((lane >> 3) & 1) * 8;  // row this lane addresses
+            const uint32_t kb = smem_u32(kst) + warp_base;
+            const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // row (of the warp's 16) this lane addresses
             if constexpr (DT == PKV_BF16) {
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const int chunk = 2 * (ks & 3) + (lane >> 4);
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kb + (ks >> 2) * kHalfBytes + swz(lrow, chunk), a0, a1, a2, a3);
+                    ldsm_x4(kb + (ks >> 2) * half_stride + swz(lrow, chunk), a0, a1, a2, a3);
                     mma16816<DT>(sc, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
                 }
             } else {
@@ -404,18 +427,18 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             const uint32_t pb0 = movmatrix_t(pack2<DT>(p0, p1));  // tokens 0-7 of the warp's 16
             const uint32_t pb1 = movmatrix_t(pack2<DT>(p2, p3));  // tokens 8-15
             // ---- O^T += V^T P^T
-            const uint32_t vb_ = smem_u32(vst);
+            const uint32_t vb_ = smem_u32(vst) + warp_base;
             if constexpr (DT == PKV_BF16) {
-                const int trow = row0 + (lane & 7) + ((lane >> 4) & 1) * 8;
+                const int trow = (lane & 7) + ((lane >> 4) & 1) * 8;
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     const int chunk = 2 * (mt & 3) + ((lane >> 3) & 1);
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(vb_ + (mt >> 2) * kHalfBytes + swz(trow, chunk), a0, a1, a2, a3);
+                    ldsm_x4_t(vb_ + (mt >> 2) * half_stride + swz(trow, chunk), a0, a1, a2, a3);
                     mma16816<DT>(o[mt], a0, a1, a2, a3, pb0, pb1);
                 }
             } else {
-                const int ta = row0 + 2 * q;  // tokens ta, ta+1, ta+8, ta+9
+                const int ta = 2 * q;  // the warp's rows ta, ta+1, ta+8, ta+9
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int chunk = 2 * j + (r >> 2);

@@ -17,6 +17,7 @@ struct pkv_pool {
     float k_inv_scale;       // binary32 1/k_scale (FP8 pools), else 1
     float v_inv_scale;
     int tmap_state;          // 0: not encoded yet, 1: ready, -1: unavailable
+    int tmap_3d;             // BF16: 1 = one 3D box per block row pair, 0 = two 2D boxes
     CUtensorMap tmap_k;      // TMA descriptors of the whole K / V pool (2D: head_dim x rows)
     CUtensorMap tmap_v;
 };
@@ -46,6 +47,7 @@ struct DecodeArgs {
     float* lse_part;          // [B][Hq][num_splits] log2-domain log-sum-exp
     int32_t* err;             // optional error word
     int layer;
+    int tma_3d;               // TMA descriptor kind (see pkv_pool::tmap_3d)
     int max_blocks;
     int max_len;              // host bound of seq_lens (<= max_blocks * block_size)
     int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
