@@ -178,7 +178,8 @@ def run_ours(args):
     out = torch.empty_like(q)
     S, NS, wsb = pk.decode_plan(batch.pool, w.num_seqs, w.num_q_heads, max_len, args.split)
     algo = pk.decode_algo(batch.pool, w.num_q_heads, args.algo)
-    work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    schedule = "balanced" if (algo == "mma" and args.split == 0) else "fixed splits"
+    work = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -227,7 +228,7 @@ def run_ours(args):
     # algorithmic bytes of one attention call (split kernel + combine)
     blocks_read = int(((inst.lens.long() + w.block_size - 1) // w.block_size).sum())
     part = 0
-    if NS > 1:
+    if schedule != "balanced" and NS > 1:
         nsplit = int(((inst.lens.long() + S - 1) // S).sum())
         part = 2 * nsplit * Hq * (D + 1) * 4  # partials written then read
     att_bytes = kv_bytes + B * Hq * D * qb * 2 + blocks_read * 4 + B * 4 + part
@@ -235,7 +236,8 @@ def run_ours(args):
     achieved = att_bytes / (att_ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
     traffic = _profile_traffic("%s/%s/%s" % (args.workload, algo, w.kv_dtype), kernel_hash(algo))
-    launches = args.steps * (2 + (1 if NS > 1 else 0))
+    combine = schedule != "balanced" and NS > 1
+    launches = args.steps * (2 + (1 if combine else 0))
 
     # ---- end to end through the public API: pinned host buffers in, result out
     pin = lambda t: t.pin_memory()
@@ -271,11 +273,11 @@ def run_ours(args):
         "config": {"workload": "%s: %d seqs, lens %s, %dq/%dkv heads, head_dim %d, block %d, %s KV"
                    % (w.name, B, _lens_desc(w), Hq, Hkv, D, w.block_size, w.kv_dtype),
                    "sum_seq_len": sum_len, "kv_bytes_per_step": kv_bytes, "split_tokens": S,
-                   "num_splits": NS, "algo": algo, "parallelism": "replica per GPU" if ws > 1 else "1 GPU",
+                   "num_splits": NS if schedule != "balanced" else None, "schedule": schedule, "algo": algo, "parallelism": "replica per GPU" if ws > 1 else "1 GPU",
                    "l2": "inputs exceed L2 (%.0f MB KV per step vs 129 MB L2); no flush" % (kv_bytes / 1e6)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "paged_decode_attention call (decode_%s_kernel%s)" % (algo, " + combine" if NS > 1 else ""),
+                     "kernel": "paged_decode_attention call (decode_%s_kernel%s)" % (algo, " + combine" if combine else ""),
                      "ms_per_launch": round(att_ms, 5), "bytes_per_launch": att_bytes,
                      "peak_kind": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},

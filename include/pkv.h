@@ -125,13 +125,14 @@ pkv_status kv_append(const pkv_pool* pool, int32_t layer, const void* k, const v
 
 /*
  * Split planning for paged_decode_attention.  Flash-decoding splits each
- * sequence's tokens into chunks of `split_tokens` (0 = choose automatically
- * from the batch shape and the GPU's SM count), attends to each chunk in its
- * own CTA and merges the partial results by their log-sum-exp.  Outputs (any
- * may be NULL): the split size actually used, the number of splits of the
- * longest sequence, and the workspace bytes the call needs (0 when a single
- * split covers max_seq_len).  split_tokens, when given, must be a positive
- * multiple of 64 and of block_size.
+ * sequence's tokens into chunks, attends to each chunk in its own CTA and
+ * merges the partial results by their log-sum-exp.  Outputs (any may be
+ * NULL): the fixed split size a fixed-split call uses (split_tokens, or the
+ * automatic choice from the batch shape and the SM count when it is 0), the
+ * number of such splits of the longest sequence, and the workspace bytes the
+ * call needs whichever schedule it runs (0 only for a fixed-split call whose
+ * single split covers max_seq_len).  split_tokens, when given, must be a
+ * positive multiple of 64 and of block_size.
  */
 pkv_status paged_decode_plan(const pkv_pool* pool, int32_t num_seqs, int32_t num_q_heads,
                              int32_t max_seq_len, int32_t split_tokens, int32_t* split_tokens_out,
@@ -154,9 +155,20 @@ pkv_status paged_decode_plan(const pkv_pool* pool, int32_t num_seqs, int32_t num
  *                 <= max_blocks_per_seq * block_size.  Longer device lengths
  *                 are clamped to it and flagged PKV_ERRBIT_SEQ_LEN.
  *   workspace     device scratch of at least the planned bytes (may be NULL
- *                 when the plan needs none); its contents on entry do not
- *                 matter.  Calls that share a workspace must be stream-ordered.
+ *                 when the plan needs none).  Its first 4*num_seqs*num_kv_heads
+ *                 bytes (rounded up to 256) are per-(sequence, KV head)
+ *                 counters that must be zero before the first call; every
+ *                 call leaves them zero again (a call that reports
+ *                 PKV_ERRBIT_TIMEOUT may not: clear them then).  The rest is
+ *                 overwritten.  Calls that share a workspace must be
+ *                 stream-ordered.
  *   out           device [num_seqs][num_q_heads][head_dim] in q_dtype.
+ *   split_tokens  0: the tensor-core design balances the batch itself (a
+ *                 persistent grid of 2 CTAs per SM, each streaming an equal
+ *                 share of the (sequence, KV head, 64-token tile) list, with
+ *                 an in-kernel log-sum-exp merge of shared sequences); the
+ *                 SIMT design picks a split size.  > 0: fixed splits of that
+ *                 many tokens and a separate combine kernel.
  *   algo          PKV_ALGO_AUTO, or a specific kernel design.
  * Softmax and accumulation are fp32; the output is rounded to q_dtype (RN).
  */

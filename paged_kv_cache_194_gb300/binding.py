@@ -213,7 +213,8 @@ def workspace_for(pool: KVPool, num_seqs: int, num_q_heads: int, max_seq_len: in
     _, _, ws = decode_plan(pool, num_seqs, num_q_heads, max_seq_len, split_tokens)
     if ws == 0:
         return None
-    return torch.empty(ws, dtype=torch.uint8, device=pool.k.device)
+    # the leading per-sequence counters must start at zero
+    return torch.zeros(ws, dtype=torch.uint8, device=pool.k.device)
 
 
 def paged_decode_attention(q: torch.Tensor, pool: KVPool, layer: int, block_tables: torch.Tensor,

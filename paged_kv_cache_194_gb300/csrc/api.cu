@@ -26,6 +26,23 @@ pkv_status cuda_status(cudaError_t e) {
 
 int g_sms[64] = {0};
 
+// Balanced persistent schedule: at most this many sequences (each CTA scans
+// the lengths once), at most kBalCtasPerSm CTAs per SM.
+constexpr int kMaxBalancedSeqs = 4096;
+constexpr int kBalCtasPerSm = 2;
+
+size_t counters_bytes(int B, int Hkv) { return round_up(static_cast<size_t>(B) * Hkv * sizeof(int32_t), 256); }
+size_t fixed_bytes(int B, int Hq, int D, int64_t ns) {
+    if (ns <= 1) return 0;
+    const size_t rows = static_cast<size_t>(B) * Hq * ns;
+    return round_up(rows * D * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+}
+int bal_ctas() { return (num_sms() > 0 ? num_sms() : 148) * kBalCtasPerSm; }
+size_t bal_o_bytes(int ctas, int G, int D) { return round_up(static_cast<size_t>(ctas) * 2 * G * D * sizeof(float), 256); }
+size_t bal_bytes(int ctas, int G, int D) {
+    return bal_o_bytes(ctas, G, D) + round_up(static_cast<size_t>(ctas) * 2 * G * sizeof(float), 256);
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -220,11 +237,14 @@ pkv_status paged_decode_plan(const pkv_pool* p, int32_t num_seqs, int32_t num_q_
     int64_t ns = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + S - 1) / S : 1;
     if (ns < 1) ns = 1;
     if (ns > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-    size_t ws = 0;
-    if (ns > 1) {
-        const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * ns;
-        ws = round_up(rows * p->d.head_dim * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+    // layout: [counters][partials of whichever schedule the call runs]
+    size_t body = fixed_bytes(num_seqs, num_q_heads, p->d.head_dim, ns);
+    const int G = num_q_heads / p->d.num_kv_heads;
+    if (split_tokens == 0 && num_seqs <= kMaxBalancedSeqs) {
+        const size_t bb = bal_bytes(bal_ctas(), G, p->d.head_dim);
+        if (bb > body) body = bb;
     }
+    size_t ws = body > 0 ? counters_bytes(num_seqs, p->d.num_kv_heads) + body : 0;
     if (split_out) *split_out = S;
     if (nsplit_out) *nsplit_out = static_cast<int32_t>(ns);
     if (ws_out) *ws_out = ws;
@@ -301,20 +321,29 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
     a.num_blocks = p->d.num_blocks;
     a.split_tokens = S;
     a.num_splits = NS;
+    const bool balanced = use_mma && split_tokens == 0 && num_seqs <= kMaxBalancedSeqs;
     const float log2e = 1.4426950408889634f;
     a.qk_scale_log2 = scale * p->d.k_scale * log2e;
     a.v_scale = p->d.v_scale;
-    if (NS > 1) {
-        const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * NS;
-        a.o_part = static_cast<float*>(workspace);
-        a.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                              round_up(rows * p->d.head_dim * sizeof(float), 256));
+    if (need > 0) {
+        uint8_t* w = static_cast<uint8_t*>(workspace);
+        a.counters = reinterpret_cast<int32_t*>(w);
+        uint8_t* body = w + counters_bytes(num_seqs, p->d.num_kv_heads);
+        if (balanced) {
+            a.bal_max_ctas = bal_ctas();
+            a.bal_o = reinterpret_cast<float*>(body);
+            a.bal_lse = reinterpret_cast<float*>(body + bal_o_bytes(a.bal_max_ctas, G, p->d.head_dim));
+        } else if (NS > 1) {
+            const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * NS;
+            a.o_part = reinterpret_cast<float*>(body);
+            a.lse_part = reinterpret_cast<float*>(body + round_up(rows * p->d.head_dim * sizeof(float), 256));
+        }
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = use_mma ? launch_decode_mma(p->d.kv_dtype, a, &p->tmap_k, &p->tmap_v, s)
                             : launch_decode_simt(p->d.kv_dtype, a, s);
     if (e != cudaSuccess) return cuda_status(e);
-    if (NS > 1) return cuda_status(launch_combine(q_dtype, a, s));
+    if (!balanced && NS > 1) return cuda_status(launch_combine(q_dtype, a, s));
     return PKV_OK;
 }
 

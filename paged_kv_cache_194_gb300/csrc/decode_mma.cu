@@ -4,17 +4,30 @@
 // "How does TensorRT-LLM work?", "Custom attention kernels": one kernel does
 // the whole attention step and keeps the intermediate scores on chip.
 // "Introduction to TensorRT-LLM", figure "TensorRT-LLM Acceleration Stack":
-// Flash-Decoding splits the key/value length across CTAs; the log-sum-exp
-// merge of the splits runs in the combine kernel.
+// Flash-Decoding splits the key/value length across CTAs and merges the
+// pieces by their log-sum-exp.
 //
-// CTA = one (split, KV head, sequence); 4 consumer warps + 1 producer warp.
+// Work is a list of 64-token tiles of (sequence, KV head) pairs.  Two
+// schedules share the same producer and consumer code:
+//  * balanced (the default): a persistent grid of 2 CTAs per SM; CTA c takes
+//    the contiguous tile range [c*T/P, (c+1)*T/P) of the flattened list
+//    (T tiles, P CTAs), so every CTA streams the same number of KV bytes
+//    whatever the length mix.  A (sequence, KV head) whose tiles straddle
+//    CTAs leaves one fp32 partial per CTA; the CTA that finishes that pair
+//    last (an atomic counter in the workspace, no waiting) merges the
+//    partials by their log-sum-exp and writes the output.
+//  * fixed splits (when the caller names a split size): one CTA per
+//    (split, KV head, sequence); partials go to the combine kernel.
+// CTA = 4 consumer warps + 1 producer warp.
 //  * Producer: one lane walks the block table and issues, per 64-token stage,
 //    one TMA tile load (cp.async.bulk.tensor, 128-byte swizzle) per block of
-//    K and of V into the stage: for BF16 a 3D box {64 columns, bs rows,
-//    2 halves} fetches the block's whole 256-byte rows at once (two 2D boxes
-//    if the driver refuses that descriptor); a full mbarrier counts the
-//    bytes, an empty mbarrier (4 arrivals) frees the stage.
-//    Every KV byte crosses HBM once; the G query heads of the KV head share it.
+//    K and of V: for BF16 a 3D box {64 columns, bs rows, 2 halves} fetches a
+//    block's whole 256-byte rows at once (two 2D boxes if the driver refuses
+//    that descriptor).  At the first tile of a segment it also bulk-copies the
+//    G query rows into the stage.  A full mbarrier counts the bytes, an empty
+//    mbarrier (4 arrivals) frees the stage; a per-stage TileInfo tells the
+//    consumers what the stage holds and marks the CTA's last tile.
+//    Every KV byte crosses HBM once; the G query heads of a KV head share it.
 //  * Consumer warp w owns tokens [16w, 16w+16) of each stage:
 //      S^T[16 tok x 8] = K[16 x 128] . Q^T[128 x 8]   8 x mma.m16n8k16
 //      (tokens fill M; the G query heads fill N, padded to 8)
@@ -28,8 +41,8 @@
 //    permuted consistently in K and Q (a dot product does not depend on the
 //    order of its terms); V^T pairs two tokens' bytes with one byte_perm.
 //    Q is converted from BF16 to f16 (exact for |q| in [2^-14, 65504]).
-//  * The 4 warps' (m, l, O) are merged through shared memory at the end; the
-//    CTA writes the final row (one split) or fp32 partials + log2-sum-exp.
+//  * At a segment's end the 4 warps' (m, l, O) are merged through shared
+//    memory and the CTA writes the final row or its fp32 partial.
 // Rows past the sequence end inside a loaded block are masked in S and zeroed
 // in V (uninitialised pool bytes could hold NaN patterns, and 0 * NaN = NaN).
 // Every mbarrier wait is bounded; on expiry the CTA flags PKV_ERRBIT_TIMEOUT,
@@ -45,43 +58,62 @@ constexpr int kCWarps = 4;
 constexpr int kMmaThreads = (kCWarps + 1) * 32;
 constexpr int kTT = kTileTokens;           // tokens per stage (16 per consumer warp)
 constexpr int kBoxRowBytes = 128;          // one swizzled TMA row
+constexpr int kHalfBytes = kTT * kBoxRowBytes;
+constexpr int kD = 128;                    // head_dim served by this design
 constexpr uint32_t kSpinLimit = 1u << 22;  // try_wait polls before a wait gives up
 
 template <int DT>
 struct MmaCfg;
 template <>
 struct MmaCfg<PKV_BF16> {
-    static constexpr int kHalves = 2;  // 128 columns = two 64-column (128-byte) boxes
+    static constexpr int kHalves = 2;  // 128 columns = two 64-column (128-byte) halves
     static constexpr int kStages = 3;
 };
 template <>
 struct MmaCfg<PKV_FP8_E4M3> {
-    static constexpr int kHalves = 1;  // 128 one-byte columns = one 128-byte box
-    static constexpr int kStages = 5;
+    static constexpr int kHalves = 1;  // 128 one-byte columns = one 128-byte row
+    static constexpr int kStages = 6;
 };
 
-// Stage layout of one tensor (K or V): [block of the tile][half][bs rows][128 B].
-// A block's two halves (head_dim 0-63 and 64-127 for BF16) are bs*128 bytes
-// apart; both start on 1024-byte boundaries (bs >= 16), so the 128-byte
-// swizzle phase of a row is its row index within the block, mod 8.
-constexpr int kHalfBytes = kTT * kBoxRowBytes;  // 8 KB: 64 rows x 128 B
-template <int DT>
-constexpr int tensor_stage_bytes() { return MmaCfg<DT>::kHalves * kHalfBytes; }
-template <int DT>
-constexpr int stage_bytes() { return 2 * tensor_stage_bytes<DT>(); }
+// What one pipeline stage holds.
+struct TileInfo {
+    int b, h;       // sequence, KV head
+    int tok0, n;    // first token of the tile, valid tokens in it (1..64)
+    int flags;      // kSeg* / kEnd bits
+    int pieces;     // CTAs that share this (sequence, KV head)
+    int c_first;    // the first of them
+    int s_first;    // partial slot that first CTA uses
+};
+constexpr int kSegFirst = 1;  // first tile of a segment (load q, reset state)
+constexpr int kSegLast = 2;   // last tile of a segment (merge and emit)
+constexpr int kSegWhole = 4;  // the segment is the whole sequence
+constexpr int kCtaFirst = 8;  // the segment holds the CTA's first tile
+constexpr int kEnd = 16;      // no tiles at all (a CTA that owns none)
+constexpr int kCtaLast = 32;  // the CTA's last tile
 
-constexpr int kMergeStride = 128 + 4;  // padded d stride of the merge buffer
-constexpr int kMergeBytes = (kCWarps * 8 * kMergeStride + 2 * kCWarps * 8) * 4;
-
-template <int DT>
-constexpr size_t body_bytes() {
-    const size_t st = static_cast<size_t>(MmaCfg<DT>::kStages) * stage_bytes<DT>();
-    return st > kMergeBytes ? st : kMergeBytes;
-}
-template <int DT>
-constexpr size_t mma_smem_bytes() {
-    return 1024 /* alignment slack */ + body_bytes<DT>() + 2 * MmaCfg<DT>::kStages * 8 + 16;
-}
+// Shared memory of one CTA:
+//   stages: [kStages][K, V][block of the tile][half][bs rows][128 B]
+//     A block's two halves (head_dim 0-63 and 64-127 for BF16) are bs*128
+//     bytes apart; both start on 1024-byte boundaries (bs >= 16), so the
+//     128-byte swizzle phase of a row is its row index within the block, mod 8.
+//   q slots [kStages][G][128] BF16, tile info [kStages],
+//   merge area [warp][G][128] O + [warp][G] m, l, + one flag word,
+//   barriers full[kStages], empty[kStages], consumer sync, abort word.
+template <int DT, int G>
+struct Layout {
+    static constexpr int kHalves = MmaCfg<DT>::kHalves;
+    static constexpr int kStages = MmaCfg<DT>::kStages;
+    static constexpr int kTensorBytes = kHalves * kHalfBytes;
+    static constexpr int kStageBytes = 2 * kTensorBytes;
+    static constexpr int kQBytes = G * kD * 2;
+    static constexpr size_t kQOff = static_cast<size_t>(kStages) * kStageBytes;
+    static constexpr size_t kInfoOff = kQOff + static_cast<size_t>(kStages) * kQBytes;
+    static constexpr size_t kMergeOff = kInfoOff + static_cast<size_t>(kStages) * sizeof(TileInfo);
+    static constexpr size_t kMergeBytes = (static_cast<size_t>(kCWarps) * G * (kD + 2) + 4) * 4;
+    static constexpr size_t kBarOff = (kMergeOff + kMergeBytes + 15) / 16 * 16;
+    static constexpr size_t kBytes = kBarOff + (2 * kStages + 1) * 8 + 16;
+    static constexpr size_t kAlloc = kBytes + 1024;  // + alignment slack
+};
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -122,8 +154,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(kCWarps * 32) : "memory"); }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -202,45 +238,322 @@ __device__ __forceinline__ int o_dim(int mt, int m) {
     }
 }
 
+// ---------------------------------------------------------------- consumers
+template <int DT>
+struct Acc {
+    float m0, m1, l0, l1;  // running max (log2 domain) and lane-partial sums, heads 2q and 2q+1
+    float o[8][4];         // O^T accumulator fragments
+    uint32_t bq[8][2];     // Q^T as the mma B operand
+};
+
+// Start a segment: clear the state and build the Q^T fragments from the
+// stage's query rows qs[G][128] (BF16, shared memory).
 template <int DT, int G>
+__device__ __forceinline__ void acc_begin(Acc<DT>& s, const __nv_bfloat16* qs, int lane) {
+    s.m0 = s.m1 = -INFINITY;
+    s.l0 = s.l1 = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) s.o[mt][0] = s.o[mt][1] = s.o[mt][2] = s.o[mt][3] = 0.f;
+    const int r = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        if (r >= G) {
+            s.bq[ks][0] = s.bq[ks][1] = 0u;
+            continue;
+        }
+        if constexpr (DT == PKV_BF16) {
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(qs + r * kD + ks * 16 + 2 * q);
+            s.bq[ks][0] = w[0];
+            s.bq[ks][1] = w[4];  // +8 elements
+        } else {  // head_dim order permuted like K's: chunk ks, bytes 4q..4q+3
+            const __nv_bfloat16* p = qs + r * kD + ks * 16 + 4 * q;
+            s.bq[ks][0] = pack2<DT>(__bfloat162float(p[0]), __bfloat162float(p[1]));
+            s.bq[ks][1] = pack2<DT>(__bfloat162float(p[2]), __bfloat162float(p[3]));
+        }
+    }
+}
+
+// One 64-token stage for this warp's 16 rows [row0, row0+16) (n valid rows in
+// the stage).  warp_base: byte offset of the warp's first row in a tensor of
+// the stage; half_stride: bytes between a block's two 64-column halves.
+template <int DT>
+__device__ __forceinline__ void consume_tile(Acc<DT>& s, uint8_t* kst, uint8_t* vst, int n, int row0, int lane,
+                                             uint32_t warp_base, uint32_t half_stride, float qk) {
+    constexpr int kHalves = MmaCfg<DT>::kHalves;
+    if (row0 >= n) return;
+    const int r = lane >> 2, q = lane & 3;
+    if (n < row0 + 16) {  // zero this warp's V rows past the end
+        for (int i = lane; i < 16 * kHalves * 8; i += 32) {
+            const int lr = i / (kHalves * 8);
+            const int rest = i % (kHalves * 8);
+            if (row0 + lr >= n)
+                *reinterpret_cast<uint4*>(vst + warp_base + (rest >> 3) * half_stride + lr * kBoxRowBytes +
+                                          (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async();
+        __syncwarp();
+    }
+    // ---- S^T = K Q^T
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t kb = smem_u32(kst) + warp_base;
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // row (of the warp's 16) this lane addresses
+    if constexpr (DT == PKV_BF16) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int chunk = 2 * (ks & 3) + (lane >> 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kb + (ks >> 2) * half_stride + swz(lrow, chunk), a0, a1, a2, a3);
+            mma16816<DT>(sc, a0, a1, a2, a3, s.bq[ks][0], s.bq[ks][1]);
+        }
+    } else {
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {  // two k-steps (chunks 2kp, 2kp+1) per ldmatrix.x4
+            const int chunk = 2 * kp + (lane >> 4);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(kb + swz(lrow, chunk), r0, r1, r2, r3);
+            mma16816<DT>(sc, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
+                         e4m3x2_to_f16x2(r1 >> 16), s.bq[2 * kp][0], s.bq[2 * kp][1]);
+            mma16816<DT>(sc, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+                         e4m3x2_to_f16x2(r3 >> 16), s.bq[2 * kp + 1][0], s.bq[2 * kp + 1][1]);
+        }
+    }
+    // ---- online softmax (log2 domain); rows row0+r and row0+r+8
+    const bool va = row0 + r < n, vb = row0 + r + 8 < n;
+    const float s0 = va ? sc[0] * qk : -INFINITY;
+    const float s1 = va ? sc[1] * qk : -INFINITY;
+    const float s2 = vb ? sc[2] * qk : -INFINITY;
+    const float s3 = vb ? sc[3] * qk : -INFINITY;
+    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xFFFFFFFFu, x0, off));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xFFFFFFFFu, x1, off));
+    }
+    const float n0 = fmaxf(s.m0, x0), n1 = fmaxf(s.m1, x1);
+    const float al0 = exp2f(s.m0 - n0), al1 = exp2f(s.m1 - n1);
+    const float p0 = exp2f(s0 - n0), p1 = exp2f(s1 - n1);
+    const float p2 = exp2f(s2 - n0), p3 = exp2f(s3 - n1);
+    s.l0 = s.l0 * al0 + (p0 + p2);
+    s.l1 = s.l1 * al1 + (p1 + p3);
+    s.m0 = n0;
+    s.m1 = n1;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        s.o[mt][0] *= al0;
+        s.o[mt][1] *= al1;
+        s.o[mt][2] *= al0;
+        s.o[mt][3] *= al1;
+    }
+    const uint32_t pb0 = movmatrix_t(pack2<DT>(p0, p1));  // tokens 0-7 of the warp's 16
+    const uint32_t pb1 = movmatrix_t(pack2<DT>(p2, p3));  // tokens 8-15
+    // ---- O^T += V^T P^T
+    const uint32_t vb_ = smem_u32(vst) + warp_base;
+    if constexpr (DT == PKV_BF16) {
+        const int trow = (lane & 7) + ((lane >> 4) & 1) * 8;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int chunk = 2 * (mt & 3) + ((lane >> 3) & 1);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vb_ + (mt >> 2) * half_stride + swz(trow, chunk), a0, a1, a2, a3);
+            mma16816<DT>(s.o[mt], a0, a1, a2, a3, pb0, pb1);
+        }
+    } else {
+        const int ta = 2 * q;  // the warp's rows ta, ta+1, ta+8, ta+9
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int chunk = 2 * j + (r >> 2);
+            const uint32_t inner = static_cast<uint32_t>((r & 3) * 4);
+            const uint32_t w0 = lds32(vb_ + swz(ta, chunk) + inner);
+            const uint32_t w1 = lds32(vb_ + swz(ta + 1, chunk) + inner);
+            const uint32_t w8 = lds32(vb_ + swz(ta + 8, chunk) + inner);
+            const uint32_t w9 = lds32(vb_ + swz(ta + 9, chunk) + inner);
+            const uint32_t x01 = __byte_perm(w0, w1, 0x5140), x23 = __byte_perm(w0, w1, 0x7362);
+            const uint32_t y01 = __byte_perm(w8, w9, 0x5140), y23 = __byte_perm(w8, w9, 0x7362);
+            mma16816<DT>(s.o[2 * j], e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16), e4m3x2_to_f16x2(y01),
+                         e4m3x2_to_f16x2(y01 >> 16), pb0, pb1);
+            mma16816<DT>(s.o[2 * j + 1], e4m3x2_to_f16x2(x23), e4m3x2_to_f16x2(x23 >> 16), e4m3x2_to_f16x2(y23),
+                         e4m3x2_to_f16x2(y23 >> 16), pb0, pb1);
+        }
+    }
+}
+
+// Merge area: O [warp][G][128], m [warp][G], l [warp][G], one flag word.
+template <int G>
+struct Merge {
+    float* o;
+    float* m;
+    float* l;
+    volatile int* flag;
+    __device__ explicit Merge(uint8_t* base) {
+        o = reinterpret_cast<float*>(base);
+        m = o + kCWarps * G * kD;
+        l = m + kCWarps * G;
+        flag = reinterpret_cast<volatile int*>(l + kCWarps * G);
+    }
+};
+
+// Publish this warp's (m, l, O) for the G real heads.
+template <int DT, int G>
+__device__ __forceinline__ void merge_put(const Acc<DT>& s, const Merge<G>& mg, int warp, int lane) {
+    const int r = lane >> 2, q = lane & 3;
+    float l0 = s.l0, l1 = s.l1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
+        l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
+    }
+    const int h0 = 2 * q, h1 = 2 * q + 1;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        if (h0 < G) {
+            mg.o[(warp * G + h0) * kD + o_dim<DT>(mt, r)] = s.o[mt][0];
+            mg.o[(warp * G + h0) * kD + o_dim<DT>(mt, r + 8)] = s.o[mt][2];
+        }
+        if (h1 < G) {
+            mg.o[(warp * G + h1) * kD + o_dim<DT>(mt, r)] = s.o[mt][1];
+            mg.o[(warp * G + h1) * kD + o_dim<DT>(mt, r + 8)] = s.o[mt][3];
+        }
+    }
+    if (lane < 4) {
+        if (h0 < G) {
+            mg.m[warp * G + h0] = s.m0;
+            mg.l[warp * G + h0] = l0;
+        }
+        if (h1 < G) {
+            mg.m[warp * G + h1] = s.m1;
+            mg.l[warp * G + h1] = l1;
+        }
+    }
+}
+
+// Merged (sum O, max m, sum l) of head g at head-dim index d.
+template <int G>
+__device__ __forceinline__ void merge_get(const Merge<G>& mg, int g, int d, float& acc, float& M, float& lsum) {
+    M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kCWarps; ++w) M = fmaxf(M, mg.m[w * G + g]);
+    acc = 0.f;
+    lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCWarps; ++w) {
+        const float f = exp2f(mg.m[w * G + g] - M);  // warps without rows: 2^-inf = 0
+        acc += f * mg.o[(w * G + g) * kD + d];
+        lsum += f * mg.l[w * G + g];
+    }
+}
+
+// ---------------------------------------------------------------- producer
+// Stage s <- tile ti: tile info, the query rows at a segment's first tile,
+// and one TMA box per KV block (K and V).  All 32 producer lanes call it
+// (they share the block-table window); lane 0 issues.
+template <int DT, int G>
+__device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                            uint8_t* smem, uint64_t* full, int s, const TileInfo& ti,
+                                            const int32_t* table, int& cache, int& cache_base, int lane) {
+    using Lt = Layout<DT, G>;
+    const int bs = a.block_size;
+    uint8_t* kst = smem + s * Lt::kStageBytes;
+    uint8_t* vst = kst + Lt::kTensorBytes;
+    const uint32_t fb = smem_u32(&full[s]);
+    const int nblk = (ti.n + bs - 1) / bs;
+    const bool need_q = (ti.flags & kSegFirst) != 0;
+    if (lane == 0) {
+        reinterpret_cast<TileInfo*>(smem + Lt::kInfoOff)[s] = ti;
+        mbar_expect_tx(fb, static_cast<uint32_t>(nblk * bs * kBoxRowBytes * Lt::kHalves * 2 +
+                                                 (need_q ? Lt::kQBytes : 0)));
+        if (need_q) {
+            const __nv_bfloat16* qsrc = static_cast<const __nv_bfloat16*>(a.q) +
+                                        (static_cast<size_t>(ti.b) * a.num_q_heads + static_cast<size_t>(ti.h) * G) * kD;
+            bulk_load(smem_u32(smem + Lt::kQOff + s * Lt::kQBytes), qsrc, Lt::kQBytes, fb);
+        }
+    }
+    const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
+    for (int k = 0; k < nblk; ++k) {
+        const int j = ti.tok0 / bs + k;  // block index within the sequence
+        if (cache_base < 0 || j - cache_base >= 32 || j < cache_base) {
+            cache_base = j & ~31;
+            const int idx = cache_base + lane;
+            cache = idx < a.max_blocks ? table[idx] : -1;
+        }
+        int blk = __shfl_sync(0xFFFFFFFFu, cache, j - cache_base);
+        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks)) {
+            if (lane == 0 && a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
+            blk = 0;  // read an in-bounds block; the flag marks the output invalid
+        }
+        if (lane == 0) {
+            const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + ti.h) * bs);
+            const uint32_t off = k * Lt::kHalves * bs * kBoxRowBytes;
+            if (Lt::kHalves == 2 && a.tma_3d) {  // one box: both 128-byte halves of every row
+                tma_load_3d(smem_u32(kst + off), tmk, 0, y, 0, fb);
+                tma_load_3d(smem_u32(vst + off), tmv, 0, y, 0, fb);
+            } else {
+                for (int hf = 0; hf < Lt::kHalves; ++hf) {
+                    const uint32_t o2 = off + hf * bs * kBoxRowBytes;
+                    tma_load_2d(smem_u32(kst + o2), tmk, hf * 64, y, fb);
+                    tma_load_2d(smem_u32(vst + o2), tmv, hf * 64, y, fb);
+                }
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Tiles of sequence b (64 tokens each), 0 past the batch.
+__device__ __forceinline__ int seq_tiles(const DecodeArgs& a, int b) {
+    return b < a.num_seqs ? (clamped_len(a, b, false) + kTT - 1) / kTT : 0;
+}
+
+// kBal: balanced persistent schedule (grid = P CTAs); otherwise one CTA per
+// (split, KV head, sequence) with grid (num_splits, num_kv_heads, num_seqs).
+template <int DT, int G, bool kBal>
 __global__ void __launch_bounds__(kMmaThreads, 2)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
-    using C = MmaCfg<DT>;
-    constexpr int kStages = C::kStages;
-    constexpr int kHalves = C::kHalves;
-    constexpr int kTB = tensor_stage_bytes<DT>();
-    constexpr int kSB = stage_bytes<DT>();
+    using Lt = Layout<DT, G>;
+    constexpr int kStages = Lt::kStages;
+    constexpr int kHalves = Lt::kHalves;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + body_bytes<DT>());
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lt::kBarOff);
     uint64_t* empty = full + kStages;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+    uint64_t* csync_bar = empty + kStages;  // the 4 consumer warps meet here at segment ends
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(csync_bar + 1);
+    const TileInfo* info = reinterpret_cast<const TileInfo*>(smem + Lt::kInfoOff);
+    const Merge<G> mg(smem + Lt::kMergeOff);
 
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = clamped_len(a, b, split == 0 && h == 0 && threadIdx.x == 0);
-    const int t_begin = split * a.split_tokens;
-    const int t_end = min(L, t_begin + a.split_tokens);
-    const bool direct = a.num_splits == 1;
-    const int hq0 = h * G;
-    constexpr int D = 128;
 
-    if (t_begin >= t_end) {
-        if (direct) {
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(b) * a.num_q_heads + hq0) * D;
-            for (int i = threadIdx.x; i < G * D; i += kMmaThreads) o[i] = __float2bfloat16_rn(0.f);
+    // fixed schedule: this CTA's one segment
+    int fb_ = 0, fh_ = 0, fsplit = 0, t_begin = 0, t_end = 0;
+    if constexpr (!kBal) {
+        fsplit = blockIdx.x;
+        fh_ = blockIdx.y;
+        fb_ = blockIdx.z;
+        const int L = clamped_len(a, fb_, fsplit == 0 && fh_ == 0 && threadIdx.x == 0);
+        t_begin = fsplit * a.split_tokens;
+        t_end = min(L, t_begin + a.split_tokens);
+        if (t_begin >= t_end) {
+            if (a.num_splits == 1) {  // empty sequence: zero output rows
+                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
+                                   (static_cast<size_t>(fb_) * a.num_q_heads + fh_ * G) * kD;
+                for (int i = threadIdx.x; i < G * kD; i += kMmaThreads) o[i] = __float2bfloat16_rn(0.f);
+            }
+            return;
         }
-        return;
     }
-    const int num_tiles = (t_end - t_begin + kTT - 1) / kTT;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), kCWarps);
         }
+        mbar_init(smem_u32(csync_bar), kCWarps);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -248,56 +561,118 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
     if (warp == kCWarps) {
         // ------------------------------------------------------------ producer
-        const int bs = a.block_size;
-        const int32_t* table = a.tables + static_cast<size_t>(b) * a.max_blocks;
-        const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
         int cache = -1, cache_base = -1;
-        int issued = 0;
+        long long k = 0;  // stages issued
         bool ok = true;
-        for (int tile = 0; tile < num_tiles && ok; ++tile) {
-            const int s = tile % kStages;
-            if (tile >= kStages) {
-                ok = mbar_wait(smem_u32(&empty[s]), ((tile / kStages) - 1) & 1);
-                if (!ok) break;
-            }
-            if (*abort_flag) {
-                ok = false;
-                break;
-            }
-            const int tok0 = t_begin + tile * kTT;
-            const int n = min(kTT, t_end - tok0);
-            const int nblk = (n + bs - 1) / bs;
-            if (lane == 0) mbar_expect_tx(smem_u32(&full[s]), static_cast<uint32_t>(nblk * bs * kBoxRowBytes * kHalves * 2));
-            uint8_t* kst = smem + s * kSB;
-            uint8_t* vst = kst + kTB;
-            for (int k = 0; k < nblk; ++k) {
-                const int j = tok0 / bs + k;  // block index within the sequence
-                if (cache_base < 0 || j - cache_base >= 32) {
-                    cache_base = j & ~31;
-                    const int idx = cache_base + lane;
-                    cache = idx < a.max_blocks ? table[idx] : -1;
+        auto acquire = [&](long long kk) -> int {  // stage for the kk-th issue, after it is free
+            const int s = static_cast<int>(kk % kStages);
+            if (kk >= kStages && ok) ok = mbar_wait(smem_u32(&empty[s]), static_cast<uint32_t>(((kk / kStages) - 1) & 1));
+            if (*abort_flag) ok = false;
+            return s;
+        };
+        if constexpr (kBal) {
+            const int B = a.num_seqs, Hkv = a.num_kv_heads;
+            long long T = 0;
+#pragma unroll 4
+            for (int b0 = 0; b0 < B; b0 += 32) T += warp_sum_ll(seq_tiles(a, b0 + lane));
+            T *= Hkv;
+            // CTA c < P owns tiles [c*T/P, (c+1)*T/P); P <= T keeps every range non-empty
+            const long long P = T < static_cast<long long>(gridDim.x) ? T : static_cast<long long>(gridDim.x);
+            const long long c = blockIdx.x;
+            const long long g0 = c < P ? c * T / P : T, g1 = c < P ? (c + 1) * T / P : T;
+            if (g0 < g1) {
+                // locate tile g0: sequence b, and cum = tiles before b (x Hkv)
+                long long cum = 0;
+                int b = 0;
+                for (int b0 = 0; b0 < B; b0 += 32) {
+                    const long long u = static_cast<long long>(seq_tiles(a, b0 + lane)) * Hkv;
+                    long long incl = u;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                        if (lane >= o) incl += t;
+                    }
+                    const long long tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+                    if (g0 < cum + tot) {
+                        const unsigned m = __ballot_sync(0xFFFFFFFFu, cum + incl > g0);
+                        const int l = __ffs(m) - 1;
+                        cum += __shfl_sync(0xFFFFFFFFu, incl - u, l);
+                        b = b0 + l;
+                        break;
+                    }
+                    cum += tot;
                 }
-                int blk = __shfl_sync(0xFFFFFFFFu, cache, j - cache_base);
-                if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks)) {
-                    if (lane == 0 && a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
-                    blk = 0;  // read an in-bounds block; the flag marks the output invalid
-                }
-                if (lane == 0) {
-                    const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + h) * bs);
-                    const uint32_t off = k * kHalves * bs * kBoxRowBytes;
-                    if (kHalves == 2 && a.tma_3d) {  // one box: both 128-byte halves of every row
-                        tma_load_3d(smem_u32(kst + off), &tmk, 0, y, 0, smem_u32(&full[s]));
-                        tma_load_3d(smem_u32(vst + off), &tmv, 0, y, 0, smem_u32(&full[s]));
-                    } else {
-                        for (int hf = 0; hf < kHalves; ++hf) {
-                            const uint32_t o2 = off + hf * bs * kBoxRowBytes;
-                            tma_load_2d(smem_u32(kst + o2), &tmk, hf * 64, y, smem_u32(&full[s]));
-                            tma_load_2d(smem_u32(vst + o2), &tmv, hf * 64, y, smem_u32(&full[s]));
+                int L = clamped_len(a, b, false);
+                int nt = (L + kTT - 1) / kTT;
+                const long long off = g0 - cum;
+                int h = static_cast<int>(off / nt), t = static_cast<int>(off % nt);
+                const int32_t* table = a.tables + static_cast<size_t>(b) * a.max_blocks;
+                auto owner = [&](long long g) { return ((g + 1) * P - 1) / T; };
+                TileInfo ti;
+                for (long long g = g0; g < g1 && ok; ++g, ++k) {
+                    const int s = acquire(k);
+                    if (!ok) break;
+                    const long long pstart = cum + static_cast<long long>(h) * nt, pend = pstart + nt;
+                    if (g == g0 || t == 0) {  // a new segment: who shares this (sequence, KV head)
+                        const long long cf = owner(pstart);
+                        ti.b = b;
+                        ti.h = h;
+                        ti.c_first = static_cast<int>(cf);
+                        ti.pieces = static_cast<int>(owner(pend - 1) - cf + 1);
+                        ti.s_first = (cf * T / P < pstart) ? 1 : 0;
+                    }
+                    ti.tok0 = t * kTT;
+                    ti.n = min(kTT, L - ti.tok0);
+                    ti.flags = ((g == g0 || t == 0) ? kSegFirst : 0) | ((g == g1 - 1 || t == nt - 1) ? kSegLast : 0) |
+                               ((pstart >= g0 && pend <= g1) ? kSegWhole : 0) | (pstart <= g0 ? kCtaFirst : 0) |
+                               (g == g1 - 1 ? kCtaLast : 0);
+                    issue_stage<DT, G>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane);
+                    if (++t == nt) {  // next (sequence, KV head)
+                        t = 0;
+                        if (++h == Hkv) {
+                            h = 0;
+                            cum += static_cast<long long>(nt) * Hkv;
+                            ++b;
+                            while (b < B) {
+                                L = clamped_len(a, b, false);
+                                if (L > 0) break;
+                                ++b;
+                            }
+                            if (b < B) {
+                                nt = (L + kTT - 1) / kTT;
+                                table = a.tables + static_cast<size_t>(b) * a.max_blocks;
+                                cache_base = -1;
+                            }
                         }
                     }
                 }
             }
-            ++issued;
+        } else {
+            const int32_t* table = a.tables + static_cast<size_t>(fb_) * a.max_blocks;
+            const int ntiles = (t_end - t_begin + kTT - 1) / kTT;
+            for (int t = 0; t < ntiles && ok; ++t, ++k) {
+                const int s = acquire(k);
+                if (!ok) break;
+                TileInfo ti;
+                ti.b = fb_;
+                ti.h = fh_;
+                ti.tok0 = t_begin + t * kTT;
+                ti.n = min(kTT, t_end - ti.tok0);
+                ti.flags = (t == 0 ? kSegFirst : 0) | (t == ntiles - 1 ? kSegLast | kCtaLast : 0) |
+                           (a.num_splits == 1 ? kSegWhole : 0) | kCtaFirst;
+                ti.pieces = 1;
+                ti.c_first = 0;
+                ti.s_first = 0;
+                issue_stage<DT, G>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane);
+            }
+        }
+        if (ok && k == 0) {  // a CTA without tiles: tell the consumers
+            if (lane == 0) {
+                TileInfo* ti = reinterpret_cast<TileInfo*>(smem + Lt::kInfoOff);
+                ti->flags = kEnd;
+                mbar_arrive(smem_u32(&full[0]));
+            }
+            k = 1;
         }
         if (!ok && lane == 0) {
             *abort_flag = 1;
@@ -305,52 +680,46 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         // drain: every issued copy has landed before the CTA may exit
         if (lane == 0) {
-            for (int t = issued - 1; t >= 0 && t >= issued - kStages; --t)
-                (void)mbar_wait(smem_u32(&full[t % kStages]), (t / kStages) & 1);
+            for (long long kk = k - 1; kk >= 0 && kk >= k - kStages; --kk)
+                (void)mbar_wait(smem_u32(&full[kk % kStages]), static_cast<uint32_t>((kk / kStages) & 1));
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    const int r = lane >> 2, q = lane & 3;  // fragment row / column-pair index
-    // Q^T as the B operand, one k-step of 16 head-dim entries per register pair.
-    uint32_t bq[8][2];
-    {
-        const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(a.q) +
-                                    (static_cast<size_t>(b) * a.num_q_heads + hq0 + (r < G ? r : 0)) * D;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            if (r >= G) {
-                bq[ks][0] = bq[ks][1] = 0u;
-                continue;
-            }
-            if constexpr (DT == PKV_BF16) {
-                const uint32_t* w = reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * q);
-                bq[ks][0] = w[0];
-                bq[ks][1] = w[4];  // +8 elements
-            } else {
-                const __nv_bfloat16* p = qrow + ks * 16 + 4 * q;
-                bq[ks][0] = pack2<DT>(__bfloat162float(p[0]), __bfloat162float(p[1]));
-                bq[ks][1] = pack2<DT>(__bfloat162float(p[2]), __bfloat162float(p[3]));
-            }
-        }
-    }
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2q, 2q+1
-    float o[8][4];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     const int row0 = warp * 16;
     const float qk = a.qk_scale_log2;
     const int bsz = a.block_size;
     const uint32_t half_stride = static_cast<uint32_t>(bsz * kBoxRowBytes);
     // this warp's 16 rows: block row0/bs of the tile, rows row0%bs.. of it
-    const uint32_t warp_base = static_cast<uint32_t>((row0 / bsz) * kHalves * bsz * kBoxRowBytes +
-                                                     (row0 % bsz) * kBoxRowBytes);
+    const uint32_t warp_base =
+        static_cast<uint32_t>((row0 / bsz) * kHalves * bsz * kBoxRowBytes + (row0 % bsz) * kBoxRowBytes);
+    const int d = threadIdx.x;  // 128 consumer threads = 128 head-dim entries
+    Acc<DT> acc;
     bool aborted = false;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    // Bounded meeting point of the 4 consumer warps (an mbarrier, so that a
+    // warp that gave up on a wait cannot leave the others blocked forever).
+    uint32_t cphase = 0;
+    auto csync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(csync_bar));
+        const bool okw = mbar_wait(smem_u32(csync_bar), cphase);
+        cphase ^= 1u;
+        __syncwarp();
+        if (!okw) {
+            aborted = true;
+            if (lane == 0) {
+                *abort_flag = 1;
+                if (a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
+            }
+        }
+        return okw;
+    };
 
-    for (int tile = 0; tile < num_tiles; ++tile) {
-        const int s = tile % kStages;
-        if (!mbar_wait(smem_u32(&full[s]), (tile / kStages) & 1)) {
+    for (long long k = 0;; ++k) {
+        const int s = static_cast<int>(k % kStages);
+        if (!mbar_wait(smem_u32(&full[s]), static_cast<uint32_t>((k / kStages) & 1))) {
             aborted = true;
             if (lane == 0) {
                 *abort_flag = 1;
@@ -358,182 +727,126 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             }
             break;
         }
-        const int n = min(kTT, t_end - (t_begin + tile * kTT));
-        uint8_t* kst = smem + s * kSB;
-        uint8_t* vst = kst + kTB;
-        if (row0 < n) {
-            if (n < row0 + 16) {  // zero this warp's V rows past the end
-                for (int i = lane; i < 16 * kHalves * 8; i += 32) {
-                    const int lr = i / (kHalves * 8);
-                    const int rest = i % (kHalves * 8);
-                    if (row0 + lr >= n)
-                        *reinterpret_cast<uint4*>(vst + warp_base + (rest >> 3) * half_stride + lr * kBoxRowBytes +
-                                                  (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async();
-                __syncwarp();
-            }
-            // ---- S^T = K Q^T
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint32_t kb = smem_u32(kst) + warp_base;
-            const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // row (of the warp's 16) this lane addresses
-            if constexpr (DT == PKV_BF16) {
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int chunk = 2 * (ks & 3) + (lane >> 4);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kb + (ks >> 2) * half_stride + swz(lrow, chunk), a0, a1, a2, a3);
-                    mma16816<DT>(sc, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
-                }
-            } else {
-#pragma unroll
-                for (int kp = 0; kp < 4; ++kp) {  // two k-steps (chunks 2kp, 2kp+1) per ldmatrix.x4
-                    const int chunk = 2 * kp + (lane >> 4);
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4(kb + swz(lrow, chunk), r0, r1, r2, r3);
-                    mma16816<DT>(sc, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
-                                 e4m3x2_to_f16x2(r1 >> 16), bq[2 * kp][0], bq[2 * kp][1]);
-                    mma16816<DT>(sc, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
-                                 e4m3x2_to_f16x2(r3 >> 16), bq[2 * kp + 1][0], bq[2 * kp + 1][1]);
-                }
-            }
-            // ---- online softmax (log2 domain); rows row0+r and row0+r+8
-            const bool va = row0 + r < n, vb = row0 + r + 8 < n;
-            const float s0 = va ? sc[0] * qk : -INFINITY;
-            const float s1 = va ? sc[1] * qk : -INFINITY;
-            const float s2 = vb ? sc[2] * qk : -INFINITY;
-            const float s3 = vb ? sc[3] * qk : -INFINITY;
-            float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                x0 = fmaxf(x0, __shfl_xor_sync(0xFFFFFFFFu, x0, off));
-                x1 = fmaxf(x1, __shfl_xor_sync(0xFFFFFFFFu, x1, off));
-            }
-            const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-            const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
-            const float p0 = exp2f(s0 - n0), p1 = exp2f(s1 - n1);
-            const float p2 = exp2f(s2 - n0), p3 = exp2f(s3 - n1);
-            l0 = l0 * al0 + (p0 + p2);
-            l1 = l1 * al1 + (p1 + p3);
-            m0 = n0;
-            m1 = n1;
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                o[mt][0] *= al0;
-                o[mt][1] *= al1;
-                o[mt][2] *= al0;
-                o[mt][3] *= al1;
-            }
-            const uint32_t pb0 = movmatrix_t(pack2<DT>(p0, p1));  // tokens 0-7 of the warp's 16
-            const uint32_t pb1 = movmatrix_t(pack2<DT>(p2, p3));  // tokens 8-15
-            // ---- O^T += V^T P^T
-            const uint32_t vb_ = smem_u32(vst) + warp_base;
-            if constexpr (DT == PKV_BF16) {
-                const int trow = (lane & 7) + ((lane >> 4) & 1) * 8;
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    const int chunk = 2 * (mt & 3) + ((lane >> 3) & 1);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(vb_ + (mt >> 2) * half_stride + swz(trow, chunk), a0, a1, a2, a3);
-                    mma16816<DT>(o[mt], a0, a1, a2, a3, pb0, pb1);
-                }
-            } else {
-                const int ta = 2 * q;  // the warp's rows ta, ta+1, ta+8, ta+9
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int chunk = 2 * j + (r >> 2);
-                    const uint32_t inner = static_cast<uint32_t>((r & 3) * 4);
-                    const uint32_t w0 = lds32(vb_ + swz(ta, chunk) + inner);
-                    const uint32_t w1 = lds32(vb_ + swz(ta + 1, chunk) + inner);
-                    const uint32_t w8 = lds32(vb_ + swz(ta + 8, chunk) + inner);
-                    const uint32_t w9 = lds32(vb_ + swz(ta + 9, chunk) + inner);
-                    const uint32_t x01 = __byte_perm(w0, w1, 0x5140), x23 = __byte_perm(w0, w1, 0x7362);
-                    const uint32_t y01 = __byte_perm(w8, w9, 0x5140), y23 = __byte_perm(w8, w9, 0x7362);
-                    mma16816<DT>(o[2 * j], e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16), e4m3x2_to_f16x2(y01),
-                                 e4m3x2_to_f16x2(y01 >> 16), pb0, pb1);
-                    mma16816<DT>(o[2 * j + 1], e4m3x2_to_f16x2(x23), e4m3x2_to_f16x2(x23 >> 16),
-                                 e4m3x2_to_f16x2(y23), e4m3x2_to_f16x2(y23 >> 16), pb0, pb1);
-                }
-            }
-        }
+        const TileInfo ti = info[s];
+        if (ti.flags & kEnd) break;
+        uint8_t* kst = smem + s * Lt::kStageBytes;
+        if (ti.flags & kSegFirst)
+            acc_begin<DT, G>(acc, reinterpret_cast<const __nv_bfloat16*>(smem + Lt::kQOff + s * Lt::kQBytes), lane);
+        consume_tile<DT>(acc, kst, kst + Lt::kTensorBytes, ti.n, row0, lane, warp_base, half_stride, qk);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-    }
+        if (!(ti.flags & kSegLast)) continue;
 
-    // ---- merge the 4 warps' partial (m, l, O) through shared memory
+        // ---- segment end: merge the 4 warps, emit
+        merge_put<DT, G>(acc, mg, warp, lane);
+        if (!csync()) break;
+        const size_t qrow = static_cast<size_t>(ti.b) * a.num_q_heads + static_cast<size_t>(ti.h) * G;
+        if (ti.flags & kSegWhole) {
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
-        l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
-    }
-    consumer_sync();  // every consumer is done with the stages
-    float* mo = reinterpret_cast<float*>(smem);          // [warp][head 8][kMergeStride]
-    float* mm = mo + kCWarps * 8 * kMergeStride;         // [warp][head 8]
-    float* ml = mm + kCWarps * 8;                        // [warp][head 8]
+            for (int g = 0; g < G; ++g) {
+                float v, M, l;
+                merge_get<G>(mg, g, d, v, M, l);
+                out[(qrow + g) * kD + d] = __float2bfloat16_rn(v * (a.v_scale / l));
+            }
+        } else if constexpr (!kBal) {
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        float* base = mo + (warp * 8 + 2 * q) * kMergeStride;
-        base[o_dim<DT>(mt, r)] = o[mt][0];
-        base[kMergeStride + o_dim<DT>(mt, r)] = o[mt][1];
-        base[o_dim<DT>(mt, r + 8)] = o[mt][2];
-        base[kMergeStride + o_dim<DT>(mt, r + 8)] = o[mt][3];
-    }
-    if (lane < 4) {
-        mm[warp * 8 + 2 * q] = m0;
-        mm[warp * 8 + 2 * q + 1] = m1;
-        ml[warp * 8 + 2 * q] = l0;
-        ml[warp * 8 + 2 * q + 1] = l1;
-    }
-    consumer_sync();
-    if (aborted || *abort_flag) return;
-    const int d = threadIdx.x;  // 128 consumer threads = 128 head-dim entries
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kCWarps; ++w) M = fmaxf(M, mm[w * 8 + g]);
-        float acc = 0.f, lsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kCWarps; ++w) {
-            const float f = exp2f(mm[w * 8 + g] - M);
-            acc += f * mo[(w * 8 + g) * kMergeStride + d];
-            lsum += f * ml[w * 8 + g];
-        }
-        const float val = acc * (a.v_scale / lsum);
-        const size_t row = static_cast<size_t>(b) * a.num_q_heads + hq0 + g;
-        if (direct) {
-            static_cast<__nv_bfloat16*>(a.out)[row * D + d] = __float2bfloat16_rn(val);
+            for (int g = 0; g < G; ++g) {
+                float v, M, l;
+                merge_get<G>(mg, g, d, v, M, l);
+                a.o_part[((qrow + g) * a.num_splits + fsplit) * kD + d] = v * (a.v_scale / l);
+                if (d == 0) a.lse_part[(qrow + g) * a.num_splits + fsplit] = M + log2f(l);
+            }
         } else {
-            a.o_part[(row * a.num_splits + split) * D + d] = val;
-            if (d == 0) a.lse_part[row * a.num_splits + split] = M + log2f(lsum);
+            // partial of a (sequence, KV head) shared with other CTAs
+            const int slot = (ti.flags & kCtaFirst) ? 0 : 1;
+            const size_t pbase = (static_cast<size_t>(blockIdx.x) * 2 + slot) * G;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float v, M, l;
+                merge_get<G>(mg, g, d, v, M, l);
+                a.bal_o[(pbase + g) * kD + d] = v * (a.v_scale / l);
+                if (d == 0) a.bal_lse[pbase + g] = M + log2f(l);
+            }
+            __threadfence();
+            if (!csync()) break;
+            int* counter = a.counters + static_cast<size_t>(ti.b) * a.num_kv_heads + ti.h;
+            if (threadIdx.x == 0) *mg.flag = (atomicAdd(counter, 1) == ti.pieces - 1) ? 1 : 0;
+            if (!csync()) break;
+            if (*mg.flag) {  // every other piece is published: merge them all
+                __threadfence();
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float M = -INFINITY;
+                    for (int j = 0; j < ti.pieces; ++j) {
+                        const size_t pj = (static_cast<size_t>(ti.c_first + j) * 2 + (j == 0 ? ti.s_first : 0)) * G + g;
+                        M = fmaxf(M, __ldcg(a.bal_lse + pj));
+                    }
+                    float v = 0.f, z = 0.f;
+                    for (int j = 0; j < ti.pieces; ++j) {
+                        const size_t pj = (static_cast<size_t>(ti.c_first + j) * 2 + (j == 0 ? ti.s_first : 0)) * G + g;
+                        const float w = exp2f(__ldcg(a.bal_lse + pj) - M);
+                        z += w;
+                        v = fmaf(w, __ldcg(a.bal_o + pj * kD + d), v);
+                    }
+                    out[(qrow + g) * kD + d] = __float2bfloat16_rn(v / z);
+                }
+                if (threadIdx.x == 0) *counter = 0;  // ready for the next call
+            }
+        }
+        if (!csync()) break;  // the merge area is reused by the next segment
+        if (ti.flags & kCtaLast) break;
+    }
+    if (aborted || *abort_flag) return;
+    if constexpr (kBal) {  // zero the rows of empty sequences (and report bad lengths once)
+        for (int b = blockIdx.x; b < a.num_seqs; b += gridDim.x) {
+            if (clamped_len(a, b, threadIdx.x == 0) == 0) {
+                __nv_bfloat16* o = out + static_cast<size_t>(b) * a.num_q_heads * kD;
+                for (int i = threadIdx.x; i < a.num_q_heads * kD; i += kCWarps * 32) o[i] = __float2bfloat16_rn(0.f);
+            }
         }
     }
 }
 
-template <int DT, int G>
+template <int DT, int G, bool kBal>
 cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-    constexpr size_t smem = mma_smem_bytes<DT>();
-    auto kern = decode_mma_kernel<DT, G>;
+    using Lt = Layout<DT, G>;
+    constexpr size_t smem = Lt::kAlloc;
+    auto kern = decode_mma_kernel<DT, G, kBal>;
     static int configured_mask = 0;
+    static int ctas_per_sm[32] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 31 && !(configured_mask & (1 << dev))) {
+    if (dev >= 31) return cudaErrorNotSupported;
+    if (!(configured_mask & (1 << dev))) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        // ask for the largest shared-memory carveout so that two CTAs fit per SM
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kMmaThreads, smem);
+        if (e != cudaSuccess) return e;
+        ctas_per_sm[dev] = occ > 0 ? occ : 1;
         configured_mask |= 1 << dev;
     }
-    dim3 grid(a.num_splits, a.num_kv_heads, a.num_seqs);
+    dim3 grid;
+    if constexpr (kBal) {
+        const int P = num_sms() * ctas_per_sm[dev];
+        grid = dim3(P < a.bal_max_ctas ? P : a.bal_max_ctas);
+    } else {
+        grid = dim3(a.num_splits, a.num_kv_heads, a.num_seqs);
+    }
     kern<<<grid, kMmaThreads, smem, stream>>>(tk, tv, a);
     return cudaGetLastError();
 }
 
-template <int DT>
+template <int DT, bool kBal>
 cudaError_t launch_dt(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
     switch (a.num_q_heads / a.num_kv_heads) {
-        case 1: return launch_g<DT, 1>(a, tk, tv, stream);
-        case 2: return launch_g<DT, 2>(a, tk, tv, stream);
-        case 4: return launch_g<DT, 4>(a, tk, tv, stream);
-        case 8: return launch_g<DT, 8>(a, tk, tv, stream);
+        case 1: return launch_g<DT, 1, kBal>(a, tk, tv, stream);
+        case 2: return launch_g<DT, 2, kBal>(a, tk, tv, stream);
+        case 4: return launch_g<DT, 4, kBal>(a, tk, tv, stream);
+        case 8: return launch_g<DT, 8, kBal>(a, tk, tv, stream);
         default: return cudaErrorNotSupported;
     }
 }
@@ -542,7 +855,7 @@ cudaError_t launch_dt(const DecodeArgs& a, const CUtensorMap& tk, const CUtensor
 
 bool decode_mma_supported(pkv_dtype kv, int head_dim, int group, int block_size) {
     if (kv != PKV_BF16 && kv != PKV_FP8_E4M3) return false;
-    if (head_dim != 128) return false;
+    if (head_dim != kD) return false;
     if (group != 1 && group != 2 && group != 4 && group != 8) return false;
     return block_size == 16 || block_size == 32 || block_size == 64;
 }
@@ -551,8 +864,12 @@ cudaError_t launch_decode_mma(pkv_dtype kv, const DecodeArgs& a, const void* tma
                               cudaStream_t stream) {
     const CUtensorMap& tk = *static_cast<const CUtensorMap*>(tmap_k);
     const CUtensorMap& tv = *static_cast<const CUtensorMap*>(tmap_v);
-    if (kv == PKV_BF16) return launch_dt<PKV_BF16>(a, tk, tv, stream);
-    if (kv == PKV_FP8_E4M3) return launch_dt<PKV_FP8_E4M3>(a, tk, tv, stream);
+    const bool bal = a.bal_max_ctas > 0;
+    if (kv == PKV_BF16)
+        return bal ? launch_dt<PKV_BF16, true>(a, tk, tv, stream) : launch_dt<PKV_BF16, false>(a, tk, tv, stream);
+    if (kv == PKV_FP8_E4M3)
+        return bal ? launch_dt<PKV_FP8_E4M3, true>(a, tk, tv, stream)
+                   : launch_dt<PKV_FP8_E4M3, false>(a, tk, tv, stream);
     return cudaErrorNotSupported;
 }
 

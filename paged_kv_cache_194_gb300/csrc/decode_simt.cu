@@ -322,6 +322,9 @@ cudaError_t launch_one(const DecodeArgs& a, cudaStream_t stream) {
         if (dev < 31 && !(configured_mask & (1 << dev))) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
             if (e != cudaSuccess) return e;
             configured_mask |= 1 << dev;
         }

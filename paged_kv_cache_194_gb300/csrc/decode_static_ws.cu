@@ -13,14 +13,16 @@
 // library is loaded holds it until the process exits.  All calls share it:
 // calls that overlap on the GPU (different streams without ordering, or
 // different host threads) race on it.  Nothing in it needs clearing between
-// calls, because each call writes every partial it later reads.
+// calls: the only words that must start at zero (the per-sequence piece
+// counters) are cleared once, when the array is first set up on a device, and
+// every call leaves them at zero again.
 #include <cstdio>
 
 #include "pkv_internal.h"
 
-namespace {
+static __device__ __align__(256) unsigned char g_decode_scratch[PKV_STATIC_SCRATCH_BYTES];
 
-__device__ __align__(256) unsigned char g_decode_scratch[PKV_STATIC_SCRATCH_BYTES];
+namespace {
 
 // Device address of g_decode_scratch per device; resolved on the first call
 // made with that device current.
@@ -52,6 +54,8 @@ extern "C" pkv_status paged_decode_attention_static_ws(const void* q, pkv_dtype 
         if (!g_scratch_addr[dev]) {  // once per device, with that device current
             void* p = nullptr;
             e = cudaGetSymbolAddress(&p, g_decode_scratch);
+            // the piece counters must start at zero; cleared in stream order
+            if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, PKV_STATIC_SCRATCH_BYTES, static_cast<cudaStream_t>(stream));
             if (e != cudaSuccess) {
                 pkv::set_last_error(e);
                 return PKV_ERR_CUDA;

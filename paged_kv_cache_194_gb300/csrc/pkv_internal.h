@@ -45,6 +45,10 @@ struct DecodeArgs {
     const int32_t* lens;
     float* o_part;            // [B][Hq][num_splits][D] fp32 (split partials)
     float* lse_part;          // [B][Hq][num_splits] log2-domain log-sum-exp
+    int32_t* counters;        // [B][Hkv] finished pieces per (sequence, KV head); zero between calls
+    float* bal_o;             // balanced schedule: [CTA][2 slots][G][D] fp32 partials
+    float* bal_lse;           // balanced schedule: [CTA][2 slots][G] log2-sum-exp
+    int bal_max_ctas;         // > 0 selects the balanced persistent schedule (grid <= this)
     int32_t* err;             // optional error word
     int layer;
     int tma_3d;               // TMA descriptor kind (see pkv_pool::tmap_3d)

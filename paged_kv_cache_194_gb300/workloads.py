@@ -198,6 +198,8 @@ def fp8_scales(w: Workload, lens: torch.Tensor) -> Tuple[float, float]:
     for layer in range(w.num_layers):
         for b in range(w.num_seqs):
             n = int(lens[b]) + w.steps - 1
+            if n <= 0:
+                continue
             k, v = seq_kv(w, layer, b, n)
             ka = torch.maximum(ka, k.float().abs().max())
             va = torch.maximum(va, v.float().abs().max())

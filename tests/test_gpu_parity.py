@@ -238,3 +238,34 @@ def test_long_context_layers():
         ref, _ = oracle_reference(w, 1.0, 1.0, layer, q, tables, lens.tolist(), [0, 3])
         compare(out[[0, 3]], ref, TOL["bf16"], "long layer %d" % layer)
     assert batch.pool.errors() == 0
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_balanced_schedule_repeats_and_leaves_counters_zero(kv):
+    """Three calls on one workspace give identical bits; the per-sequence
+    counters at the front of the workspace are zero after every call."""
+    w = _w("balanced_" + kv, 4, 2, 128, 16, kv, "bf16", (5000, 1, 0, 64, 700, 4096, 129), seed=33)
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    q, tables, lens, _ = _run_step(batch, algo="mma")
+    ws = pk.workspace_for(batch.pool, w.num_seqs, w.num_q_heads, int(lens.max()))
+    outs = []
+    for _ in range(3):
+        outs.append(pk.paged_decode_attention(q.cuda(), batch.pool, 0, tables.cuda(), lens.cuda(), int(lens.max()),
+                                              w.scale, workspace=ws, algo="mma"))
+        torch.cuda.synchronize()
+        assert int(ws[:4 * w.num_seqs * w.num_kv_heads].count_nonzero()) == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    ref, _ = oracle_reference(w, inst.k_scale, inst.v_scale, 0, q, tables, lens.tolist(), list(range(w.num_seqs)))
+    compare(outs[0], ref, TOL[kv], "balanced " + kv)
+    assert batch.pool.errors() == 0
+
+
+def test_balanced_schedule_tiny_batch():
+    """Fewer tiles than CTAs: most CTAs own nothing."""
+    w = _w("balanced_tiny", 4, 1, 128, 16, "bf16", "bf16", (3, 70), seed=34)
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    q, tables, lens, out = _run_step(batch, algo="mma")
+    ref, _ = oracle_reference(w, 1.0, 1.0, 0, q, tables, lens.tolist(), [0, 1])
+    compare(out, ref, TOL["bf16"], "balanced tiny")

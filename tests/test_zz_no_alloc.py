@@ -30,13 +30,15 @@ def _batch(kv="bf16", lens=(1, 15, 16, 17, 64, 65, 300, 1000, 2047)):
     return w, batch, q.cuda(), batch.tables().cuda(), batch.seq_lens().cuda(), int(batch.seq_lens().max())
 
 
+@pytest.mark.parametrize("split", [64, 0], ids=["fixed_splits", "balanced"])
 @pytest.mark.parametrize("algo", ["simt", "mma"])
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
-def test_static_scratch_matches_workspace_entry_point(kv, algo):
+def test_static_scratch_matches_workspace_entry_point(kv, algo, split):
     w, batch, q, tables, lens, max_len = _batch(kv)
-    split = 64  # 32 splits for the longest sequence: the partials are used
+    # split 64: 32 fixed splits for the longest sequence; split 0: the
+    # tensor-core design's balanced schedule shares sequences between CTAs
     _, ns, need = pk.decode_plan(batch.pool, w.num_seqs, w.num_q_heads, max_len, split)
-    assert ns > 1 and 0 < need <= pk.STATIC_SCRATCH_BYTES
+    assert 0 < need <= pk.STATIC_SCRATCH_BYTES
     ref = pk.paged_decode_attention(q, batch.pool, 0, tables, lens, max_len, w.scale, split_tokens=split, algo=algo)
     for _ in range(2):  # two calls in a row share the library's array
         out = torch.full_like(q, float("nan"))
