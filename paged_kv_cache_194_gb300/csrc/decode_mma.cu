@@ -56,9 +56,7 @@ namespace {
 
 constexpr int kCWarps = 4;
 constexpr int kMmaThreads = (kCWarps + 1) * 32;
-constexpr int kTT = kTileTokens;           // tokens per stage (16 per consumer warp)
 constexpr int kBoxRowBytes = 128;          // one swizzled TMA row
-constexpr int kHalfBytes = kTT * kBoxRowBytes;
 constexpr int kD = 128;                    // head_dim served by this design
 constexpr uint32_t kSpinLimit = 1u << 22;  // try_wait polls before a wait gives up
 
@@ -68,11 +66,13 @@ template <>
 struct MmaCfg<PKV_BF16> {
     static constexpr int kHalves = 2;  // 128 columns = two 64-column (128-byte) halves
     static constexpr int kStages = 3;
+    static constexpr int kMT = 1;      // 16-token m-tiles per consumer warp per stage
 };
 template <>
 struct MmaCfg<PKV_FP8_E4M3> {
     static constexpr int kHalves = 1;  // 128 one-byte columns = one 128-byte row
-    static constexpr int kStages = 6;
+    static constexpr int kStages = 3;
+    static constexpr int kMT = 2;      // two independent m-tiles per warp: half the bytes per token need more ILP
 };
 
 // What one pipeline stage holds.
@@ -91,7 +91,7 @@ constexpr int kCtaFirst = 8;  // the segment holds the CTA's first tile
 constexpr int kEnd = 16;      // no tiles at all (a CTA that owns none)
 constexpr int kCtaLast = 32;  // the CTA's last tile
 
-// Shared memory of one CTA:
+// Shared memory of one CTA (a stage holds kTT = 64 * kMT tokens):
 //   stages: [kStages][K, V][block of the tile][half][bs rows][128 B]
 //     A block's two halves (head_dim 0-63 and 64-127 for BF16) are bs*128
 //     bytes apart; both start on 1024-byte boundaries (bs >= 16), so the
@@ -103,7 +103,9 @@ template <int DT, int G>
 struct Layout {
     static constexpr int kHalves = MmaCfg<DT>::kHalves;
     static constexpr int kStages = MmaCfg<DT>::kStages;
-    static constexpr int kTensorBytes = kHalves * kHalfBytes;
+    static constexpr int kMT = MmaCfg<DT>::kMT;
+    static constexpr int kTT = 16 * kCWarps * kMT;  // tokens per stage
+    static constexpr int kTensorBytes = kHalves * kTT * kBoxRowBytes;
     static constexpr int kStageBytes = 2 * kTensorBytes;
     static constexpr int kQBytes = G * kD * 2;
     static constexpr size_t kQOff = static_cast<size_t>(kStages) * kStageBytes;
@@ -173,9 +175,10 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                  : "r"(addr)
                  : "memory");
 }
+template <int kImm = 0>
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+    asm volatile("ld.shared.b32 %0, [%1+%2];\n" : "=r"(v) : "r"(addr), "n"(kImm) : "memory");
     return v;
 }
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
@@ -273,106 +276,183 @@ __device__ __forceinline__ void acc_begin(Acc<DT>& s, const __nv_bfloat16* qs, i
     }
 }
 
-// One 64-token stage for this warp's 16 rows [row0, row0+16) (n valid rows in
-// the stage).  warp_base: byte offset of the warp's first row in a tensor of
-// the stage; half_stride: bytes between a block's two 64-column halves.
+// Per-lane byte offsets (relative to the warp's first row in a tensor of a
+// stage) of the shared-memory fragments a consumer lane reads every tile;
+// they depend only on the lane, so they are computed once.
+struct LaneOffsets {
+    uint32_t k[4];  // K ldmatrix rows: chunk pair i (BF16: + half * half_stride)
+    uint32_t v[8];  // BF16: V ldmatrix.trans, chunk pair i (4 used); FP8: V bytes, (j, row ta / ta+1)
+};
+
 template <int DT>
+__device__ __forceinline__ LaneOffsets lane_offsets(int lane) {
+    LaneOffsets o;
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // K: row (of the warp's 16) this lane addresses
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o.k[i] = swz(lrow, 2 * i + (lane >> 4));
+    if constexpr (DT == PKV_BF16) {
+        const int trow = (lane & 7) + ((lane >> 4) & 1) * 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o.v[i] = swz(trow, 2 * i + ((lane >> 3) & 1));
+#pragma unroll
+        for (int i = 4; i < 8; ++i) o.v[i] = 0;
+    } else {
+        const int r = lane >> 2, q = lane & 3;
+        const uint32_t inner = static_cast<uint32_t>((r & 3) * 4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            o.v[2 * j] = swz(2 * q, 2 * j + (r >> 2)) + inner;
+            o.v[2 * j + 1] = swz(2 * q + 1, 2 * j + (r >> 2)) + inner;
+        }
+    }
+    return o;
+}
+
+// One stage for this warp's MT m-tiles of 16 rows, [row0, row0 + 16*MT)
+// (n valid rows in the stage).  wb[i]: byte offset of m-tile i's first row in
+// a tensor of the stage; half_stride: bytes between a block's two 64-column
+// halves.  The m-tiles' S chains are interleaved and share one softmax update.
+template <int DT, int MT>
 __device__ __forceinline__ void consume_tile(Acc<DT>& s, uint8_t* kst, uint8_t* vst, int n, int row0, int lane,
-                                             uint32_t warp_base, uint32_t half_stride, float qk) {
+                                             const uint32_t (&wb)[MT], uint32_t half_stride, float qk,
+                                             const LaneOffsets& lo) {
     constexpr int kHalves = MmaCfg<DT>::kHalves;
     if (row0 >= n) return;
-    const int r = lane >> 2, q = lane & 3;
-    if (n < row0 + 16) {  // zero this warp's V rows past the end
-        for (int i = lane; i < 16 * kHalves * 8; i += 32) {
-            const int lr = i / (kHalves * 8);
-            const int rest = i % (kHalves * 8);
-            if (row0 + lr >= n)
-                *reinterpret_cast<uint4*>(vst + warp_base + (rest >> 3) * half_stride + lr * kBoxRowBytes +
-                                          (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    const int r = lane >> 2;
+    if (n < row0 + 16 * MT) {  // zero this warp's V rows past the end
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            if (row0 + 16 * i >= n) continue;  // a fully empty m-tile is skipped below
+            for (int e = lane; e < 16 * kHalves * 8; e += 32) {
+                const int lr = e / (kHalves * 8);
+                const int rest = e % (kHalves * 8);
+                if (row0 + 16 * i + lr >= n)
+                    *reinterpret_cast<uint4*>(vst + wb[i] + (rest >> 3) * half_stride + lr * kBoxRowBytes +
+                                              (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
         fence_proxy_async();
         __syncwarp();
     }
-    // ---- S^T = K Q^T
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t kb = smem_u32(kst) + warp_base;
-    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // row (of the warp's 16) this lane addresses
+    bool live[MT];
+#pragma unroll
+    for (int i = 0; i < MT; ++i) live[i] = row0 + 16 * i < n;
+    // ---- S^T = K Q^T, m-tiles interleaved
+    float sc[MT][4];
+#pragma unroll
+    for (int i = 0; i < MT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+    const uint32_t kb = smem_u32(kst);
     if constexpr (DT == PKV_BF16) {
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            const int chunk = 2 * (ks & 3) + (lane >> 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(kb + (ks >> 2) * half_stride + swz(lrow, chunk), a0, a1, a2, a3);
-            mma16816<DT>(sc, a0, a1, a2, a3, s.bq[ks][0], s.bq[ks][1]);
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                if (!live[i]) continue;
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kb + wb[i] + (ks >> 2) * half_stride + lo.k[ks & 3], a0, a1, a2, a3);
+                mma16816<DT>(sc[i], a0, a1, a2, a3, s.bq[ks][0], s.bq[ks][1]);
+            }
         }
     } else {
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {  // two k-steps (chunks 2kp, 2kp+1) per ldmatrix.x4
-            const int chunk = 2 * kp + (lane >> 4);
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(kb + swz(lrow, chunk), r0, r1, r2, r3);
-            mma16816<DT>(sc, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
-                         e4m3x2_to_f16x2(r1 >> 16), s.bq[2 * kp][0], s.bq[2 * kp][1]);
-            mma16816<DT>(sc, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
-                         e4m3x2_to_f16x2(r3 >> 16), s.bq[2 * kp + 1][0], s.bq[2 * kp + 1][1]);
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                if (!live[i]) continue;
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4(kb + wb[i] + lo.k[kp], r0, r1, r2, r3);
+                mma16816<DT>(sc[i], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
+                             e4m3x2_to_f16x2(r1 >> 16), s.bq[2 * kp][0], s.bq[2 * kp][1]);
+                mma16816<DT>(sc[i], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+                             e4m3x2_to_f16x2(r3 >> 16), s.bq[2 * kp + 1][0], s.bq[2 * kp + 1][1]);
+            }
         }
     }
-    // ---- online softmax (log2 domain); rows row0+r and row0+r+8
-    const bool va = row0 + r < n, vb = row0 + r + 8 < n;
-    const float s0 = va ? sc[0] * qk : -INFINITY;
-    const float s1 = va ? sc[1] * qk : -INFINITY;
-    const float s2 = vb ? sc[2] * qk : -INFINITY;
-    const float s3 = vb ? sc[3] * qk : -INFINITY;
-    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+    // ---- online softmax (log2 domain) over the warp's 16*MT rows
+    float sv[MT][4];
+    float x0 = -INFINITY, x1 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+        const bool va = row0 + 16 * i + r < n, vb = row0 + 16 * i + r + 8 < n;
+        sv[i][0] = va ? sc[i][0] * qk : -INFINITY;
+        sv[i][1] = va ? sc[i][1] * qk : -INFINITY;
+        sv[i][2] = vb ? sc[i][2] * qk : -INFINITY;
+        sv[i][3] = vb ? sc[i][3] * qk : -INFINITY;
+        x0 = fmaxf(x0, fmaxf(sv[i][0], sv[i][2]));
+        x1 = fmaxf(x1, fmaxf(sv[i][1], sv[i][3]));
+    }
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         x0 = fmaxf(x0, __shfl_xor_sync(0xFFFFFFFFu, x0, off));
         x1 = fmaxf(x1, __shfl_xor_sync(0xFFFFFFFFu, x1, off));
     }
     const float n0 = fmaxf(s.m0, x0), n1 = fmaxf(s.m1, x1);
-    const float al0 = exp2f(s.m0 - n0), al1 = exp2f(s.m1 - n1);
-    const float p0 = exp2f(s0 - n0), p1 = exp2f(s1 - n1);
-    const float p2 = exp2f(s2 - n0), p3 = exp2f(s3 - n1);
-    s.l0 = s.l0 * al0 + (p0 + p2);
-    s.l1 = s.l1 * al1 + (p1 + p3);
-    s.m0 = n0;
-    s.m1 = n1;
+    float p[MT][4];
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        s.o[mt][0] *= al0;
-        s.o[mt][1] *= al1;
-        s.o[mt][2] *= al0;
-        s.o[mt][3] *= al1;
+    for (int i = 0; i < MT; ++i) {
+        p[i][0] = exp2f(sv[i][0] - n0);
+        p[i][1] = exp2f(sv[i][1] - n1);
+        p[i][2] = exp2f(sv[i][2] - n0);
+        p[i][3] = exp2f(sv[i][3] - n1);
     }
-    const uint32_t pb0 = movmatrix_t(pack2<DT>(p0, p1));  // tokens 0-7 of the warp's 16
-    const uint32_t pb1 = movmatrix_t(pack2<DT>(p2, p3));  // tokens 8-15
-    // ---- O^T += V^T P^T
-    const uint32_t vb_ = smem_u32(vst) + warp_base;
-    if constexpr (DT == PKV_BF16) {
-        const int trow = (lane & 7) + ((lane >> 4) & 1) * 8;
+    // rescale only when some head's running max moved (the factor is exactly 1 otherwise)
+    if (__any_sync(0xFFFFFFFFu, n0 != s.m0 || n1 != s.m1)) {
+        const float al0 = exp2f(s.m0 - n0), al1 = exp2f(s.m1 - n1);
+        s.l0 *= al0;
+        s.l1 *= al1;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-            const int chunk = 2 * (mt & 3) + ((lane >> 3) & 1);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(vb_ + (mt >> 2) * half_stride + swz(trow, chunk), a0, a1, a2, a3);
-            mma16816<DT>(s.o[mt], a0, a1, a2, a3, pb0, pb1);
+            s.o[mt][0] *= al0;
+            s.o[mt][1] *= al1;
+            s.o[mt][2] *= al0;
+            s.o[mt][3] *= al1;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+        s.l0 += p[i][0] + p[i][2];
+        s.l1 += p[i][1] + p[i][3];
+    }
+    s.m0 = n0;
+    s.m1 = n1;
+    uint32_t pb[MT][2];
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+        pb[i][0] = movmatrix_t(pack2<DT>(p[i][0], p[i][1]));  // tokens 0-7 of m-tile i
+        pb[i][1] = movmatrix_t(pack2<DT>(p[i][2], p[i][3]));  // tokens 8-15
+    }
+    // ---- O^T += V^T P^T
+    const uint32_t vb0 = smem_u32(vst);
+    if constexpr (DT == PKV_BF16) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                if (!live[i]) continue;
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vb0 + wb[i] + (mt >> 2) * half_stride + lo.v[mt & 3], a0, a1, a2, a3);
+                mma16816<DT>(s.o[mt], a0, a1, a2, a3, pb[i][0], pb[i][1]);
+            }
         }
     } else {
-        const int ta = 2 * q;  // the warp's rows ta, ta+1, ta+8, ta+9
+        // rows ta, ta+1 (ta = 2q) at offsets v[2j], v[2j+1]; rows ta+8, ta+9 are 8 rows (1024 B) further
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int chunk = 2 * j + (r >> 2);
-            const uint32_t inner = static_cast<uint32_t>((r & 3) * 4);
-            const uint32_t w0 = lds32(vb_ + swz(ta, chunk) + inner);
-            const uint32_t w1 = lds32(vb_ + swz(ta + 1, chunk) + inner);
-            const uint32_t w8 = lds32(vb_ + swz(ta + 8, chunk) + inner);
-            const uint32_t w9 = lds32(vb_ + swz(ta + 9, chunk) + inner);
-            const uint32_t x01 = __byte_perm(w0, w1, 0x5140), x23 = __byte_perm(w0, w1, 0x7362);
-            const uint32_t y01 = __byte_perm(w8, w9, 0x5140), y23 = __byte_perm(w8, w9, 0x7362);
-            mma16816<DT>(s.o[2 * j], e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16), e4m3x2_to_f16x2(y01),
-                         e4m3x2_to_f16x2(y01 >> 16), pb0, pb1);
-            mma16816<DT>(s.o[2 * j + 1], e4m3x2_to_f16x2(x23), e4m3x2_to_f16x2(x23 >> 16), e4m3x2_to_f16x2(y23),
-                         e4m3x2_to_f16x2(y23 >> 16), pb0, pb1);
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                if (!live[i]) continue;
+                const uint32_t vb_ = vb0 + wb[i];
+                const uint32_t w0 = lds32(vb_ + lo.v[2 * j]);
+                const uint32_t w1 = lds32(vb_ + lo.v[2 * j + 1]);
+                const uint32_t w8 = lds32<8 * kBoxRowBytes>(vb_ + lo.v[2 * j]);
+                const uint32_t w9 = lds32<8 * kBoxRowBytes>(vb_ + lo.v[2 * j + 1]);
+                const uint32_t x01 = __byte_perm(w0, w1, 0x5140), x23 = __byte_perm(w0, w1, 0x7362);
+                const uint32_t y01 = __byte_perm(w8, w9, 0x5140), y23 = __byte_perm(w8, w9, 0x7362);
+                mma16816<DT>(s.o[2 * j], e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(x01 >> 16), e4m3x2_to_f16x2(y01),
+                             e4m3x2_to_f16x2(y01 >> 16), pb[i][0], pb[i][1]);
+                mma16816<DT>(s.o[2 * j + 1], e4m3x2_to_f16x2(x23), e4m3x2_to_f16x2(x23 >> 16),
+                             e4m3x2_to_f16x2(y23), e4m3x2_to_f16x2(y23 >> 16), pb[i][0], pb[i][1]);
+            }
         }
     }
 }
@@ -503,7 +583,8 @@ __device__ __forceinline__ long long warp_sum_ll(long long v) {
     return v;
 }
 
-// Tiles of sequence b (64 tokens each), 0 past the batch.
+// Tiles of sequence b (kTT tokens each), 0 past the batch.
+template <int kTT>
 __device__ __forceinline__ int seq_tiles(const DecodeArgs& a, int b) {
     return b < a.num_seqs ? (clamped_len(a, b, false) + kTT - 1) / kTT : 0;
 }
@@ -517,6 +598,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     using Lt = Layout<DT, G>;
     constexpr int kStages = Lt::kStages;
     constexpr int kHalves = Lt::kHalves;
+    constexpr int kMT = Lt::kMT;
+    constexpr int kTT = Lt::kTT;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -574,7 +657,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             const int B = a.num_seqs, Hkv = a.num_kv_heads;
             long long T = 0;
 #pragma unroll 4
-            for (int b0 = 0; b0 < B; b0 += 32) T += warp_sum_ll(seq_tiles(a, b0 + lane));
+            for (int b0 = 0; b0 < B; b0 += 32) T += warp_sum_ll(seq_tiles<kTT>(a, b0 + lane));
             T *= Hkv;
             // CTA c < P owns tiles [c*T/P, (c+1)*T/P); P <= T keeps every range non-empty
             const long long P = T < static_cast<long long>(gridDim.x) ? T : static_cast<long long>(gridDim.x);
@@ -585,7 +668,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 long long cum = 0;
                 int b = 0;
                 for (int b0 = 0; b0 < B; b0 += 32) {
-                    const long long u = static_cast<long long>(seq_tiles(a, b0 + lane)) * Hkv;
+                    const long long u = static_cast<long long>(seq_tiles<kTT>(a, b0 + lane)) * Hkv;
                     long long incl = u;
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
@@ -687,14 +770,18 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
 
     // ---------------------------------------------------------------- consumers
-    const int row0 = warp * 16;
+    const int row0 = warp * 16 * kMT;
     const float qk = a.qk_scale_log2;
     const int bsz = a.block_size;
     const uint32_t half_stride = static_cast<uint32_t>(bsz * kBoxRowBytes);
-    // this warp's 16 rows: block row0/bs of the tile, rows row0%bs.. of it
-    const uint32_t warp_base =
-        static_cast<uint32_t>((row0 / bsz) * kHalves * bsz * kBoxRowBytes + (row0 % bsz) * kBoxRowBytes);
+    // this warp's m-tile i: rows row0+16i.. = block (row0+16i)/bs of the tile, rows (row0+16i)%bs.. of it
+    uint32_t wb[kMT];
+#pragma unroll
+    for (int i = 0; i < kMT; ++i)
+        wb[i] = static_cast<uint32_t>(((row0 + 16 * i) / bsz) * kHalves * bsz * kBoxRowBytes +
+                                      ((row0 + 16 * i) % bsz) * kBoxRowBytes);
     const int d = threadIdx.x;  // 128 consumer threads = 128 head-dim entries
+    const LaneOffsets lane_off = lane_offsets<DT>(lane);
     Acc<DT> acc;
     bool aborted = false;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
@@ -732,7 +819,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         uint8_t* kst = smem + s * Lt::kStageBytes;
         if (ti.flags & kSegFirst)
             acc_begin<DT, G>(acc, reinterpret_cast<const __nv_bfloat16*>(smem + Lt::kQOff + s * Lt::kQBytes), lane);
-        consume_tile<DT>(acc, kst, kst + Lt::kTensorBytes, ti.n, row0, lane, warp_base, half_stride, qk);
+        consume_tile<DT, kMT>(acc, kst, kst + Lt::kTensorBytes, ti.n, row0, lane, wb, half_stride, qk, lane_off);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         if (!(ti.flags & kSegLast)) continue;
