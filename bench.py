@@ -163,29 +163,37 @@ def run_ours(args):
     torch.cuda.set_device(local)
     pk.lib()
     w = replicas.rank_workload(wl.WORKLOADS[args.workload], rank)
-    if w.num_layers > 1:
-        raise SystemExit("multi-layer workloads are parity cases, not bench lines")
+    split = w.split_tokens if args.split is None else args.split
     inst = wl.instance(w)
-    batch = DecodeBatch(inst)
+    layers = list(range(w.num_layers))
+    # one layer drawn on the CPU (the oracle baseline regenerates it); the
+    # rest of a multi-layer pool is drawn on the device
+    batch = DecodeBatch(inst, cpu_layers=[0])
     dev = torch.device("cuda", local)
     slots_h = batch.next_token_slots()
-    q_h, kn_h, vn_h = batch.step_inputs(0)
+    inputs_h = [batch.step_inputs(l) for l in layers]  # (q, k_new, v_new) per layer
     tables_h, lens_h = batch.tables(), batch.seq_lens()
     max_len = int(lens_h.max())
-    q, kn, vn = q_h.to(dev), kn_h.to(dev), vn_h.to(dev)
+    qs = [x[0].to(dev) for x in inputs_h]
+    kns = [x[1].to(dev) for x in inputs_h]
+    vns = [x[2].to(dev) for x in inputs_h]
     slots = torch.from_numpy(slots_h).to(dev)
     tables, lens = tables_h.to(dev), lens_h.to(dev)
-    out = torch.empty_like(q)
-    S, NS, wsb = pk.decode_plan(batch.pool, w.num_seqs, w.num_q_heads, max_len, args.split)
+    out = torch.empty_like(qs[0])
+    S, NS, wsb = pk.decode_plan(batch.pool, w.num_seqs, w.num_q_heads, max_len, split)
     algo = pk.decode_algo(batch.pool, w.num_q_heads, args.algo)
-    schedule = "balanced" if (algo == "mma" and args.split == 0) else "fixed splits"
+    schedule = "balanced" if (algo == "mma" and split == 0) else "fixed splits"
     work = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    def attend(l):
+        pk.paged_decode_attention(qs[l], batch.pool, l, tables, lens, max_len, w.scale, out=out, workspace=work,
+                                  split_tokens=split, algo=args.algo, stream=stream)
+
     def step():
-        pk.kv_append(batch.pool, 0, kn, vn, slots, stream)
-        pk.paged_decode_attention(q, batch.pool, 0, tables, lens, max_len, w.scale, out=out, workspace=work,
-                                  split_tokens=args.split, algo=args.algo, stream=stream)
+        for l in layers:
+            pk.kv_append(batch.pool, l, kns[l], vns[l], slots, stream)
+            attend(l)
 
     for _ in range(args.warmup):
         step()
@@ -202,15 +210,18 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps * len(layers))]
     t_begin = time.time()
     ev0.record(stream)
-    for i in range(args.steps):
-        pk.kv_append(batch.pool, 0, kn, vn, slots, stream)
-        att[i][0].record(stream)
-        pk.paged_decode_attention(q, batch.pool, 0, tables, lens, max_len, w.scale, out=out, workspace=work,
-                                  split_tokens=args.split, algo=args.algo, stream=stream)
-        att[i][1].record(stream)
+    i = 0
+    for _ in range(args.steps):
+        for l in layers:
+            pk.kv_append(batch.pool, l, kns[l], vns[l], slots, stream)
+            att[i][0].record(stream)
+            attend(l)
+            att[i][1].record(stream)
+            i += 1
     ev1.record(stream)
     torch.cuda.synchronize()
     t_end = time.time()
@@ -218,43 +229,46 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop(t_begin, t_end)
     ms_total = replicas.max_over_ranks(ev0.elapsed_time(ev1), dev)
-    att_ms = sum(a.elapsed_time(b) for a, b in att) / args.steps
+    att_ms = sum(a.elapsed_time(b) for a, b in att) / len(att)
     ms_step = ms_total / args.steps
 
-    sum_len, kv_bytes, qb, kvb = workload_bytes(w, inst.lens)
+    sum_len, kv_layer, qb, kvb = workload_bytes(w, inst.lens)
+    kv_bytes = kv_layer * len(layers)
     all_kv_bytes = replicas.sum_over_ranks(kv_bytes, dev)
     all_len = replicas.sum_over_ranks(sum_len, dev)
     B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
-    # algorithmic bytes of one attention call (split kernel + combine)
+    # algorithmic bytes of one attention call (one layer)
     blocks_read = int(((inst.lens.long() + w.block_size - 1) // w.block_size).sum())
+    combine = schedule != "balanced" and NS > 1
     part = 0
-    if schedule != "balanced" and NS > 1:
+    if combine:
         nsplit = int(((inst.lens.long() + S - 1) // S).sum())
         part = 2 * nsplit * Hq * (D + 1) * 4  # partials written then read
-    att_bytes = kv_bytes + B * Hq * D * qb * 2 + blocks_read * 4 + B * 4 + part
+    att_bytes = kv_layer + B * Hq * D * qb * 2 + blocks_read * 4 + B * 4 + part
     value = all_kv_bytes / (ms_step * 1e-3) / 1e9
     achieved = att_bytes / (att_ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
     traffic = _profile_traffic("%s/%s/%s" % (args.workload, algo, w.kv_dtype), kernel_hash(algo))
-    combine = schedule != "balanced" and NS > 1
-    launches = args.steps * (2 + (1 if combine else 0))
+    launches = args.steps * len(layers) * (2 + (1 if combine else 0))
 
     # ---- end to end through the public API: pinned host buffers in, result out
     pin = lambda t: t.pin_memory()
-    hq_, hk_, hv_ = pin(q_h), pin(kn_h), pin(vn_h)
+    hin = [[pin(t) for t in x] for x in inputs_h]
     hs_, ht_, hl_ = pin(torch.from_numpy(slots_h)), pin(tables_h), pin(lens_h)
     hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    e2e_steps = max(1, min(args.steps, 2000))
-    h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_, hs_, ht_, hl_))
+    e2e_steps = max(1, min(args.steps, max(1, 2000 // len(layers))))
+    h2d = sum(t.numel() * t.element_size() for x in hin for t in x) + sum(
+        t.numel() * t.element_size() for t in (hs_, ht_, hl_))
     d2h = hout.numel() * hout.element_size()
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        q.copy_(hq_, non_blocking=True)
-        kn.copy_(hk_, non_blocking=True)
-        vn.copy_(hv_, non_blocking=True)
+        for l in layers:
+            qs[l].copy_(hin[l][0], non_blocking=True)
+            kns[l].copy_(hin[l][1], non_blocking=True)
+            vns[l].copy_(hin[l][2], non_blocking=True)
         slots.copy_(hs_, non_blocking=True)
         tables.copy_(ht_, non_blocking=True)
         lens.copy_(hl_, non_blocking=True)
@@ -268,13 +282,16 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
-        "tokens_per_s": round(all_len / (ms_step * 1e-3), 1),
-        "decode_tokens_per_s_32_layers": round(ws * B / (ms_step * 1e-3 * LAYERS), 1),
-        "config": {"workload": "%s: %d seqs, lens %s, %dq/%dkv heads, head_dim %d, block %d, %s KV"
-                   % (w.name, B, _lens_desc(w), Hq, Hkv, D, w.block_size, w.kv_dtype),
-                   "sum_seq_len": sum_len, "kv_bytes_per_step": kv_bytes, "split_tokens": S,
-                   "num_splits": NS if schedule != "balanced" else None, "schedule": schedule, "algo": algo, "parallelism": "replica per GPU" if ws > 1 else "1 GPU",
-                   "l2": "inputs exceed L2 (%.0f MB KV per step vs 129 MB L2); no flush" % (kv_bytes / 1e6)},
+        "tokens_per_s": round(all_len * len(layers) / (ms_step * 1e-3), 1),
+        "decode_tokens_per_s_32_layers": round(ws * B / (ms_step * 1e-3 * LAYERS / len(layers)), 1),
+        "config": {"workload": "%s: %d seqs, lens %s, %dq/%dkv heads, head_dim %d, block %d, %s KV%s"
+                   % (w.name, B, _lens_desc(w), Hq, Hkv, D, w.block_size, w.kv_dtype,
+                      ", %d layers per step" % len(layers) if len(layers) > 1 else ""),
+                   "sum_seq_len": sum_len, "kv_bytes_per_step": kv_bytes,
+                   "split_tokens": S if schedule != "balanced" else None,
+                   "num_splits": NS if schedule != "balanced" else None, "schedule": schedule, "algo": algo,
+                   "parallelism": "replica per GPU" if ws > 1 else "1 GPU",
+                   "l2": "inputs exceed L2 (%.0f MB KV per layer vs 129 MB L2); no flush" % (kv_layer / 1e6)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "paged_decode_attention call (decode_%s_kernel%s)" % (algo, " + combine" if combine else ""),
@@ -397,7 +414,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="llama")
     ap.add_argument("--algo", default="auto", choices=["auto", "simt", "mma"])
-    ap.add_argument("--split", type=int, default=0)
+    ap.add_argument("--split", type=int, default=None,
+                    help="fixed split size in tokens; 0 = balanced schedule; default: the workload's recipe")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)

@@ -161,6 +161,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -612,6 +617,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream (the append): nothing is read before that grid has finished.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
     // fixed schedule: this CTA's one segment
     int fb_ = 0, fh_ = 0, fsplit = 0, t_begin = 0, t_end = 0;
     if constexpr (!kBal) {
@@ -854,31 +863,35 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 a.bal_o[(pbase + g) * kD + d] = v * (a.v_scale / l);
                 if (d == 0) a.bal_lse[pbase + g] = M + log2f(l);
             }
-            __threadfence();
+            // Publish: after the consumer barrier one GPU-scope acq_rel atomic by
+            // thread 0 orders every consumer's partial writes before the count,
+            // and (for the last arriver) the other pieces' writes before our reads.
             if (!csync()) break;
             int* counter = a.counters + static_cast<size_t>(ti.b) * a.num_kv_heads + ti.h;
-            if (threadIdx.x == 0) *mg.flag = (atomicAdd(counter, 1) == ti.pieces - 1) ? 1 : 0;
+            if (threadIdx.x == 0) *mg.flag = (atom_add_acq_rel(counter, 1) == ti.pieces - 1) ? 1 : 0;
             if (!csync()) break;
-            if (*mg.flag) {  // every other piece is published: merge them all
-                __threadfence();
+            if (*mg.flag) {  // every other piece is published: merge them all in one pass
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    float M = -INFINITY;
+                    float M = -INFINITY, v = 0.f, z = 0.f;
+#pragma unroll 4
                     for (int j = 0; j < ti.pieces; ++j) {
                         const size_t pj = (static_cast<size_t>(ti.c_first + j) * 2 + (j == 0 ? ti.s_first : 0)) * G + g;
-                        M = fmaxf(M, __ldcg(a.bal_lse + pj));
-                    }
-                    float v = 0.f, z = 0.f;
-                    for (int j = 0; j < ti.pieces; ++j) {
-                        const size_t pj = (static_cast<size_t>(ti.c_first + j) * 2 + (j == 0 ? ti.s_first : 0)) * G + g;
-                        const float w = exp2f(__ldcg(a.bal_lse + pj) - M);
-                        z += w;
-                        v = fmaf(w, __ldcg(a.bal_o + pj * kD + d), v);
+                        const float lj = __ldcg(a.bal_lse + pj), oj = __ldcg(a.bal_o + pj * kD + d);
+                        const float Mn = fmaxf(M, lj);
+                        const float c = exp2f(M - Mn), w = exp2f(lj - Mn);
+                        v = fmaf(v, c, w * oj);
+                        z = fmaf(z, c, w);
+                        M = Mn;
                     }
                     out[(qrow + g) * kD + d] = __float2bfloat16_rn(v / z);
                 }
                 if (threadIdx.x == 0) *counter = 0;  // ready for the next call
             }
+            // every consumer read the merge area before the second barrier, so
+            // the next segment may overwrite it without another barrier
+            if (ti.flags & kCtaLast) break;
+            continue;
         }
         if (!csync()) break;  // the merge area is reused by the next segment
         if (ti.flags & kCtaLast) break;
@@ -923,8 +936,17 @@ cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
     } else {
         grid = dim3(a.num_splits, a.num_kv_heads, a.num_seqs);
     }
-    kern<<<grid, kMmaThreads, smem, stream>>>(tk, tv, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the previous kernel drains
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
 }
 
 template <int DT, bool kBal>

@@ -84,6 +84,9 @@ kv_append_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
                  const int64_t* __restrict__ slots, int num_tokens, int kv_heads, int head_dim,
                  int block_size, int64_t num_slots, uint8_t* __restrict__ k_layer,
                  uint8_t* __restrict__ v_layer, float k_inv, float v_inv, int32_t* err) {
+    // let a dependent decode launch start its set-up now; it waits for this
+    // grid to finish before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     constexpr int kPoolBytes = PDT == PKV_F32 ? 4 : (PDT == PKV_BF16 ? 2 : 1);
     constexpr int kInBytes = IDT == PKV_F32 ? 4 : 2;
     constexpr int kPer = 16 / kPoolBytes;  // elements per output chunk
