@@ -353,9 +353,16 @@ def cpu_baseline(w, inst, budget_s=15.0):
         _, _, threads = oracle.paged_attention(q, w.query_dtype, pool, 0, t, l, w.scale, return_threads=True)
         spent += time.perf_counter() - t0
         reps += 1
+    # one thread, on the first sequence only (a few seconds)
+    one = [0]
+    t0 = time.perf_counter()
+    oracle.paged_attention(q[one], w.query_dtype, pool, 0, t[one], l[one], w.scale, threads=1)
+    one_s = time.perf_counter() - t0
     return {"value": round(reps * kv_bytes / spent / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": "fp64 oracle attention over the whole %s batch (%d seqs, %d tokens), %d repetitions, %.1f s"
-                      % (w.name, len(seqs), int(l.sum()), reps, spent)}
+            "value_1_thread": round(_kv_bytes(w, int(l[0])) / one_s / 1e9, 4),
+            "sample": "fp64 oracle attention over the whole %s batch (%d seqs, %d tokens), %d repetitions, %.1f s; "
+                      "1-thread figure: sequence 0 (%d tokens) once"
+                      % (w.name, len(seqs), int(l.sum()), reps, spent, int(l[0]))}
 
 
 def run_reference(args):

@@ -65,7 +65,7 @@ def _algos(w):
 
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
 @pytest.mark.parametrize("split", [0, 64, 128])
-def test_small_parity(w, split):
+def test_small_parity(w, split, record_property):
     if split % w.block_size:
         pytest.skip("split must be a multiple of the block size")
     inst = wl.instance(w)
@@ -74,7 +74,9 @@ def test_small_parity(w, split):
         q, tables, lens, out = _run_step(batch, split=split, algo=algo)
         ref, _ = oracle_reference(w, inst.k_scale, inst.v_scale, 0, q, tables, lens.tolist(),
                                   list(range(w.num_seqs)))
-        compare(out, ref, TOL[w.kv_dtype], "%s split=%d algo=%s" % (w.name, split, algo))
+        e = compare(out, ref, TOL[w.kv_dtype], "%s split=%d algo=%s" % (w.name, split, algo))
+        record_property("max_abs_" + algo, e[0])
+        record_property("max_rel_" + algo, e[1])
         assert batch.pool.errors() == 0
 
 
@@ -197,33 +199,40 @@ def _sampled(B, k=4):
 
 
 @pytest.mark.parametrize("name", ["llama", "fp8"])
-def test_full_size_sampled(name):
+def test_full_size_sampled(name, record_property):
     w = wl.WORKLOADS[name]
     inst = wl.instance(w)
     batch = DecodeBatch(inst)
-    q, tables, lens, out = _run_step(batch)  # auto split, as the benchmark runs it
+    q, tables, lens, out = _run_step(batch)  # default schedule, as the benchmark runs it
     seqs = _sampled(w.num_seqs)
     ref, _ = oracle_reference(w, inst.k_scale, inst.v_scale, 0, q, tables, lens.tolist(), seqs)
-    compare(out[seqs], ref, TOL[w.kv_dtype], name)
+    max_abs, max_rel = compare(out[seqs], ref, TOL[w.kv_dtype], name)
+    record_property("max_abs", max_abs)
+    record_property("max_rel", max_rel)
+    record_property("sampled_seqs", len(seqs))
     assert batch.pool.errors() == 0
 
 
-def test_ragged_in_flight_steps():
+def test_ragged_in_flight_steps(record_property):
     w = wl.WORKLOADS["ragged"]
     inst = wl.instance(w)
     batch = DecodeBatch(inst)
     seqs = _sampled(w.num_seqs)
+    worst = (0.0, 0.0)
     for step in range(w.steps):
         q, tables, lens, out = _run_step(batch, step=step)
         if step in (0, w.steps - 1):
             ref, _ = oracle_reference(w, 1.0, 1.0, 0, q, tables, lens.tolist(), seqs)
-            compare(out[seqs], ref, TOL["bf16"], "ragged step %d" % step)
+            e = compare(out[seqs], ref, TOL["bf16"], "ragged step %d" % step)
+            worst = (max(worst[0], e[0]), max(worst[1], e[1]))
         batch.bm.check()
+    record_property("max_abs", worst[0])
+    record_property("max_rel", worst[1])
     assert batch.pool.errors() == 0
     assert lens.tolist() == [int(x) + w.steps - 1 for x in inst.lens]
 
 
-def test_long_context_layers():
+def test_long_context_layers(record_property):
     w = wl.WORKLOADS["long"]
     inst = wl.instance(w)
     batch = DecodeBatch(inst, cpu_layers=[0, 31])
@@ -236,7 +245,9 @@ def test_long_context_layers():
                                         int(lens.max()), w.scale, split_tokens=w.split_tokens)
         torch.cuda.synchronize()
         ref, _ = oracle_reference(w, 1.0, 1.0, layer, q, tables, lens.tolist(), [0, 3])
-        compare(out[[0, 3]], ref, TOL["bf16"], "long layer %d" % layer)
+        e = compare(out[[0, 3]], ref, TOL["bf16"], "long layer %d" % layer)
+        record_property("max_abs_layer%d" % layer, e[0])
+        record_property("max_rel_layer%d" % layer, e[1])
     assert batch.pool.errors() == 0
 
 
