@@ -46,7 +46,9 @@ typedef enum pkv_status {
     PKV_ERR_UNSUPPORTED = 2,   /* geometry or dtype this build has no kernel for */
     PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
     PKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
-    PKV_ERR_DEVICE_BOUNDS = 5  /* reserved for callers decoding the error word */
+    PKV_ERR_DEVICE_BOUNDS = 5, /* reserved for callers decoding the error word */
+    PKV_ERR_OUT_OF_BLOCKS = 6, /* block manager: the free list cannot cover the request */
+    PKV_ERR_INCONSISTENT = 7   /* block manager: an internal invariant does not hold */
 } pkv_status;
 
 /* Element types.  PKV_FP8_E4M3 is OCP E4M3 (bias 7, max 448, no infinities). */
@@ -212,6 +214,61 @@ pkv_status paged_decode_attention_static_ws(const void* q, pkv_dtype q_dtype, co
  * MMA for BF16/FP8 pools with head_dim 128 and G in {1, 2, 4, 8} (when the
  * driver provides TMA descriptors), SIMT otherwise. */
 int32_t paged_decode_algo(const pkv_pool* pool, int32_t group, pkv_algo requested);
+
+/*
+ * Host-side block manager ("How does TensorRT-LLM work?", "The paged KV
+ * cache": a pool of equal blocks handed out one at a time, a per-request
+ * table of its blocks in order, blocks returned the moment a request
+ * finishes, and requests that begin with the same text pointing at the same
+ * blocks; "TensorRT-LLM, in depth", "In-flight batching and the scheduler":
+ * a request that cannot get a block for its next token is paused; "The paged
+ * KV cache and block reuse": reuse only for identical token prefixes).
+ *
+ * Host memory only; no CUDA call.  Blocks are reference counted: a block is
+ * free when no sequence's table holds it.  Freed blocks go to the tail of an
+ * LRU free list and stay matchable by content until they are reallocated.
+ * A full block written by tokens with ids is identified by a 64-bit hash of
+ * the whole id prefix up to it; only such blocks are shared, so a shared block
+ * is never written again.  Slots are block * block_size + offset.  Not
+ * thread-safe: one manager per scheduler thread.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* free_order: a permutation of 0..num_blocks-1 (NULL = ascending) giving the
+ * order in which free blocks are handed out. */
+pkv_status kv_block_manager_create(int32_t num_blocks, int32_t block_size, int32_t max_blocks_per_seq,
+                                   const int32_t* free_order, pkv_block_manager** out);
+void kv_block_manager_destroy(pkv_block_manager* bm);
+int32_t kv_bm_num_free(const pkv_block_manager* bm);
+pkv_status kv_bm_add_sequence(pkv_block_manager* bm, int64_t seq_id);
+/* Drop a finished sequence: each of its blocks loses one reference. */
+pkv_status kv_bm_free_sequence(pkv_block_manager* bm, int64_t seq_id);
+/* Reserve the next n_tokens positions of a sequence and write their slots
+ * (slots_out may be NULL).  token_ids (may be NULL) identify the tokens for
+ * prefix reuse.  PKV_ERR_OUT_OF_BLOCKS, with nothing changed, when the free
+ * list or max_blocks_per_seq cannot cover them. */
+pkv_status kv_bm_grow(pkv_block_manager* bm, int64_t seq_id, int32_t n_tokens, const int32_t* token_ids,
+                      int64_t* slots_out);
+/* One decode step: the slot of each listed sequence's next token; a sequence
+ * that cannot get a block keeps its length and gets slot -1 (paused); the
+ * number of paused sequences goes to *n_paused. */
+pkv_status kv_bm_decode_slots(pkv_block_manager* bm, const int64_t* seq_ids, int32_t n, int64_t* slots_out,
+                              int32_t* n_paused);
+/* For an empty sequence about to hold a prompt of n_tokens ids: share every
+ * cached full block of the longest matching prefix (at most (n_tokens-1) /
+ * block_size blocks, so the last prompt token is always appended).  The
+ * sequence's length becomes the reused token count. */
+pkv_status kv_bm_match_prefix(pkv_block_manager* bm, int64_t seq_id, const int32_t* token_ids, int32_t n_tokens,
+                              int32_t* reused_tokens_out);
+int32_t kv_bm_seq_len(const pkv_block_manager* bm, int64_t seq_id);
+/* Host tables [n][width] (padded with -1) and lengths of the listed sequences. */
+pkv_status kv_bm_block_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int32_t n, int32_t width,
+                              int32_t* tables_out, int32_t* lens_out);
+/* Free list in hand-out order (up to cap entries); returns its length. */
+int32_t kv_bm_free_list(const pkv_block_manager* bm, int32_t* out, int32_t cap);
+int32_t kv_bm_block_ref(const pkv_block_manager* bm, int32_t block);
+/* Verify every invariant; PKV_ERR_INCONSISTENT if one fails. */
+pkv_status kv_bm_check(const pkv_block_manager* bm);
 
 /* Human-readable name of a status. */
 const char* pkv_status_string(pkv_status status);

@@ -19,13 +19,16 @@ LIB_PATH = os.path.join(HERE, "libpkv.so")
 PKV_F32, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 ALGOS = {"auto": 0, "simt": 1, "mma": 2}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda error",
-          5: "device bounds"}
+          5: "device bounds", 6: "out of blocks", 7: "inconsistent"}
 ERRBIT_BLOCK_ID, ERRBIT_SLOT, ERRBIT_SEQ_LEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("kv_pool_create", "kv_pool_destroy", "kv_pool_tensor_bytes", "kv_bytes_per_token",
            "kv_append", "paged_decode_plan", "paged_decode_algo", "paged_decode_attention",
-           "paged_decode_attention_static_ws", "pkv_status_string", "pkv_last_cuda_error")
+           "paged_decode_attention_static_ws", "pkv_status_string", "pkv_last_cuda_error",
+           "kv_block_manager_create", "kv_block_manager_destroy", "kv_bm_num_free", "kv_bm_add_sequence",
+           "kv_bm_free_sequence", "kv_bm_grow", "kv_bm_decode_slots", "kv_bm_match_prefix", "kv_bm_seq_len",
+           "kv_bm_block_tables", "kv_bm_free_list", "kv_bm_block_ref", "kv_bm_check")
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 ALGO_NAMES = {1: "simt", 2: "mma"}
 

@@ -152,6 +152,8 @@ const char* pkv_status_string(pkv_status s) {
         case PKV_ERR_WORKSPACE: return "workspace missing or too small";
         case PKV_ERR_CUDA: return "CUDA error";
         case PKV_ERR_DEVICE_BOUNDS: return "device-side index out of bounds";
+        case PKV_ERR_OUT_OF_BLOCKS: return "out of KV blocks";
+        case PKV_ERR_INCONSISTENT: return "block manager invariant violated";
     }
     return "unknown status";
 }

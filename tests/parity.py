@@ -21,12 +21,13 @@ TOL = {"bf16": 1e-2, "fp8": 2e-2, "f32": 1e-4}
 
 
 def oracle_reference(w: wl.Workload, k_scale: float, v_scale: float, layer: int, q: torch.Tensor,
-                     tables: torch.Tensor, lens: Sequence[int], seqs: Sequence[int]):
+                     tables: torch.Tensor, lens: Sequence[int], seqs: Sequence[int], rows_fn=None):
     """fp64 oracle output for the listed sequences ([len(seqs), Hq, D]).
 
     Only the blocks of the listed sequences are materialised: their ids are
     relabelled 0..n-1 in table order (the result does not depend on block
-    placement)."""
+    placement).  rows_fn(b, L) -> (k, v) supplies a sequence's rows when they
+    do not come from the workload generator."""
     tables = tables.numpy() if isinstance(tables, torch.Tensor) else np.asarray(tables)
     nblk = [(int(lens[b]) + w.block_size - 1) // w.block_size for b in seqs]
     total = max(1, sum(nblk))
@@ -41,7 +42,7 @@ def oracle_reference(w: wl.Workload, k_scale: float, v_scale: float, layer: int,
         L = int(lens[b])
         if L == 0:
             continue
-        k, v = wl.seq_kv(w, layer, b, L)
+        k, v = rows_fn(b, L) if rows_fn is not None else wl.seq_kv(w, layer, b, L)
         slots = oracle.slot_mapping(sub, w.block_size, np.full(L, i), np.arange(L))
         oracle.kv_append(pool, 0, k, v, w.in_dtype, slots)
     qs = q[list(seqs)]

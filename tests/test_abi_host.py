@@ -175,3 +175,124 @@ def test_block_manager_reproduces_paging_diagram():
         assert [b + 1 for b in bm.tables[name]] == blocks
     assert sorted(b + 1 for b in bm.free) == g["free"]
     bm.check()
+
+
+def test_prefix_reuse_shares_full_blocks_and_counts_references():
+    bm = BlockManager(16, 4, 8)
+    prompt = list(range(100, 111))  # 11 tokens: 2 full blocks + 3
+    bm.add("a")
+    bm.grow("a", len(prompt), token_ids=prompt)
+    a_blocks = bm.tables["a"]
+    bm.add("b")
+    reused = bm.match_prefix("b", prompt + [7, 8])  # same prefix, longer prompt
+    assert reused == 8 and bm.tables["b"] == a_blocks[:2]
+    assert [bm.ref(x) for x in a_blocks] == [2, 2, 1]
+    bm.grow("b", 5, token_ids=prompt[8:] + [7, 8])  # the rest of b's prompt: own blocks
+    assert set(bm.tables["b"][2:]).isdisjoint(a_blocks)
+    bm.check()
+    # a different prompt shares only the blocks whose whole prefix matches
+    bm.add("c")
+    assert bm.match_prefix("c", prompt[:4] + [0] * 9) == 4
+    bm.check()
+    bm.free_sequence("a")
+    assert [bm.ref(x) for x in a_blocks] == [3 - 1, 1, 0]  # c and b still hold block 0; b holds block 1
+    bm.check()
+
+
+def test_prefix_reuse_never_takes_the_last_prompt_token():
+    bm = BlockManager(8, 4, 4)
+    ids = [5, 6, 7, 8, 9, 10, 11, 12]  # exactly two full blocks
+    bm.add("a")
+    bm.grow("a", 8, token_ids=ids)
+    bm.add("b")
+    assert bm.match_prefix("b", ids) == 4  # the second block holds the last token: recomputed
+    bm.check()
+
+
+def test_freed_blocks_stay_matchable_until_reallocated():
+    bm = BlockManager(6, 2, 6)
+    ids = [1, 2, 3, 4, 5]
+    bm.add("a")
+    bm.grow("a", 5, token_ids=ids)  # blocks: [1,2] [3,4] [5]
+    cached = bm.tables["a"][:2]
+    bm.free_sequence("a")
+    assert bm.num_free == 6
+    bm.add("b")
+    assert bm.match_prefix("b", ids) == 4 and bm.tables["b"] == cached  # revived from the free list
+    bm.free_sequence("b")
+    # hand out every free block: the cached ones are evicted on reallocation
+    bm.add("hog")
+    bm.grow("hog", 12)
+    bm.free_sequence("hog")
+    bm.add("c")
+    assert bm.match_prefix("c", ids) == 0
+    bm.check()
+
+
+def test_decode_slots_pause_when_out_of_blocks():
+    bm = BlockManager(4, 2, 4)
+    for s, n in (("a", 2), ("b", 1), ("c", 4)):
+        bm.add(s)
+        bm.grow(s, n)
+    assert bm.num_free == 0
+    slots = bm.decode_slots(["a", "b", "c"])  # a and c need a new block, b has room
+    assert slots[0] == -1 and slots[2] == -1 and slots[1] >= 0 and bm.last_paused == 2
+    assert bm.lens == {"a": 2, "b": 2, "c": 4}
+    bm.free_sequence("b")
+    slots = bm.decode_slots(["a", "c"])  # one block freed: a gets it, c still waits
+    assert slots[0] >= 0 and slots[1] == -1
+    bm.check()
+
+
+def test_block_manager_random_ops_keep_invariants_and_slots():
+    rng = np.random.default_rng(1)
+    bs, nb, width = 4, 40, 12
+    bm = BlockManager(nb, bs, width, free_order=rng.permutation(nb))
+    live, prompts, slot_log = [], {}, {}
+    for step in range(400):
+        op = rng.integers(0, 5)
+        if op == 0 or not live:
+            s = "s%d" % step
+            bm.add(s)
+            live.append(s)
+            n = int(rng.integers(1, 20))
+            donors = [x for x in live if x in prompts]
+            base = prompts[donors[int(rng.integers(0, len(donors)))]][:8] if donors and rng.random() < 0.5 else []
+            ids = (base + [int(x) for x in rng.integers(0, 3, n)])[: max(1, n)]
+            reused = bm.match_prefix(s, ids)
+            try:
+                slots = bm.grow(s, len(ids) - reused, token_ids=ids[reused:])
+            except OutOfBlocks:
+                slots = np.zeros(0, np.int64)
+            prompts[s] = ids
+            slot_log[s] = {}
+            for i, sl in enumerate(slots):
+                slot_log[s][reused + i] = int(sl)
+        elif op == 1:
+            s = live.pop(int(rng.integers(0, len(live))))
+            bm.free_sequence(s)
+            del slot_log[s]
+        elif op == 2:
+            s = live[int(rng.integers(0, len(live)))]
+            try:
+                L = bm.seq_len(s)
+                for i, sl in enumerate(bm.grow(s, int(rng.integers(1, 6)))):
+                    slot_log[s][L + i] = int(sl)
+            except OutOfBlocks:
+                pass
+        else:
+            L0 = {s: bm.seq_len(s) for s in live}
+            for s, sl in zip(live, bm.decode_slots(live)):
+                if sl >= 0:
+                    slot_log[s][L0[s]] = int(sl)
+        bm.check()
+    # every slot the manager handed out agrees with the oracle's mapping of the final tables
+    tables = bm.block_tables(live, width).numpy()
+    for i, s in enumerate(live):
+        pos = sorted(slot_log[s])
+        if pos:
+            ref = oracle.slot_mapping(tables, bs, np.full(len(pos), i), np.array(pos))
+            assert np.array_equal(ref, [slot_log[s][p] for p in pos])
+    # no slot is written by two live sequences (shared blocks are never written again)
+    written = [sl for s in live for sl in slot_log[s].values()]
+    assert len(written) == len(set(written))
