@@ -390,3 +390,97 @@ void or_bf16_encode_array(const float* x, int64_t n, uint16_t* out) {
 void or_bf16_decode_array(const uint16_t* c, int64_t n, double* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = or_bf16_to_double(c[i]);
 }
+
+/* ------------------------------------------------- multi-query attention */
+
+/* Several queries per sequence: the last C tokens of sequence b (positions
+ * L_b - C .. L_b - 1) each ask a query, as when a decode step verifies C
+ * drafted tokens ("How does TensorRT-LLM work?", "Speculative decoding": the
+ * big model checks several guessed tokens in one pass) or a prompt chunk is
+ * processed ("TensorRT-LLM, in depth", "In-flight batching and the
+ * scheduler": chunked prefill).  Query c sits at position L_b - C + c and
+ * attends causally, to tokens 0 .. L_b - C + c:
+ *     out[b][c][hq][:] = softmax_t(scale * q[b][c][hq] . K_t) V_t
+ * q is [B][C][Hq][D]; out is [B][C][Hq][D] and lse [B][C][Hq] (double).
+ * A query with no token (L_b - C + c < 0) gets zeros and lse = -inf. */
+int or_paged_attention_mq(const void* q, int q_dtype, const void* k_pool, const void* v_pool,
+                          int kv_dtype, int num_layers, int num_blocks, int block_size,
+                          int kv_heads, int head_dim, int layer, float k_scale, float v_scale,
+                          const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* seq_lens, int num_seqs, int num_queries, int num_q_heads,
+                          float scale, double* out, double* lse, int num_threads) {
+    if (layer < 0 || layer >= num_layers || kv_heads <= 0 || num_q_heads % kv_heads != 0 ||
+        num_queries < 1)
+        return OR_BAD_ARG;
+    if (elem_bytes(kv_dtype) == 0 || (q_dtype != OR_F32 && q_dtype != OR_BF16)) return OR_BAD_ARG;
+    const int G = num_q_heads / kv_heads;
+    const int C = num_queries;
+    const double ks = (kv_dtype == OR_E4M3) ? (double)k_scale : 1.0;
+    const double vs = (kv_dtype == OR_E4M3) ? (double)v_scale : 1.0;
+    int status = OR_OK;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#else
+    num_threads = 1;
+#endif
+    const int64_t rows = (int64_t)num_seqs * C * num_q_heads;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+    for (int64_t pr = 0; pr < rows; ++pr) {
+        const int b = (int)(pr / ((int64_t)C * num_q_heads));
+        const int c = (int)((pr / num_q_heads) % C);
+        const int hq = (int)(pr % num_q_heads);
+        const int h = hq / G;
+        double* o = out + pr * head_dim;
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        lse[pr] = -INFINITY;
+        const int L = seq_lens[b];
+        if (L < 0 || L > max_blocks_per_seq * block_size) {
+#pragma omp atomic write
+            status = OR_BAD_INDEX;
+            continue;
+        }
+        const int n = L - C + c + 1; /* tokens 0 .. position of query c */
+        if (n <= 0) continue;
+        double* s = (double*)malloc(sizeof(double) * (size_t)n);
+        int64_t* row = (int64_t*)malloc(sizeof(int64_t) * (size_t)n);
+        int bad = 0;
+        for (int t = 0; t < n; ++t) {
+            int32_t blk = block_tables[(int64_t)b * max_blocks_per_seq + t / block_size];
+            if (blk < 0 || blk >= num_blocks) { bad = 1; break; }
+            row[t] = ((((int64_t)layer * num_blocks + blk) * kv_heads + h) * block_size +
+                      t % block_size) * head_dim;
+        }
+        if (bad) {
+#pragma omp atomic write
+            status = OR_BAD_INDEX;
+            free(s);
+            free(row);
+            continue;
+        }
+        double smax = -INFINITY;
+        for (int t = 0; t < n; ++t) {
+            double acc = 0.0;
+            for (int d = 0; d < head_dim; ++d) {
+                double qd = (q_dtype == OR_F32) ? (double)((const float*)q)[pr * head_dim + d]
+                                                : or_bf16_to_double(((const uint16_t*)q)[pr * head_dim + d]);
+                acc += qd * (load_elem(k_pool, kv_dtype, row[t] + d) * ks);
+            }
+            s[t] = (double)scale * acc;
+            if (s[t] > smax) smax = s[t];
+        }
+        double z = 0.0;
+        for (int t = 0; t < n; ++t) {
+            s[t] = exp(s[t] - smax);
+            z += s[t];
+        }
+        for (int t = 0; t < n; ++t) {
+            double w = s[t] / z;
+            for (int d = 0; d < head_dim; ++d)
+                o[d] += w * (load_elem(v_pool, kv_dtype, row[t] + d) * vs);
+        }
+        lse[pr] = smax + log(z);
+        free(s);
+        free(row);
+    }
+    return status;
+}

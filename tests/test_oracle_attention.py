@@ -288,3 +288,47 @@ def test_pages_closed_forms():
     # the fp8 workload is the pages' 55 full-context requests
     w = wl.WORKLOADS["fp8"]
     assert w.num_seqs * w.fixed_lens[0] == cap["bf16_tokens"]
+
+
+# ----------------------------------------------------------- multi-query
+
+@pytest.mark.parametrize("C,G", [(1, 4), (2, 4), (4, 2), (8, 1)])
+def test_multi_query_matches_causal_bruteforce(C, G):
+    w = _small("mq", G=G, Hkv=2, kv="bf16", lens=(C, C + 1, 17, 64, 100))
+    inst = wl.instance(w)
+    pool, rows = _fill_oracle(inst)
+    q = torch.randn(w.num_seqs, C, w.num_q_heads, w.head_dim,
+                    generator=torch.Generator().manual_seed(C)).to(torch.bfloat16)
+    out, lse = oracle.paged_attention_mq(q, "bf16", pool, 0, inst.tables, inst.lens, w.scale)
+    sc = float(np.float32(w.scale))
+    for b in range(w.num_seqs):
+        L = int(inst.lens[b])
+        K = rows[b][0].to(torch.float64)
+        V = rows[b][1].to(torch.float64)
+        for c in range(C):
+            qpos = L - C + c
+            for hq in range(w.num_q_heads):
+                h = hq // G
+                s = (K[:, h, :] @ q[b, c, hq].to(torch.float64)) * sc
+                s[qpos + 1:] = -math.inf  # causal: nothing after the query's own position
+                np.testing.assert_allclose(out[b, c, hq], (torch.softmax(s, 0) @ V[:, h, :]).numpy(),
+                                           rtol=1e-12, atol=1e-12)
+                assert abs(lse[b, c, hq] - float(torch.logsumexp(s, 0))) < 1e-12
+
+
+def test_multi_query_rows_equal_decode_on_prefixes():
+    """Query c is exactly decode attention over the first L - C + c + 1 tokens,
+    and C = 1 is plain decode."""
+    C = 3
+    w = _small("mq_prefix", G=4, Hkv=2, kv="fp8", lens=(5, 40, 129))
+    inst = wl.instance(w)
+    pool, _ = _fill_oracle(inst)
+    q = torch.randn(w.num_seqs, C, w.num_q_heads, w.head_dim,
+                    generator=torch.Generator().manual_seed(4)).to(torch.bfloat16)
+    out, lse = oracle.paged_attention_mq(q, "bf16", pool, 0, inst.tables, inst.lens, w.scale)
+    for c in range(C):
+        lens_c = inst.lens - (C - 1 - c)
+        ref, ref_lse = oracle.paged_attention(q[:, c].contiguous(), "bf16", pool, 0, inst.tables, lens_c, w.scale)
+        assert np.array_equal(out[:, c], ref) and np.array_equal(lse[:, c], ref_lse)
+    one, _ = oracle.paged_attention_mq(q[:, -1:].contiguous(), "bf16", pool, 0, inst.tables, inst.lens, w.scale)
+    assert np.array_equal(one[:, 0], out[:, -1])
