@@ -183,6 +183,33 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
                                   void* stream);
 
 /*
+ * Multi-query paged attention: the last num_queries (C) tokens of every
+ * sequence ask a query each, attending causally -- query c, at position
+ * seq_lens[b] - C + c, sees tokens 0 .. seq_lens[b] - C + c.  This is how a
+ * decode step verifies C drafted tokens ("How does TensorRT-LLM work?",
+ * "Speculative decoding": the real model checks several guessed tokens in one
+ * pass) and how a chunk of a prompt attends to the cache ("How does
+ * TensorRT-LLM work?", "In-flight batching": chunked prefill).
+ *   q    device [num_seqs][C][num_q_heads][head_dim];
+ *   out  device [num_seqs][C][num_q_heads][head_dim];
+ * other arguments as paged_decode_attention (which is the C = 1 case).  The
+ * tensor-core design serves C * (num_q_heads / num_kv_heads) <= 8; the SIMT
+ * design up to 8 (BF16) or 16 (F32) query rows per KV head, fewer for FP8.
+ * A query whose position is negative (seq_lens[b] < C) gets a zero row.
+ */
+pkv_status paged_multi_query_plan(const pkv_pool* pool, int32_t num_seqs, int32_t num_queries,
+                                  int32_t num_q_heads, int32_t max_seq_len, int32_t split_tokens,
+                                  int32_t* split_tokens_out, int32_t* num_splits_out,
+                                  size_t* workspace_bytes_out);
+pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const pkv_pool* pool,
+                                       int32_t layer, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                       int32_t num_seqs, int32_t num_queries, int32_t num_q_heads,
+                                       int32_t max_seq_len, float scale, int32_t split_tokens,
+                                       pkv_algo algo, void* workspace, size_t workspace_bytes,
+                                       void* out, void* stream);
+
+/*
  * paged_decode_attention without a caller-provided workspace, for callers that
  * may not allocate device memory where they run decode attention (plug-ins
  * whose device memory the host application plans once up front, loops that
@@ -209,7 +236,8 @@ pkv_status paged_decode_attention_static_ws(const void* q, pkv_dtype q_dtype, co
                                             void* stream);
 
 /* The kernel design paged_decode_attention would run for this pool, group
- * size (num_q_heads / num_kv_heads) and request: PKV_ALGO_SIMT or
+ * size (num_q_heads / num_kv_heads; for multi-query attention, times
+ * num_queries) and request: PKV_ALGO_SIMT or
  * PKV_ALGO_MMA, or -1 when the request cannot be served.  PKV_ALGO_AUTO picks
  * MMA for BF16/FP8 pools with head_dim 128 and G in {1, 2, 4, 8} (when the
  * driver provides TMA descriptors), SIMT otherwise. */

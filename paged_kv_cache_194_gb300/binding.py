@@ -25,6 +25,7 @@ ERRBIT_BLOCK_ID, ERRBIT_SLOT, ERRBIT_SEQ_LEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
 # Every symbol include/pkv.h declares.
 EXPORTS = ("kv_pool_create", "kv_pool_destroy", "kv_pool_tensor_bytes", "kv_bytes_per_token",
            "kv_append", "paged_decode_plan", "paged_decode_algo", "paged_decode_attention",
+           "paged_multi_query_plan", "paged_multi_query_attention",
            "paged_decode_attention_static_ws", "pkv_status_string", "pkv_last_cuda_error",
            "kv_block_manager_create", "kv_block_manager_destroy", "kv_bm_num_free", "kv_bm_add_sequence",
            "kv_bm_free_sequence", "kv_bm_grow", "kv_bm_decode_slots", "kv_bm_match_prefix", "kv_bm_seq_len",
@@ -80,6 +81,13 @@ def lib() -> ctypes.CDLL:
     L.paged_decode_attention.argtypes = [P, c.c_int, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                          c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int, P,
                                          c.c_size_t, P, P]
+    L.paged_multi_query_plan.restype = c.c_int
+    L.paged_multi_query_plan.argtypes = [P, c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+                                         c.POINTER(c.c_int32), c.POINTER(c.c_int32), c.POINTER(c.c_size_t)]
+    L.paged_multi_query_attention.restype = c.c_int
+    L.paged_multi_query_attention.argtypes = [P, c.c_int, P, c.c_int32, P, c.c_int32, P, c.c_int32, c.c_int32,
+                                              c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int, P,
+                                              c.c_size_t, P, P]
     L.paged_decode_attention_static_ws.restype = c.c_int
     L.paged_decode_attention_static_ws.argtypes = [P, c.c_int, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                                    c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int, P, P]
@@ -257,4 +265,35 @@ def paged_decode_attention_static_ws(q: torch.Tensor, pool: KVPool, layer: int, 
         block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Hq, max_seq_len, float(scale),
         split_tokens, ALGOS[algo], _dev(out, "out", q.dtype), _stream_ptr(stream))
     _check(rc, "paged_decode_attention_static_ws")
+    return out
+
+
+def multi_query_plan(pool: KVPool, num_seqs: int, num_queries: int, num_q_heads: int, max_seq_len: int,
+                     split_tokens: int = 0) -> Tuple[int, int, int]:
+    S, NS, ws = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    _check(lib().paged_multi_query_plan(pool.handle, num_seqs, num_queries, num_q_heads, max_seq_len, split_tokens,
+                                        ctypes.byref(S), ctypes.byref(NS), ctypes.byref(ws)),
+           "paged_multi_query_plan")
+    return S.value, NS.value, ws.value
+
+
+def paged_multi_query_attention(q: torch.Tensor, pool: KVPool, layer: int, block_tables: torch.Tensor,
+                                seq_lens: torch.Tensor, max_seq_len: int, scale: float,
+                                out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                                split_tokens: int = 0, algo: str = "auto", stream=None) -> torch.Tensor:
+    """q [B, C, Hq, D]: the last C tokens of each sequence, each attending
+    causally (query c at position seq_lens[b] - C + c).  Returns [B, C, Hq, D]."""
+    B, C, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        _, _, ws = multi_query_plan(pool, B, C, Hq, max_seq_len, split_tokens)
+        workspace = torch.zeros(ws, dtype=torch.uint8, device=q.device) if ws else None
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else ctypes.c_void_p()
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().paged_multi_query_attention(
+        _dev(q, "q"), _dtype_code(q.dtype), pool.handle, layer, _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, C, Hq, max_seq_len, float(scale),
+        split_tokens, ALGOS[algo], ws_ptr, ws_bytes, _dev(out, "out", q.dtype), _stream_ptr(stream))
+    _check(rc, "paged_multi_query_attention")
     return out

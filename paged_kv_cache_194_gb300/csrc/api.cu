@@ -220,9 +220,11 @@ pkv_status kv_append(const pkv_pool* p, int32_t layer, const void* k, const void
                                         static_cast<cudaStream_t>(stream)));
 }
 
-pkv_status paged_decode_plan(const pkv_pool* p, int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
-                             int32_t split_tokens, int32_t* split_out, int32_t* nsplit_out, size_t* ws_out) {
+pkv_status paged_multi_query_plan(const pkv_pool* p, int32_t num_seqs, int32_t num_queries, int32_t num_q_heads,
+                                  int32_t max_seq_len, int32_t split_tokens, int32_t* split_out,
+                                  int32_t* nsplit_out, size_t* ws_out) {
     if (!p || num_seqs < 0 || num_q_heads < 1 || max_seq_len < 0 || split_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_queries < 1 || num_queries > 64) return PKV_ERR_INVALID_ARG;
     if (num_q_heads % p->d.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     int S = split_tokens;
     if (S > 0) {
@@ -240,8 +242,8 @@ pkv_status paged_decode_plan(const pkv_pool* p, int32_t num_seqs, int32_t num_q_
     if (ns < 1) ns = 1;
     if (ns > INT32_MAX) return PKV_ERR_UNSUPPORTED;
     // layout: [counters][partials of whichever schedule the call runs]
-    size_t body = fixed_bytes(num_seqs, num_q_heads, p->d.head_dim, ns);
-    const int G = num_q_heads / p->d.num_kv_heads;
+    size_t body = fixed_bytes(num_seqs, num_queries * num_q_heads, p->d.head_dim, ns);
+    const int G = num_queries * (num_q_heads / p->d.num_kv_heads);  // query rows per KV head
     if (split_tokens == 0 && num_seqs <= kMaxBalancedSeqs) {
         const size_t bb = bal_bytes(bal_ctas(), G, p->d.head_dim);
         if (bb > body) body = bb;
@@ -251,6 +253,12 @@ pkv_status paged_decode_plan(const pkv_pool* p, int32_t num_seqs, int32_t num_q_
     if (nsplit_out) *nsplit_out = static_cast<int32_t>(ns);
     if (ws_out) *ws_out = ws;
     return PKV_OK;
+}
+
+pkv_status paged_decode_plan(const pkv_pool* p, int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
+                             int32_t split_tokens, int32_t* split_out, int32_t* nsplit_out, size_t* ws_out) {
+    return paged_multi_query_plan(p, num_seqs, 1, num_q_heads, max_seq_len, split_tokens, split_out, nsplit_out,
+                                  ws_out);
 }
 
 int32_t paged_decode_algo(const pkv_pool* p, int32_t G, pkv_algo algo) {
@@ -265,12 +273,14 @@ int32_t paged_decode_algo(const pkv_pool* p, int32_t G, pkv_algo algo) {
     return simt_ok ? PKV_ALGO_SIMT : -1;
 }
 
-pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,
-                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                  const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
-                                  int32_t max_seq_len, float scale, int32_t split_tokens, pkv_algo algo,
-                                  void* workspace, size_t workspace_bytes, void* out, void* stream) {
+pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, int32_t num_seqs, int32_t num_queries,
+                                       int32_t num_q_heads, int32_t max_seq_len, float scale, int32_t split_tokens,
+                                       pkv_algo algo, void* workspace, size_t workspace_bytes, void* out,
+                                       void* stream) {
     if (!p || layer < 0 || layer >= p->d.num_layers) return PKV_ERR_INVALID_ARG;
+    if (num_queries < 1 || num_queries > 64) return PKV_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 || max_seq_len < 0) return PKV_ERR_INVALID_ARG;
     if (num_q_heads % p->d.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * p->d.block_size)
@@ -284,7 +294,7 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
     if (!q || !out || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PKV_ERR_INVALID_ARG;
-    const int G = num_q_heads / p->d.num_kv_heads;
+    const int G = num_queries * (num_q_heads / p->d.num_kv_heads);  // query rows per KV head
 
     bool use_mma = false;
     pkv_pool* mp = const_cast<pkv_pool*>(p);  // the handle caches its TMA descriptors
@@ -299,7 +309,8 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
 
     int32_t S = 0, NS = 0;
     size_t need = 0;
-    pkv_status st = paged_decode_plan(p, num_seqs, num_q_heads, max_seq_len, split_tokens, &S, &NS, &need);
+    pkv_status st =
+        paged_multi_query_plan(p, num_seqs, num_queries, num_q_heads, max_seq_len, split_tokens, &S, &NS, &need);
     if (st != PKV_OK) return st;
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return PKV_ERR_WORKSPACE;
 
@@ -316,6 +327,7 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
     a.max_blocks = max_blocks_per_seq;
     a.max_len = max_seq_len;
     a.num_seqs = num_seqs;
+    a.num_queries = num_queries;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = p->d.num_kv_heads;
     a.head_dim = p->d.head_dim;
@@ -336,7 +348,7 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
             a.bal_o = reinterpret_cast<float*>(body);
             a.bal_lse = reinterpret_cast<float*>(body + bal_o_bytes(a.bal_max_ctas, G, p->d.head_dim));
         } else if (NS > 1) {
-            const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * NS;
+            const size_t rows = static_cast<size_t>(num_seqs) * num_queries * num_q_heads * NS;
             a.o_part = reinterpret_cast<float*>(body);
             a.lse_part = reinterpret_cast<float*>(body + round_up(rows * p->d.head_dim * sizeof(float), 256));
         }
@@ -347,6 +359,16 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
     if (e != cudaSuccess) return cuda_status(e);
     if (!balanced && NS > 1) return cuda_status(launch_combine(q_dtype, a, s));
     return PKV_OK;
+}
+
+pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_seq_len, float scale, int32_t split_tokens, pkv_algo algo,
+                                  void* workspace, size_t workspace_bytes, void* out, void* stream) {
+    return paged_multi_query_attention(q, q_dtype, p, layer, block_tables, max_blocks_per_seq, seq_lens, num_seqs, 1,
+                                       num_q_heads, max_seq_len, scale, split_tokens, algo, workspace,
+                                       workspace_bytes, out, stream);
 }
 
 }  // extern "C"

@@ -1,5 +1,8 @@
 // Paged decode attention, tensor-core design (BF16 and FP8-E4M3 pools,
-// head_dim 128, query group G in {1, 2, 4, 8}).
+// head_dim 128).  The B operand holds the NQ = C * G query rows of one KV head:
+// G query heads (grouped-query attention) times C queries per sequence (C = 1
+// for decode; C > 1 verifies drafted tokens or processes a prompt chunk: the
+// last C tokens of the sequence, each attending causally), NQ in {1, 2, 4, 8}.
 //
 // "How does TensorRT-LLM work?", "Custom attention kernels": one kernel does
 // the whole attention step and keeps the intermediate scores on chip.
@@ -78,7 +81,8 @@ struct MmaCfg<PKV_FP8_E4M3> {
 // What one pipeline stage holds.
 struct TileInfo {
     int b, h;       // sequence, KV head
-    int tok0, n;    // first token of the tile, valid tokens in it (1..64)
+    int L;          // the sequence's length
+    int tok0, n;    // first token of the tile, valid tokens in it (1..kTT)
     int flags;      // kSeg* / kEnd bits
     int pieces;     // CTAs that share this (sequence, KV head)
     int c_first;    // the first of them
@@ -317,10 +321,12 @@ __device__ __forceinline__ LaneOffsets lane_offsets(int lane) {
 // (n valid rows in the stage).  wb[i]: byte offset of m-tile i's first row in
 // a tensor of the stage; half_stride: bytes between a block's two 64-column
 // halves.  The m-tiles' S chains are interleaved and share one softmax update.
+// lim0 / lim1: rows of the tile visible to this lane's two query columns
+// (2q, 2q+1); both <= n, and equal to n for single-query decode.
 template <int DT, int MT>
 __device__ __forceinline__ void consume_tile(Acc<DT>& s, uint8_t* kst, uint8_t* vst, int n, int row0, int lane,
                                              const uint32_t (&wb)[MT], uint32_t half_stride, float qk,
-                                             const LaneOffsets& lo) {
+                                             const LaneOffsets& lo, int lim0, int lim1) {
     constexpr int kHalves = MmaCfg<DT>::kHalves;
     if (row0 >= n) return;
     const int r = lane >> 2;
@@ -378,11 +384,11 @@ __device__ __forceinline__ void consume_tile(Acc<DT>& s, uint8_t* kst, uint8_t* 
     float x0 = -INFINITY, x1 = -INFINITY;
 #pragma unroll
     for (int i = 0; i < MT; ++i) {
-        const bool va = row0 + 16 * i + r < n, vb = row0 + 16 * i + r + 8 < n;
-        sv[i][0] = va ? sc[i][0] * qk : -INFINITY;
-        sv[i][1] = va ? sc[i][1] * qk : -INFINITY;
-        sv[i][2] = vb ? sc[i][2] * qk : -INFINITY;
-        sv[i][3] = vb ? sc[i][3] * qk : -INFINITY;
+        const int ra = row0 + 16 * i + r, rb = ra + 8;
+        sv[i][0] = ra < lim0 ? sc[i][0] * qk : -INFINITY;
+        sv[i][1] = ra < lim1 ? sc[i][1] * qk : -INFINITY;
+        sv[i][2] = rb < lim0 ? sc[i][2] * qk : -INFINITY;
+        sv[i][3] = rb < lim1 ? sc[i][3] * qk : -INFINITY;
         x0 = fmaxf(x0, fmaxf(sv[i][0], sv[i][2]));
         x1 = fmaxf(x1, fmaxf(sv[i][1], sv[i][3]));
     }
@@ -392,17 +398,20 @@ __device__ __forceinline__ void consume_tile(Acc<DT>& s, uint8_t* kst, uint8_t* 
         x1 = fmaxf(x1, __shfl_xor_sync(0xFFFFFFFFu, x1, off));
     }
     const float n0 = fmaxf(s.m0, x0), n1 = fmaxf(s.m1, x1);
+    // a column that has seen no token yet keeps max -inf and weights 0
+    const float b0 = n0 == -INFINITY ? 0.f : n0, b1 = n1 == -INFINITY ? 0.f : n1;
     float p[MT][4];
 #pragma unroll
     for (int i = 0; i < MT; ++i) {
-        p[i][0] = exp2f(sv[i][0] - n0);
-        p[i][1] = exp2f(sv[i][1] - n1);
-        p[i][2] = exp2f(sv[i][2] - n0);
-        p[i][3] = exp2f(sv[i][3] - n1);
+        p[i][0] = exp2f(sv[i][0] - b0);
+        p[i][1] = exp2f(sv[i][1] - b1);
+        p[i][2] = exp2f(sv[i][2] - b0);
+        p[i][3] = exp2f(sv[i][3] - b1);
     }
     // rescale only when some head's running max moved (the factor is exactly 1 otherwise)
     if (__any_sync(0xFFFFFFFFu, n0 != s.m0 || n1 != s.m1)) {
-        const float al0 = exp2f(s.m0 - n0), al1 = exp2f(s.m1 - n1);
+        // against b0/b1: a column still without tokens (both maxima -inf) gets 0, not 2^NaN
+        const float al0 = exp2f(s.m0 - b0), al1 = exp2f(s.m1 - b1);
         s.l0 *= al0;
         s.l1 *= al1;
 #pragma unroll
@@ -519,6 +528,7 @@ __device__ __forceinline__ void merge_get(const Merge<G>& mg, int g, int d, floa
     for (int w = 0; w < kCWarps; ++w) M = fmaxf(M, mg.m[w * G + g]);
     acc = 0.f;
     lsum = 0.f;
+    if (M == -INFINITY) return;  // no token for this query in the segment
 #pragma unroll
     for (int w = 0; w < kCWarps; ++w) {
         const float f = exp2f(mg.m[w * G + g] - M);  // warps without rows: 2^-inf = 0
@@ -546,10 +556,15 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorM
         reinterpret_cast<TileInfo*>(smem + Lt::kInfoOff)[s] = ti;
         mbar_expect_tx(fb, static_cast<uint32_t>(nblk * bs * kBoxRowBytes * Lt::kHalves * 2 +
                                                  (need_q ? Lt::kQBytes : 0)));
-        if (need_q) {
-            const __nv_bfloat16* qsrc = static_cast<const __nv_bfloat16*>(a.q) +
-                                        (static_cast<size_t>(ti.b) * a.num_q_heads + static_cast<size_t>(ti.h) * G) * kD;
-            bulk_load(smem_u32(smem + Lt::kQOff + s * Lt::kQBytes), qsrc, Lt::kQBytes, fb);
+        if (need_q) {  // query rows n = c * gh + g: C copies of gh contiguous rows
+            const int C = a.num_queries, gh = G / C;
+            for (int c = 0; c < C; ++c) {
+                const __nv_bfloat16* qsrc =
+                    static_cast<const __nv_bfloat16*>(a.q) +
+                    ((static_cast<size_t>(ti.b) * C + c) * a.num_q_heads + static_cast<size_t>(ti.h) * gh) * kD;
+                bulk_load(smem_u32(smem + Lt::kQOff + s * Lt::kQBytes + c * gh * kD * 2), qsrc,
+                          static_cast<uint32_t>(gh * kD * 2), fb);
+            }
         }
     }
     const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
@@ -622,19 +637,23 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
     // fixed schedule: this CTA's one segment
-    int fb_ = 0, fh_ = 0, fsplit = 0, t_begin = 0, t_end = 0;
+    int fb_ = 0, fh_ = 0, fsplit = 0, t_begin = 0, t_end = 0, fL = 0;
     if constexpr (!kBal) {
         fsplit = blockIdx.x;
         fh_ = blockIdx.y;
         fb_ = blockIdx.z;
         const int L = clamped_len(a, fb_, fsplit == 0 && fh_ == 0 && threadIdx.x == 0);
+        fL = L;
         t_begin = fsplit * a.split_tokens;
         t_end = min(L, t_begin + a.split_tokens);
         if (t_begin >= t_end) {
             if (a.num_splits == 1) {  // empty sequence: zero output rows
-                __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) +
-                                   (static_cast<size_t>(fb_) * a.num_q_heads + fh_ * G) * kD;
-                for (int i = threadIdx.x; i < G * kD; i += kMmaThreads) o[i] = __float2bfloat16_rn(0.f);
+                const int C = a.num_queries, gh = G / C;
+                for (int i = threadIdx.x; i < G * kD; i += kMmaThreads) {
+                    const int nq = i / kD, c = nq / gh, g = nq % gh;
+                    static_cast<__nv_bfloat16*>(a.out)[((static_cast<size_t>(fb_) * C + c) * a.num_q_heads +
+                                                        fh_ * gh + g) * kD + i % kD] = __float2bfloat16_rn(0.f);
+                }
             }
             return;
         }
@@ -713,6 +732,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                         ti.pieces = static_cast<int>(owner(pend - 1) - cf + 1);
                         ti.s_first = (cf * T / P < pstart) ? 1 : 0;
                     }
+                    ti.L = L;
                     ti.tok0 = t * kTT;
                     ti.n = min(kTT, L - ti.tok0);
                     ti.flags = ((g == g0 || t == 0) ? kSegFirst : 0) | ((g == g1 - 1 || t == nt - 1) ? kSegLast : 0) |
@@ -748,6 +768,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 TileInfo ti;
                 ti.b = fb_;
                 ti.h = fh_;
+                ti.L = fL;
                 ti.tok0 = t_begin + t * kTT;
                 ti.n = min(kTT, t_end - ti.tok0);
                 ti.flags = (t == 0 ? kSegFirst : 0) | (t == ntiles - 1 ? kSegLast | kCtaLast : 0) |
@@ -828,7 +849,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         uint8_t* kst = smem + s * Lt::kStageBytes;
         if (ti.flags & kSegFirst)
             acc_begin<DT, G>(acc, reinterpret_cast<const __nv_bfloat16*>(smem + Lt::kQOff + s * Lt::kQBytes), lane);
-        consume_tile<DT, kMT>(acc, kst, kst + Lt::kTensorBytes, ti.n, row0, lane, wb, half_stride, qk, lane_off);
+        // causal limit of this lane's columns (2q, 2q+1): query c sees positions < L - C + c + 1
+        int lim0 = ti.n, lim1 = ti.n;
+        if (a.num_queries > 1) {
+            const int gh = G / a.num_queries, q2 = (lane & 3) * 2;
+            if (q2 < G) lim0 = min(ti.n, ti.L - a.num_queries + q2 / gh + 1 - ti.tok0);
+            if (q2 + 1 < G) lim1 = min(ti.n, ti.L - a.num_queries + (q2 + 1) / gh + 1 - ti.tok0);
+        }
+        consume_tile<DT, kMT>(acc, kst, kst + Lt::kTensorBytes, ti.n, row0, lane, wb, half_stride, qk, lane_off,
+                              lim0, lim1);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         if (!(ti.flags & kSegLast)) continue;
@@ -836,21 +865,25 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         // ---- segment end: merge the 4 warps, emit
         merge_put<DT, G>(acc, mg, warp, lane);
         if (!csync()) break;
-        const size_t qrow = static_cast<size_t>(ti.b) * a.num_q_heads + static_cast<size_t>(ti.h) * G;
+        // output row of query column g: (sequence, query c, head h*gh + g % gh)
+        const int Cq = a.num_queries, gh = G / Cq;
+        auto qrow = [&](int g) -> size_t {
+            return (static_cast<size_t>(ti.b) * Cq + g / gh) * a.num_q_heads + static_cast<size_t>(ti.h) * gh + g % gh;
+        };
         if (ti.flags & kSegWhole) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 float v, M, l;
                 merge_get<G>(mg, g, d, v, M, l);
-                out[(qrow + g) * kD + d] = __float2bfloat16_rn(v * (a.v_scale / l));
+                out[qrow(g) * kD + d] = __float2bfloat16_rn(l > 0.f ? v * (a.v_scale / l) : 0.f);
             }
         } else if constexpr (!kBal) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 float v, M, l;
                 merge_get<G>(mg, g, d, v, M, l);
-                a.o_part[((qrow + g) * a.num_splits + fsplit) * kD + d] = v * (a.v_scale / l);
-                if (d == 0) a.lse_part[(qrow + g) * a.num_splits + fsplit] = M + log2f(l);
+                a.o_part[(qrow(g) * a.num_splits + fsplit) * kD + d] = l > 0.f ? v * (a.v_scale / l) : 0.f;
+                if (d == 0) a.lse_part[qrow(g) * a.num_splits + fsplit] = l > 0.f ? M + log2f(l) : -INFINITY;
             }
         } else {
             // partial of a (sequence, KV head) shared with other CTAs
@@ -860,8 +893,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             for (int g = 0; g < G; ++g) {
                 float v, M, l;
                 merge_get<G>(mg, g, d, v, M, l);
-                a.bal_o[(pbase + g) * kD + d] = v * (a.v_scale / l);
-                if (d == 0) a.bal_lse[pbase + g] = M + log2f(l);
+                a.bal_o[(pbase + g) * kD + d] = l > 0.f ? v * (a.v_scale / l) : 0.f;
+                if (d == 0) a.bal_lse[pbase + g] = l > 0.f ? M + log2f(l) : -INFINITY;
             }
             // Publish: after the consumer barrier one GPU-scope acq_rel atomic by
             // thread 0 orders every consumer's partial writes before the count,
@@ -878,13 +911,14 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     for (int j = 0; j < ti.pieces; ++j) {
                         const size_t pj = (static_cast<size_t>(ti.c_first + j) * 2 + (j == 0 ? ti.s_first : 0)) * G + g;
                         const float lj = __ldcg(a.bal_lse + pj), oj = __ldcg(a.bal_o + pj * kD + d);
+                        if (lj == -INFINITY) continue;  // a piece with no token for this query
                         const float Mn = fmaxf(M, lj);
                         const float c = exp2f(M - Mn), w = exp2f(lj - Mn);
                         v = fmaf(v, c, w * oj);
                         z = fmaf(z, c, w);
                         M = Mn;
                     }
-                    out[(qrow + g) * kD + d] = __float2bfloat16_rn(v / z);
+                    out[qrow(g) * kD + d] = __float2bfloat16_rn(z > 0.f ? v / z : 0.f);
                 }
                 if (threadIdx.x == 0) *counter = 0;  // ready for the next call
             }
@@ -900,8 +934,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     if constexpr (kBal) {  // zero the rows of empty sequences (and report bad lengths once)
         for (int b = blockIdx.x; b < a.num_seqs; b += gridDim.x) {
             if (clamped_len(a, b, threadIdx.x == 0) == 0) {
-                __nv_bfloat16* o = out + static_cast<size_t>(b) * a.num_q_heads * kD;
-                for (int i = threadIdx.x; i < a.num_q_heads * kD; i += kCWarps * 32) o[i] = __float2bfloat16_rn(0.f);
+                __nv_bfloat16* o = out + static_cast<size_t>(b) * a.num_queries * a.num_q_heads * kD;
+                for (int i = threadIdx.x; i < a.num_queries * a.num_q_heads * kD; i += kCWarps * 32)
+                    o[i] = __float2bfloat16_rn(0.f);
             }
         }
     }
@@ -951,7 +986,7 @@ cudaError_t launch_g(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorM
 
 template <int DT, bool kBal>
 cudaError_t launch_dt(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-    switch (a.num_q_heads / a.num_kv_heads) {
+    switch (a.num_queries * (a.num_q_heads / a.num_kv_heads)) {
         case 1: return launch_g<DT, 1, kBal>(a, tk, tv, stream);
         case 2: return launch_g<DT, 2, kBal>(a, tk, tv, stream);
         case 4: return launch_g<DT, 4, kBal>(a, tk, tv, stream);

@@ -86,25 +86,29 @@ decode_simt_kernel(const DecodeArgs a) {
     const int t_begin = split * a.split_tokens;
     const int t_end = min(L, t_begin + a.split_tokens);
     const bool direct = a.num_splits == 1;
-    const int hq0 = h * G;
 
+    // The G rows served here are C queries x gh heads: row g is query g / gh
+    // (position L - C + g / gh, attending causally) of head h*gh + g % gh.
+    const int Cq = a.num_queries, gh = G / Cq;
+    auto qrow = [&](int g) -> size_t {
+        return (static_cast<size_t>(b) * Cq + g / gh) * a.num_q_heads + static_cast<size_t>(h) * gh + g % gh;
+    };
     if (t_begin >= t_end) {
         if (direct) {  // empty sequence: zero output rows
-            QT* o = static_cast<QT*>(a.out) + (static_cast<size_t>(b) * a.num_q_heads + hq0) * D;
-            for (int i = tid; i < G * D; i += kThreads) o[i] = to_out<QT>(0.f);
+            for (int i = tid; i < G * D; i += kThreads) static_cast<QT*>(a.out)[qrow(i / D) * D + i % D] = to_out<QT>(0.f);
         }
         return;
     }
 
-    // q slice of this lane: chunk (lane % LPT) of each of the G heads.
+    // q slice of this lane: chunk (lane % LPT) of each of the G rows.
     const int qc = lane % LPT;
     float qf[G][E];
     {
-        const QT* qb = static_cast<const QT*>(a.q) + (static_cast<size_t>(b) * a.num_q_heads + hq0) * D;
+        const QT* qb = static_cast<const QT*>(a.q);
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
-            for (int e = 0; e < E; ++e) qf[g][e] = load_q<QT>(qb + g * D + qc * E + e) * a.qk_scale_log2;
+            for (int e = 0; e < E; ++e) qf[g][e] = load_q<QT>(qb + qrow(g) * D + qc * E + e) * a.qk_scale_log2;
     }
 
     float m_run[kHeadsPerWarp], l_run[kHeadsPerWarp];
@@ -197,17 +201,20 @@ decode_simt_kernel(const DecodeArgs a) {
         }
         __syncthreads();
 
-        // ---- online softmax, one warp per head
+        // ---- online softmax, one warp per row; row g sees tokens before L - C + g/gh + 1
 #pragma unroll
         for (int i = 0; i < kHeadsPerWarp; ++i) {
             const int g = warp + kWarps * i;
             if (g < G) {
-                const float s0 = lane < n ? sP[lane * G + g] : -INFINITY;
-                const float s1 = lane + 32 < n ? sP[(lane + 32) * G + g] : -INFINITY;
+                const int lim = min(n, L - Cq + g / gh + 1 - (t_begin + tile * kTile));
+                const float s0 = lane < lim ? sP[lane * G + g] : -INFINITY;
+                const float s1 = lane + 32 < lim ? sP[(lane + 32) * G + g] : -INFINITY;
                 const float m_new = fmaxf(m_run[i], warp_max(fmaxf(s0, s1)));
-                const float alpha = exp2f(m_run[i] - m_new);
-                const float p0 = exp2f(s0 - m_new), p1 = exp2f(s1 - m_new);
-                if (lane < n) sP[lane * G + g] = p0;
+                // a row that has seen no token yet keeps max -inf and weights 0
+                const float base = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = m_new == -INFINITY ? 1.f : exp2f(m_run[i] - m_new);
+                const float p0 = exp2f(s0 - base), p1 = exp2f(s1 - base);
+                if (lane < n) sP[lane * G + g] = p0;  // 0 past the row's causal limit
                 if (lane + 32 < n) sP[(lane + 32) * G + g] = p1;
                 l_run[i] = l_run[i] * alpha + warp_sum(p0 + p1);
                 m_run[i] = m_new;
@@ -260,13 +267,13 @@ decode_simt_kernel(const DecodeArgs a) {
 #pragma unroll
         for (int t = 0; t < NTG; ++t) sum += red[(t * G + g) * D + d];
         const float l = sL[g];
-        const float o = sum * (a.v_scale / l);
-        const size_t row = static_cast<size_t>(b) * a.num_q_heads + hq0 + g;
+        const float o = l > 0.f ? sum * (a.v_scale / l) : 0.f;
+        const size_t row = qrow(g);
         if (direct) {
             static_cast<QT*>(a.out)[row * D + d] = to_out<QT>(o);
         } else {
             a.o_part[(row * a.num_splits + split) * D + d] = o;
-            if (d == 0) a.lse_part[row * a.num_splits + split] = sM[g] + log2f(l);
+            if (d == 0) a.lse_part[row * a.num_splits + split] = l > 0.f ? sM[g] + log2f(l) : -INFINITY;
         }
     }
 }
@@ -277,9 +284,9 @@ template <int D, typename QT>
 __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     constexpr int PER = D / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 4 + warp;  // b * Hq + hq
-    if (row >= a.num_seqs * a.num_q_heads) return;
-    const int b = row / a.num_q_heads;
+    const int row = blockIdx.x * 4 + warp;  // (b * C + c) * Hq + hq
+    if (row >= a.num_seqs * a.num_queries * a.num_q_heads) return;
+    const int b = row / (a.num_queries * a.num_q_heads);
     const int L = clamped_len(a, b, false);
     const int ns = (L + a.split_tokens - 1) / a.split_tokens;
     QT* o = static_cast<QT*>(a.out) + static_cast<size_t>(row) * D + lane * PER;
@@ -296,14 +303,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     float z = 0.f, acc[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    for (int s = 0; s < ns; ++s) {
-        const float w = exp2f(lse[s] - M);
+    for (int s = 0; s < ns && M != -INFINITY; ++s) {
+        const float w = exp2f(lse[s] - M);  // a split without a token for this query has lse -inf: weight 0
         z += w;
         const float* p = part + static_cast<size_t>(s) * D;
 #pragma unroll
         for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, p[i], acc[i]);
     }
-    const float inv = 1.f / z;
+    const float inv = z > 0.f ? 1.f / z : 0.f;
 #pragma unroll
     for (int i = 0; i < PER; ++i) o[i] = to_out<QT>(acc[i] * inv);
 }
@@ -336,7 +343,7 @@ cudaError_t launch_one(const DecodeArgs& a, cudaStream_t stream) {
 
 template <int DT, int D>
 cudaError_t by_group(const DecodeArgs& a, cudaStream_t stream) {
-    switch (a.num_q_heads / a.num_kv_heads) {
+    switch (a.num_queries * (a.num_q_heads / a.num_kv_heads)) {
         case 1: return launch_one<DT, D, 1>(a, stream);
         case 2: return launch_one<DT, D, 2>(a, stream);
         case 4: return launch_one<DT, D, 4>(a, stream);
@@ -395,7 +402,7 @@ cudaError_t launch_decode_simt(pkv_dtype kv, const DecodeArgs& a, cudaStream_t s
 }
 
 cudaError_t launch_combine(pkv_dtype q_dtype, const DecodeArgs& a, cudaStream_t stream) {
-    const int rows = a.num_seqs * a.num_q_heads;
+    const int rows = a.num_seqs * a.num_queries * a.num_q_heads;
     const int blocks = (rows + 3) / 4;
     if (blocks == 0) return cudaSuccess;
     if (q_dtype == PKV_F32) {

@@ -55,6 +55,7 @@ struct DecodeArgs {
     int max_blocks;
     int max_len;              // host bound of seq_lens (<= max_blocks * block_size)
     int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
+    int num_queries;          // queries per sequence: the last num_queries tokens, causal (1 = decode)
     int split_tokens, num_splits;
     float qk_scale_log2;      // scale * k_scale * log2(e)
     float v_scale;            // v_scale (FP8) or 1

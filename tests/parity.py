@@ -55,7 +55,7 @@ def compare(gpu: torch.Tensor, ref: np.ndarray, tol: float, what: str = ""):
     g = gpu.detach().to(torch.float64).cpu().numpy()
     err = np.abs(g - ref)
     bound = tol + tol * np.abs(ref)
-    bad = err > bound
+    bad = ~(err <= bound)  # NaN counts as a mismatch
     big = np.abs(ref) > 1e-3
     max_abs = float(err.max()) if err.size else 0.0
     max_rel = float((err[big] / np.abs(ref[big])).max()) if big.any() else 0.0
@@ -65,3 +65,26 @@ def compare(gpu: torch.Tensor, ref: np.ndarray, tol: float, what: str = ""):
                              % (what, int(bad.sum()), bad.size, tol, max_abs, max_rel, idx.tolist()))
     assert np.isfinite(g).all(), what + ": non-finite output"
     return max_abs, max_rel
+
+
+def oracle_reference_mq(w: wl.Workload, k_scale: float, v_scale: float, layer: int, q: torch.Tensor,
+                        tables, lens: Sequence[int], seqs: Sequence[int]):
+    """fp64 oracle for multi-query attention of the listed sequences
+    ([len(seqs), C, Hq, D]); rows from the workload generator."""
+    tables = tables.numpy() if isinstance(tables, torch.Tensor) else np.asarray(tables)
+    nblk = [(int(lens[b]) + w.block_size - 1) // w.block_size for b in seqs]
+    total, width = max(1, sum(nblk)), max(1, max(nblk))
+    sub = np.full((len(seqs), width), -1, dtype=np.int32)
+    pos = 0
+    for i, n in enumerate(nblk):
+        sub[i, :n] = np.arange(pos, pos + n, dtype=np.int32)
+        pos += n
+    pool = oracle.OraclePool(1, total, w.block_size, w.num_kv_heads, w.head_dim, w.kv_dtype, k_scale, v_scale)
+    for i, b in enumerate(seqs):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        k, v = wl.seq_kv(w, layer, b, L)
+        oracle.kv_append(pool, 0, k, v, w.in_dtype, oracle.slot_mapping(sub, w.block_size, np.full(L, i), np.arange(L)))
+    sl = np.array([int(lens[b]) for b in seqs], dtype=np.int32)
+    return oracle.paged_attention_mq(q[list(seqs)], w.query_dtype, pool, 0, sub, sl, w.scale)

@@ -1,0 +1,71 @@
+"""GPU parity of multi-query paged attention (speculative verification /
+prompt chunks): the last C tokens of each sequence query causally."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_194_gb300 import binding as pk
+from paged_kv_cache_194_gb300 import workloads as wl
+from paged_kv_cache_194_gb300.decode import DecodeBatch
+
+from parity import TOL, compare, oracle_reference_mq
+
+pytestmark = pytest.mark.gpu
+
+
+def _w(name, G, Hkv, kv, ind, lens, bs=16, D=128):
+    return wl.Workload(name, 41, len(lens), G * Hkv, Hkv, D, bs, kv, ind, 1.0 / math.sqrt(D),
+                       lens="fixed", fixed_lens=tuple(lens), dist="uniform" if kv == "f32" else "normal")
+
+
+def _filled(w):
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    slots = batch.next_token_slots()  # the last position of each sequence
+    _, kn, vn = batch.step_inputs(0)
+    pk.kv_append(batch.pool, 0, kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda())
+    return inst, batch
+
+
+CASES = [  # (G, C, kv, designs)
+    (4, 2, "bf16", ("mma", "simt")),
+    (4, 2, "fp8", ("mma",)),
+    (2, 4, "bf16", ("mma", "simt")),
+    (1, 8, "bf16", ("mma", "simt")),
+    (2, 4, "f32", ("simt",)),
+]
+
+
+@pytest.mark.parametrize("split", [0, 64])
+@pytest.mark.parametrize("G,C,kv,algos", CASES, ids=lambda x: str(x))
+def test_multi_query_parity(G, C, kv, algos, split):
+    lens = (C - 1, C, C + 1, 17, 64, 65, 300, 1000)
+    w = _w("mq_%s_g%d_c%d" % (kv, G, C), G, 2, kv, "f32" if kv == "f32" else "bf16", lens,
+           D=64 if kv == "f32" else 128)
+    inst, batch = _filled(w)
+    tables, lens_t = batch.tables(), batch.seq_lens()
+    q = torch.randn(w.num_seqs, C, w.num_q_heads, w.head_dim, generator=torch.Generator().manual_seed(C))
+    q = q.to(wl.DTYPES[w.query_dtype])
+    ref, _ = oracle_reference_mq(w, inst.k_scale, inst.v_scale, 0, q, tables, lens_t.tolist(), list(range(w.num_seqs)))
+    for algo in algos:
+        out = pk.paged_multi_query_attention(q.cuda(), batch.pool, 0, tables.cuda(), lens_t.cuda(),
+                                             int(lens_t.max()), w.scale, split_tokens=split, algo=algo)
+        torch.cuda.synchronize()
+        compare(out, ref, TOL[kv], "%s algo=%s split=%d" % (w.name, algo, split))
+        # queries at negative positions (sequence shorter than C) are zero rows
+        assert torch.all(out[0, 0] == 0)
+    assert batch.pool.errors() == 0
+
+
+def test_one_query_equals_decode():
+    w = _w("mq_one", 4, 2, "bf16", "bf16", (5, 100, 700))
+    inst, batch = _filled(w)
+    tables, lens = batch.tables().cuda(), batch.seq_lens().cuda()
+    q = torch.randn(w.num_seqs, 1, w.num_q_heads, w.head_dim).to(torch.bfloat16).cuda()
+    for algo in ("mma", "simt"):
+        a = pk.paged_multi_query_attention(q, batch.pool, 0, tables, lens, int(lens.max()), w.scale, algo=algo)
+        b = pk.paged_decode_attention(q[:, 0].contiguous(), batch.pool, 0, tables, lens, int(lens.max()), w.scale,
+                                      algo=algo)
+        assert torch.equal(a[:, 0], b)
