@@ -192,10 +192,15 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
  * TensorRT-LLM work?", "In-flight batching": chunked prefill).
  *   q    device [num_seqs][C][num_q_heads][head_dim];
  *   out  device [num_seqs][C][num_q_heads][head_dim];
- * other arguments as paged_decode_attention (which is the C = 1 case).  The
- * tensor-core design serves C * (num_q_heads / num_kv_heads) <= 8; the SIMT
- * design up to 8 (BF16) or 16 (F32) query rows per KV head, fewer for FP8.
- * A query whose position is negative (seq_lens[b] < C) gets a zero row.
+ * other arguments as paged_decode_attention (which is the C = 1 case);
+ * 1 <= C <= 2^20.  One launch serves a chunk of consecutive queries: up to
+ * 64 query rows per KV head (chunk x num_q_heads / num_kv_heads) for the
+ * tensor-core design, a power of two up to 16 (fewer for FP8 and BF16 pools
+ * with large groups) for the SIMT design; longer query lists run as several
+ * launches on the stream, each reading only the tokens its last query sees.
+ * Workspace (from paged_multi_query_plan) is shared by those launches in
+ * stream order.  A query whose position is negative (seq_lens[b] < C) gets a
+ * zero row.
  */
 pkv_status paged_multi_query_plan(const pkv_pool* pool, int32_t num_seqs, int32_t num_queries,
                                   int32_t num_q_heads, int32_t max_seq_len, int32_t split_tokens,
@@ -237,9 +242,9 @@ pkv_status paged_decode_attention_static_ws(const void* q, pkv_dtype q_dtype, co
 
 /* The kernel design paged_decode_attention would run for this pool, group
  * size (num_q_heads / num_kv_heads; for multi-query attention, times
- * num_queries) and request: PKV_ALGO_SIMT or
- * PKV_ALGO_MMA, or -1 when the request cannot be served.  PKV_ALGO_AUTO picks
- * MMA for BF16/FP8 pools with head_dim 128 and G in {1, 2, 4, 8} (when the
+ * the queries of one launch) and request: PKV_ALGO_SIMT or PKV_ALGO_MMA, or
+ * -1 when the request cannot be served.  PKV_ALGO_AUTO picks MMA for BF16/FP8
+ * pools with head_dim 128, block size 16/32/64 and 1 <= group <= 64 (when the
  * driver provides TMA descriptors), SIMT otherwise. */
 int32_t paged_decode_algo(const pkv_pool* pool, int32_t group, pkv_algo requested);
 

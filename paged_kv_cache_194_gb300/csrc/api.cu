@@ -43,6 +43,30 @@ size_t bal_bytes(int ctas, int G, int D) {
     return bal_o_bytes(ctas, G, D) + round_up(static_cast<size_t>(ctas) * 2 * G * sizeof(float), 256);
 }
 
+// Queries per launch.  A launch serves rows = queries x gh query rows per KV
+// head: at most kMmaMaxRows for the tensor-core design; for the SIMT design
+// a power of two up to kSimtMaxRows.  Longer query lists run as several
+// launches over consecutive query chunks.
+int mma_chunk(int gh, int C) {
+    const int cap = gh <= kMmaMaxRows ? kMmaMaxRows / gh : 1;
+    return C < cap ? C : cap;
+}
+int simt_chunk(const pkv_pool* p, int gh, int C) {
+    int cap = gh <= kSimtMaxRows ? kSimtMaxRows / gh : 1;
+    if (C < cap) cap = C;
+    int c = 1;
+    while (c * 2 <= cap) c *= 2;
+    while (c > 1 && !decode_simt_supported(p->d.kv_dtype, p->d.head_dim, c * gh)) c /= 2;
+    return c;
+}
+// Template row bound of the tensor-core kernel for `rows` rows.
+int row_bound(int rows) {
+    int p = 1;
+    while (p < rows) p *= 2;
+    return p;
+}
+constexpr int kMaxQueries = 1 << 20;
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -224,7 +248,7 @@ pkv_status paged_multi_query_plan(const pkv_pool* p, int32_t num_seqs, int32_t n
                                   int32_t max_seq_len, int32_t split_tokens, int32_t* split_out,
                                   int32_t* nsplit_out, size_t* ws_out) {
     if (!p || num_seqs < 0 || num_q_heads < 1 || max_seq_len < 0 || split_tokens < 0) return PKV_ERR_INVALID_ARG;
-    if (num_queries < 1 || num_queries > 64) return PKV_ERR_INVALID_ARG;
+    if (num_queries < 1 || num_queries > kMaxQueries) return PKV_ERR_INVALID_ARG;
     if (num_q_heads % p->d.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     int S = split_tokens;
     if (S > 0) {
@@ -241,11 +265,13 @@ pkv_status paged_multi_query_plan(const pkv_pool* p, int32_t num_seqs, int32_t n
     int64_t ns = max_seq_len > 0 ? (static_cast<int64_t>(max_seq_len) + S - 1) / S : 1;
     if (ns < 1) ns = 1;
     if (ns > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-    // layout: [counters][partials of whichever schedule the call runs]
-    size_t body = fixed_bytes(num_seqs, num_queries * num_q_heads, p->d.head_dim, ns);
-    const int G = num_queries * (num_q_heads / p->d.num_kv_heads);  // query rows per KV head
+    // layout: [counters][partials of whichever schedule the call runs], sized
+    // for the largest query chunk of either design (the tensor-core one's)
+    const int gh = num_q_heads / p->d.num_kv_heads;
+    const int cq = mma_chunk(gh, num_queries);
+    size_t body = fixed_bytes(num_seqs, cq * num_q_heads, p->d.head_dim, ns);
     if (split_tokens == 0 && num_seqs <= kMaxBalancedSeqs) {
-        const size_t bb = bal_bytes(bal_ctas(), G, p->d.head_dim);
+        const size_t bb = bal_bytes(bal_ctas(), row_bound(cq * gh), p->d.head_dim);
         if (bb > body) body = bb;
     }
     size_t ws = body > 0 ? counters_bytes(num_seqs, p->d.num_kv_heads) + body : 0;
@@ -280,7 +306,7 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
                                        pkv_algo algo, void* workspace, size_t workspace_bytes, void* out,
                                        void* stream) {
     if (!p || layer < 0 || layer >= p->d.num_layers) return PKV_ERR_INVALID_ARG;
-    if (num_queries < 1 || num_queries > 64) return PKV_ERR_INVALID_ARG;
+    if (num_queries < 1 || num_queries > kMaxQueries) return PKV_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 || max_seq_len < 0) return PKV_ERR_INVALID_ARG;
     if (num_q_heads % p->d.num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * p->d.block_size)
@@ -294,18 +320,19 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
     if (!q || !out || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PKV_ERR_INVALID_ARG;
-    const int G = num_queries * (num_q_heads / p->d.num_kv_heads);  // query rows per KV head
+    const int gh = num_q_heads / p->d.num_kv_heads;  // query heads per KV head
+    const int cq_mma = mma_chunk(gh, num_queries), cq_simt = simt_chunk(p, gh, num_queries);
 
     bool use_mma = false;
     pkv_pool* mp = const_cast<pkv_pool*>(p);  // the handle caches its TMA descriptors
+    const bool mma_fits = decode_mma_supported(p->d.kv_dtype, p->d.head_dim, cq_mma * gh, p->d.block_size);
     if (algo == PKV_ALGO_MMA) {
-        if (!decode_mma_supported(p->d.kv_dtype, p->d.head_dim, G, p->d.block_size)) return PKV_ERR_UNSUPPORTED;
-        if (!ensure_tmaps(mp)) return PKV_ERR_UNSUPPORTED;
+        if (!mma_fits || !ensure_tmaps(mp)) return PKV_ERR_UNSUPPORTED;
         use_mma = true;
     } else if (algo == PKV_ALGO_AUTO) {
-        use_mma = decode_mma_supported(p->d.kv_dtype, p->d.head_dim, G, p->d.block_size) && ensure_tmaps(mp);
+        use_mma = mma_fits && ensure_tmaps(mp);
     }
-    if (!use_mma && !decode_simt_supported(p->d.kv_dtype, p->d.head_dim, G)) return PKV_ERR_UNSUPPORTED;
+    if (!use_mma && !decode_simt_supported(p->d.kv_dtype, p->d.head_dim, cq_simt * gh)) return PKV_ERR_UNSUPPORTED;
 
     int32_t S = 0, NS = 0;
     size_t need = 0;
@@ -327,7 +354,7 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
     a.max_blocks = max_blocks_per_seq;
     a.max_len = max_seq_len;
     a.num_seqs = num_seqs;
-    a.num_queries = num_queries;
+    a.q_total = num_queries;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = p->d.num_kv_heads;
     a.head_dim = p->d.head_dim;
@@ -346,18 +373,31 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
         if (balanced) {
             a.bal_max_ctas = bal_ctas();
             a.bal_o = reinterpret_cast<float*>(body);
-            a.bal_lse = reinterpret_cast<float*>(body + bal_o_bytes(a.bal_max_ctas, G, p->d.head_dim));
+            a.bal_lse = reinterpret_cast<float*>(body + bal_o_bytes(a.bal_max_ctas, row_bound(cq_mma * gh),
+                                                                    p->d.head_dim));
         } else if (NS > 1) {
-            const size_t rows = static_cast<size_t>(num_seqs) * num_queries * num_q_heads * NS;
+            const size_t rows = static_cast<size_t>(num_seqs) * cq_mma * num_q_heads * NS;
             a.o_part = reinterpret_cast<float*>(body);
             a.lse_part = reinterpret_cast<float*>(body + round_up(rows * p->d.head_dim * sizeof(float), 256));
         }
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = use_mma ? launch_decode_mma(p->d.kv_dtype, a, &p->tmap_k, &p->tmap_v, s)
-                            : launch_decode_simt(p->d.kv_dtype, a, s);
-    if (e != cudaSuccess) return cuda_status(e);
-    if (!balanced && NS > 1) return cuda_status(launch_combine(q_dtype, a, s));
+    // one launch (plus combine) per query chunk; a chunk reads only the tokens
+    // its last query can see
+    for (int c0 = 0; c0 < num_queries;) {
+        int cq = use_mma ? mma_chunk(gh, num_queries - c0) : simt_chunk(p, gh, num_queries - c0);
+        a.q_first = c0;
+        a.num_queries = cq;
+        a.len_trim = num_queries - c0 - cq;
+        cudaError_t e = use_mma ? launch_decode_mma(p->d.kv_dtype, a, &p->tmap_k, &p->tmap_v, s)
+                                : launch_decode_simt(p->d.kv_dtype, a, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        if (!balanced && NS > 1) {
+            e = launch_combine(q_dtype, a, s);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        c0 += cq;
+    }
     return PKV_OK;
 }
 

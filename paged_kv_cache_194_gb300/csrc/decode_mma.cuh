@@ -1,0 +1,1142 @@
+// Paged attention over the KV pool, tensor-core design (BF16 and FP8-E4M3
+// pools, head_dim 128), for one or several queries per sequence.
+//
+// "How does TensorRT-LLM work?", "Custom attention kernels": one kernel does
+// the whole attention step and keeps the intermediate scores on chip.
+// "Introduction to TensorRT-LLM", figure "TensorRT-LLM Acceleration Stack":
+// Flash-Decoding splits the key/value length across CTAs and merges the
+// pieces by their log-sum-exp.
+//
+// Query rows.  A CTA serves one KV head of one sequence and the NQ query rows
+// that share it: gh query heads (grouped-query attention) times C queries of
+// the sequence, row n = c * gh + g.  C = 1 is decode; C > 1 verifies drafted
+// tokens or processes a prompt chunk: the queries sit at the last C positions
+// of the visible length L and query c sees positions < L - C + c + 1.  NQ is
+// the template bound (1, 2, 4, ..., 64); the real row count may be smaller
+// (the rest is zero padding).  Longer query lists are served by several
+// launches (the host splits them).
+//
+// Work is a list of tiles (64 tokens for BF16, 128 for FP8) of (sequence, KV
+// head) pairs.  Two schedules share the same producer and consumer code:
+//  * balanced (the default): a persistent grid of 2 CTAs per SM (1 for the
+//    64-row bound); CTA c takes
+//    the contiguous tile range [c*T/P, (c+1)*T/P) of the flattened list
+//    (T tiles, P CTAs), so every CTA streams the same number of KV bytes
+//    whatever the length mix.  A (sequence, KV head) whose tiles straddle
+//    CTAs leaves one fp32 partial per CTA; the CTA that finishes that pair
+//    last (an atomic counter in the workspace, no waiting) merges the
+//    partials by their log-sum-exp and writes the output.
+//  * fixed splits (when the caller names a split size): one CTA per
+//    (split, KV head, sequence); partials go to the combine kernel.
+// CTA = 4 consumer warps + 1 producer warp.
+//  * Producer: one lane walks the block table and issues, per stage, one TMA
+//    tile load (cp.async.bulk.tensor, 128-byte swizzle) per block of K and of
+//    V: for BF16 a 3D box {64 columns, bs rows, 2 halves} fetches a block's
+//    whole 256-byte rows at once (two 2D boxes if the driver refuses that
+//    descriptor).  At the first tile of a segment it also bulk-copies the
+//    query rows into the stage.  A full mbarrier counts the bytes, an empty
+//    mbarrier (4 arrivals) frees the stage; a per-stage TileInfo tells the
+//    consumers what the stage holds and marks the CTA's last tile.
+//    Every KV byte crosses HBM once per launch; all query rows share it.
+//  * Consumers: a grid of kWT token groups x kWC column groups of warps.  Up
+//    to 8 query rows (decode) the 4 warps split the tokens of a stage and each
+//    holds all columns; beyond 8 they split the columns (8 per n-tile, 1 or 2
+//    n-tiles per warp) and read the same tokens.  Per 16-token m-tile:
+//      S^T[16 tok x 8] = K[16 x 128] . Q^T[128 x 8]   8 x mma.m16n8k16 per n-tile
+//      (tokens fill M; query rows fill N)
+//      online softmax on the fragment (3 shuffles per max, exp2 with the
+//      scale*log2(e) folded in), P packed to 16 bits and transposed in
+//      registers with movmatrix into the B operand of
+//      O^T[128 x 8] += V^T[128 x 16 tok] . P^T[16 tok x 8]  8 x mma per n-tile
+//      (V^T through ldmatrix.trans for BF16).  The K and V fragments loaded
+//      for an m-tile serve every n-tile of the warp.
+//  * FP8 pools: E4M3 converts exactly to f16 in registers and the mma runs
+//    f16 x f16 -> f32.  K is read with ldmatrix and the head_dim order is
+//    permuted consistently in K and Q (a dot product does not depend on the
+//    order of its terms); V^T pairs two tokens' bytes with one byte_perm.
+//    Q is converted from BF16 to f16 (exact for |q| in [2^-14, 65504]).
+//  * At a segment's end the token groups' (m, l, O) are merged through shared
+//    memory and the CTA writes the final rows or its fp32 partials.  When a
+//    dedicated merge area would cost the second CTA per SM, the merge uses the
+//    buffer of the segment's last stage, which is released only afterwards.
+// Rows past the sequence end inside a loaded block are masked in S and zeroed
+// in V (uninitialised pool bytes could hold NaN patterns, and 0 * NaN = NaN).
+// Every mbarrier wait is bounded; on expiry the CTA flags PKV_ERRBIT_TIMEOUT,
+// drains its in-flight copies (bounded) and skips its output.
+#pragma once
+
+#include <cuda.h>
+
+#include "device_common.cuh"
+
+namespace pkv {
+
+// Per-dtype translation units.
+cudaError_t launch_decode_mma_bf16(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   cudaStream_t stream);
+cudaError_t launch_decode_mma_fp8(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  cudaStream_t stream);
+
+namespace {
+
+constexpr int kCWarps = 4;
+constexpr int kMmaThreads = (kCWarps + 1) * 32;
+constexpr int kBoxRowBytes = 128;          // one swizzled TMA row
+constexpr int kD = 128;                    // head_dim served by this design
+constexpr uint32_t kSpinLimit = 1u << 22;  // try_wait polls before a wait gives up
+constexpr size_t kTwoCtaSmem = 115712;     // dynamic shared memory per CTA that still lets 2 CTAs share an SM
+constexpr size_t kOneCtaSmem = 232448;     // the per-CTA maximum
+
+template <int DT>
+struct MmaCfg;
+template <>
+struct MmaCfg<PKV_BF16> {
+    static constexpr int kHalves = 2;  // 128 columns = two 64-column (128-byte) halves
+    static constexpr int kMT = 1;      // 16-token m-tiles per consume step
+};
+template <>
+struct MmaCfg<PKV_FP8_E4M3> {
+    static constexpr int kHalves = 1;  // 128 one-byte columns = one 128-byte row
+    static constexpr int kMT = 2;      // two independent m-tiles per step: half the bytes per token need more ILP
+};
+
+// What one pipeline stage holds.
+struct TileInfo {
+    int b, h;       // sequence, KV head
+    int L;          // the sequence's visible length
+    int tok0, n;    // first token of the tile, valid tokens in it (1..kTT)
+    int flags;      // kSeg* / kEnd bits
+    int pieces;     // CTAs that share this (sequence, KV head)
+    int c_first;    // the first of them
+    int s_first;    // partial slot that first CTA uses
+};
+constexpr int kSegFirst = 1;  // first tile of a segment (load q, reset state)
+constexpr int kSegLast = 2;   // last tile of a segment (merge and emit)
+constexpr int kSegWhole = 4;  // the segment is the whole sequence
+constexpr int kCtaFirst = 8;  // the segment holds the CTA's first tile
+constexpr int kEnd = 16;      // no tiles at all (a CTA that owns none)
+constexpr int kCtaLast = 32;  // the CTA's last tile
+
+// Shared memory of one CTA:
+//   stages: [kStages][K, V][block of the tile][half][bs rows][128 B]
+//     A block's two halves (head_dim 0-63 and 64-127 for BF16) are bs*128
+//     bytes apart; both start on 1024-byte boundaries (bs >= 16), so the
+//     128-byte swizzle phase of a row is its row index within the block, mod 8.
+//   q slots [kStages][NQ][128] BF16, tile info [kStages],
+//   merge m, l [kWT][NQ] + one flag word,
+//   merge O [kWT][NQ][128] fp32 (dedicated, or in the segment's last stage),
+//   barriers full[kStages], empty[kStages], consumer sync, abort word.
+template <int DT, int NQ>
+struct Layout {
+    static constexpr int kHalves = MmaCfg<DT>::kHalves;
+    static constexpr int kMT = MmaCfg<DT>::kMT;
+    static constexpr int kTT = 16 * kCWarps * kMT;  // tokens per stage
+    // warp grid: kWC column groups x kWT token groups
+    static constexpr int kWC = NQ <= 8 ? 1 : (NQ / 8 < kCWarps ? NQ / 8 : kCWarps);
+    static constexpr int kWT = kCWarps / kWC;
+    static constexpr int kNT = NQ <= 8 ? 1 : NQ / (8 * kWC);  // n-tiles (8 columns) per warp
+    static constexpr int kRowsPerWarp = kTT / kWT;
+    static constexpr int kSteps = kRowsPerWarp / (16 * kMT);  // consume steps per warp per stage
+    // Up to 32 rows: 2 CTAs per SM (the register cap is then 168 per thread).
+    // 64 rows need two n-tiles of accumulators per warp: 1 CTA per SM with
+    // twice the stages keeps as many bytes in flight.
+    static constexpr int kMinBlocks = NQ <= 32 ? 2 : 1;
+    static constexpr size_t kBudget = kMinBlocks == 2 ? kTwoCtaSmem : kOneCtaSmem;
+    static constexpr int kStages = NQ <= 16 ? 3 : (kMinBlocks == 2 ? 2 : 4);
+    static constexpr int kTensorBytes = kHalves * kTT * kBoxRowBytes;
+    static constexpr int kStageBytes = 2 * kTensorBytes;
+    static constexpr int kQBytes = NQ * kD * 2;
+    static constexpr size_t kQOff = static_cast<size_t>(kStages) * kStageBytes;
+    static constexpr size_t kInfoOff = kQOff + static_cast<size_t>(kStages) * kQBytes;
+    static constexpr size_t kMlOff = kInfoOff + static_cast<size_t>(kStages) * sizeof(TileInfo);
+    static constexpr size_t kMlBytes = (static_cast<size_t>(kWT) * NQ * 2 + 4) * 4;
+    static constexpr size_t kMergeOBytes = static_cast<size_t>(kWT) * NQ * kD * 4;
+    static constexpr size_t kCtl = (2 * kStages + 1) * 8 + 16;  // barriers + abort word
+    static constexpr size_t kBase = (kMlOff + kMlBytes + 15) / 16 * 16;
+    static constexpr bool kMergeInStage = kBase + kMergeOBytes + kCtl + 1024 > kBudget;
+    static constexpr size_t kMergeOff = kBase;  // dedicated merge O (unused when kMergeInStage)
+    static constexpr size_t kBarOff = kBase + (kMergeInStage ? 0 : kMergeOBytes);
+    static constexpr size_t kBytes = kBarOff + kCtl;
+    static constexpr size_t kAlloc = kBytes + 1024;  // + alignment slack
+    static_assert(kMergeOBytes <= static_cast<size_t>(kStageBytes), "the merge area must fit in a stage");
+    static_assert(kNT * 8 * kWC >= NQ && kSteps >= 1, "warp grid must cover the rows");
+    static_assert(kAlloc <= kBudget, "shared memory budget");
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+template <int kImm = 0>
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1+%2];\n" : "=r"(v) : "r"(addr), "n"(kImm) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+
+template <int DT>
+__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    if constexpr (DT == PKV_BF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
+// Two floats -> packed 16-bit pair (low = lo) in the mma operand type.
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (DT == PKV_BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+// Two E4M3 codes (low byte first) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+    __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
+    return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `lr` inside a 128B-swizzled run
+// of rows whose first row sits on a 1024-byte boundary (and is a multiple of 8
+// rows into the run).
+__device__ __forceinline__ uint32_t swz(int lr, int chunk) {
+    return static_cast<uint32_t>(lr * kBoxRowBytes + ((chunk ^ (lr & 7)) << 4));
+}
+
+// Head-dim index held by O^T accumulator row `m` (0..15) of m-tile `mt`.
+template <int DT>
+__device__ __forceinline__ int o_dim(int mt, int m) {
+    if constexpr (DT == PKV_BF16) {
+        return mt * 16 + m;
+    } else {  // m-tiles (2j, 2j+1) rows (r, r+8) -> 32j + 4r + {0,1,2,3}
+        const int j = mt >> 1, r = m & 7;
+        return 32 * j + 4 * r + ((mt & 1) << 1) + (m >> 3);
+    }
+}
+
+// ---------------------------------------------------------------- consumers
+// State of one warp's NT n-tiles; lane (r, q) = (lane / 4, lane % 4) holds
+// columns 2q and 2q+1 of each n-tile.
+template <int NT>
+struct Acc {
+    float m[NT][2];        // running max (log2 domain) per column
+    float l[NT][2];        // lane-partial running sums
+    float o[8][NT][4];     // O^T accumulator fragments (8 m-tiles of head_dim)
+    uint32_t bq[8][NT][2]; // Q^T as the mma B operand, per 16-wide k-step
+};
+
+// Start a segment: clear the state and build the Q^T fragments of columns
+// [col0, col0 + 8*NT) from the stage's query rows qs[NQ][128] (BF16, shared
+// memory); columns >= nq are zero padding.
+template <int DT, int NT>
+__device__ __forceinline__ void acc_begin(Acc<NT>& s, const __nv_bfloat16* qs, int lane, int col0, int nq) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        s.m[j][0] = s.m[j][1] = -INFINITY;
+        s.l[j][0] = s.l[j][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) s.o[mt][j][0] = s.o[mt][j][1] = s.o[mt][j][2] = s.o[mt][j][3] = 0.f;
+    }
+    const int r = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const int n = col0 + 8 * j + r;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            if (n >= nq) {
+                s.bq[ks][j][0] = s.bq[ks][j][1] = 0u;
+                continue;
+            }
+            if constexpr (DT == PKV_BF16) {
+                const uint32_t* w = reinterpret_cast<const uint32_t*>(qs + n * kD + ks * 16 + 2 * q);
+                s.bq[ks][j][0] = w[0];
+                s.bq[ks][j][1] = w[4];  // +8 elements
+            } else {  // head_dim order permuted like K's: chunk ks, bytes 4q..4q+3
+                const __nv_bfloat16* p = qs + n * kD + ks * 16 + 4 * q;
+                s.bq[ks][j][0] = pack2<DT>(__bfloat162float(p[0]), __bfloat162float(p[1]));
+                s.bq[ks][j][1] = pack2<DT>(__bfloat162float(p[2]), __bfloat162float(p[3]));
+            }
+        }
+    }
+}
+
+// Per-lane byte offsets (relative to the warp's first row in a tensor of a
+// stage) of the shared-memory fragments a consumer lane reads every tile;
+// they depend only on the lane, so they are computed once.
+struct LaneOffsets {
+    uint32_t k[4];  // K ldmatrix rows: chunk pair i (BF16: + half * half_stride)
+    uint32_t v[8];  // BF16: V ldmatrix.trans, chunk pair i (4 used); FP8: V bytes, (j, row ta / ta+1)
+};
+
+template <int DT>
+__device__ __forceinline__ LaneOffsets lane_offsets(int lane) {
+    LaneOffsets o;
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // K: row (of the warp's 16) this lane addresses
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o.k[i] = swz(lrow, 2 * i + (lane >> 4));
+    if constexpr (DT == PKV_BF16) {
+        const int trow = (lane & 7) + ((lane >> 4) & 1) * 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o.v[i] = swz(trow, 2 * i + ((lane >> 3) & 1));
+#pragma unroll
+        for (int i = 4; i < 8; ++i) o.v[i] = 0;
+    } else {
+        const int r = lane >> 2, q = lane & 3;
+        const uint32_t inner = static_cast<uint32_t>((r & 3) * 4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            o.v[2 * j] = swz(2 * q, 2 * j + (r >> 2)) + inner;
+            o.v[2 * j + 1] = swz(2 * q + 1, 2 * j + (r >> 2)) + inner;
+        }
+    }
+    return o;
+}
+
+// One consume step: this warp's MT m-tiles of 16 rows, [row0, row0 + 16*MT)
+// (n valid rows in the stage), against its NT n-tiles.  wb[i]: byte offset of
+// m-tile i's first row in a tensor of the stage; half_stride: bytes between a
+// block's two 64-column halves.  The m-tiles' S chains are interleaved and
+// share one softmax update.  lim[j][0/1]: rows of the tile visible to this
+// lane's two columns of n-tile j (all <= n; equal to n for decode).
+template <int DT, int MT, int NT>
+__device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* vst, int n, int row0, int lane,
+                                             const uint32_t (&wb)[MT], uint32_t half_stride, float qk,
+                                             const LaneOffsets& lo, const int (&lim)[NT][2]) {
+    constexpr int kHalves = MmaCfg<DT>::kHalves;
+    if (row0 >= n) return;
+    const int r = lane >> 2;
+    if (n < row0 + 16 * MT) {  // zero these V rows past the end (other column groups write the same zeros)
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            if (row0 + 16 * i >= n) continue;  // a fully empty m-tile is skipped below
+            for (int e = lane; e < 16 * kHalves * 8; e += 32) {
+                const int lr = e / (kHalves * 8);
+                const int rest = e % (kHalves * 8);
+                if (row0 + 16 * i + lr >= n)
+                    *reinterpret_cast<uint4*>(vst + wb[i] + (rest >> 3) * half_stride + lr * kBoxRowBytes +
+                                              (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        fence_proxy_async();
+        __syncwarp();
+    }
+    bool live[MT];
+#pragma unroll
+    for (int i = 0; i < MT; ++i) live[i] = row0 + 16 * i < n;
+    // ---- S^T = K Q^T, m-tiles interleaved; one K fragment feeds every n-tile
+    float sc[MT][NT][4];
+#pragma unroll
+    for (int i = 0; i < MT; ++i)
+#pragma unroll
+        for (int j = 0; j < NT; ++j) sc[i][j][0] = sc[i][j][1] = sc[i][j][2] = sc[i][j][3] = 0.f;
+    const uint32_t kb = smem_u32(kst);
+    if constexpr (DT == PKV_BF16) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                if (!live[i]) continue;
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kb + wb[i] + (ks >> 2) * half_stride + lo.k[ks & 3], a0, a1, a2, a3);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) mma16816<DT>(sc[i][j], a0, a1, a2, a3, s.bq[ks][j][0], s.bq[ks][j][1]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {  // two k-steps (chunks 2kp, 2kp+1) per ldmatrix.x4
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                if (!live[i]) continue;
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4(kb + wb[i] + lo.k[kp], r0, r1, r2, r3);
+                const uint32_t c0 = e4m3x2_to_f16x2(r0), c1 = e4m3x2_to_f16x2(r1);
+                const uint32_t c2 = e4m3x2_to_f16x2(r0 >> 16), c3 = e4m3x2_to_f16x2(r1 >> 16);
+                const uint32_t c4 = e4m3x2_to_f16x2(r2), c5 = e4m3x2_to_f16x2(r3);
+                const uint32_t c6 = e4m3x2_to_f16x2(r2 >> 16), c7 = e4m3x2_to_f16x2(r3 >> 16);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    mma16816<DT>(sc[i][j], c0, c1, c2, c3, s.bq[2 * kp][j][0], s.bq[2 * kp][j][1]);
+                    mma16816<DT>(sc[i][j], c4, c5, c6, c7, s.bq[2 * kp + 1][j][0], s.bq[2 * kp + 1][j][1]);
+                }
+            }
+        }
+    }
+    // ---- online softmax (log2 domain) over the step's 16*MT rows, per column
+    float sv[MT][NT][4];
+    float x[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) x[j][0] = x[j][1] = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+        const int ra = row0 + 16 * i + r, rb = ra + 8;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            sv[i][j][0] = ra < lim[j][0] ? sc[i][j][0] * qk : -INFINITY;
+            sv[i][j][1] = ra < lim[j][1] ? sc[i][j][1] * qk : -INFINITY;
+            sv[i][j][2] = rb < lim[j][0] ? sc[i][j][2] * qk : -INFINITY;
+            sv[i][j][3] = rb < lim[j][1] ? sc[i][j][3] * qk : -INFINITY;
+            x[j][0] = fmaxf(x[j][0], fmaxf(sv[i][j][0], sv[i][j][2]));
+            x[j][1] = fmaxf(x[j][1], fmaxf(sv[i][j][1], sv[i][j][3]));
+        }
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            x[j][0] = fmaxf(x[j][0], __shfl_xor_sync(0xFFFFFFFFu, x[j][0], off));
+            x[j][1] = fmaxf(x[j][1], __shfl_xor_sync(0xFFFFFFFFu, x[j][1], off));
+        }
+    }
+    // a column that has seen no token yet keeps max -inf; b = its exponent base
+    float nm[NT][2], bb[NT][2];
+    bool moved = false;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            nm[j][h] = fmaxf(s.m[j][h], x[j][h]);
+            bb[j][h] = nm[j][h] == -INFINITY ? 0.f : nm[j][h];
+            moved = moved || nm[j][h] != s.m[j][h];
+        }
+    }
+    float p[MT][NT][4];
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            p[i][j][0] = exp2f(sv[i][j][0] - bb[j][0]);
+            p[i][j][1] = exp2f(sv[i][j][1] - bb[j][1]);
+            p[i][j][2] = exp2f(sv[i][j][2] - bb[j][0]);
+            p[i][j][3] = exp2f(sv[i][j][3] - bb[j][1]);
+        }
+    }
+    // rescale only when some running max moved (the factor is exactly 1
+    // otherwise); against b, a column still without tokens gets 0, not 2^NaN
+    if (__any_sync(0xFFFFFFFFu, moved)) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const float al0 = exp2f(s.m[j][0] - bb[j][0]), al1 = exp2f(s.m[j][1] - bb[j][1]);
+            s.l[j][0] *= al0;
+            s.l[j][1] *= al1;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                s.o[mt][j][0] *= al0;
+                s.o[mt][j][1] *= al1;
+                s.o[mt][j][2] *= al0;
+                s.o[mt][j][3] *= al1;
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            s.l[j][0] += p[i][j][0] + p[i][j][2];
+            s.l[j][1] += p[i][j][1] + p[i][j][3];
+        }
+        s.m[j][0] = nm[j][0];
+        s.m[j][1] = nm[j][1];
+    }
+    uint32_t pb[MT][NT][2];
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            pb[i][j][0] = movmatrix_t(pack2<DT>(p[i][j][0], p[i][j][1]));  // tokens 0-7 of m-tile i
+            pb[i][j][1] = movmatrix_t(pack2<DT>(p[i][j][2], p[i][j][3]));  // tokens 8-15
+        }
+    }
+    // ---- O^T += V^T P^T; one V fragment feeds every n-tile
+    const uint32_t vb0 = smem_u32(vst);
+    if constexpr (DT == PKV_BF16) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                if (!live[i]) continue;
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vb0 + wb[i] + (mt >> 2) * half_stride + lo.v[mt & 3], a0, a1, a2, a3);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) mma16816<DT>(s.o[mt][j], a0, a1, a2, a3, pb[i][j][0], pb[i][j][1]);
+            }
+        }
+    } else {
+        // rows ta, ta+1 (ta = 2q) at offsets v[2c], v[2c+1]; rows ta+8, ta+9 are 8 rows (1024 B) further
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                if (!live[i]) continue;
+                const uint32_t vb_ = vb0 + wb[i];
+                const uint32_t w0 = lds32(vb_ + lo.v[2 * c]);
+                const uint32_t w1 = lds32(vb_ + lo.v[2 * c + 1]);
+                const uint32_t w8 = lds32<8 * kBoxRowBytes>(vb_ + lo.v[2 * c]);
+                const uint32_t w9 = lds32<8 * kBoxRowBytes>(vb_ + lo.v[2 * c + 1]);
+                const uint32_t x01 = __byte_perm(w0, w1, 0x5140), x23 = __byte_perm(w0, w1, 0x7362);
+                const uint32_t y01 = __byte_perm(w8, w9, 0x5140), y23 = __byte_perm(w8, w9, 0x7362);
+                const uint32_t e0 = e4m3x2_to_f16x2(x01), e1 = e4m3x2_to_f16x2(x01 >> 16);
+                const uint32_t e2 = e4m3x2_to_f16x2(y01), e3 = e4m3x2_to_f16x2(y01 >> 16);
+                const uint32_t f0 = e4m3x2_to_f16x2(x23), f1 = e4m3x2_to_f16x2(x23 >> 16);
+                const uint32_t f2 = e4m3x2_to_f16x2(y23), f3 = e4m3x2_to_f16x2(y23 >> 16);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    mma16816<DT>(s.o[2 * c][j], e0, e1, e2, e3, pb[i][j][0], pb[i][j][1]);
+                    mma16816<DT>(s.o[2 * c + 1][j], f0, f1, f2, f3, pb[i][j][0], pb[i][j][1]);
+                }
+            }
+        }
+    }
+}
+
+// Merge area: O [token group][NQ][128], m and l [token group][NQ], a flag word.
+template <int NQ, int WT>
+struct Merge {
+    float* o;
+    float* m;
+    float* l;
+    volatile int* flag;
+    __device__ Merge(uint8_t* o_base, uint8_t* ml_base) {
+        o = reinterpret_cast<float*>(o_base);
+        m = reinterpret_cast<float*>(ml_base);
+        l = m + WT * NQ;
+        flag = reinterpret_cast<volatile int*>(l + WT * NQ);
+    }
+};
+
+// Publish this warp's (m, l, O) for its columns [col0, col0 + 8*NT) as token group wt.
+template <int DT, int NQ, int WT, int NT>
+__device__ __forceinline__ void merge_put(const Acc<NT>& s, const Merge<NQ, WT>& mg, int wt, int col0, int lane) {
+    const int r = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        float l0 = s.l[j][0], l1 = s.l[j][1];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
+            l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
+        }
+        const int n0 = col0 + 8 * j + 2 * q, n1 = n0 + 1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            if (n0 < NQ) {
+                mg.o[(wt * NQ + n0) * kD + o_dim<DT>(mt, r)] = s.o[mt][j][0];
+                mg.o[(wt * NQ + n0) * kD + o_dim<DT>(mt, r + 8)] = s.o[mt][j][2];
+            }
+            if (n1 < NQ) {
+                mg.o[(wt * NQ + n1) * kD + o_dim<DT>(mt, r)] = s.o[mt][j][1];
+                mg.o[(wt * NQ + n1) * kD + o_dim<DT>(mt, r + 8)] = s.o[mt][j][3];
+            }
+        }
+        if (lane < 4) {
+            if (n0 < NQ) {
+                mg.m[wt * NQ + n0] = s.m[j][0];
+                mg.l[wt * NQ + n0] = l0;
+            }
+            if (n1 < NQ) {
+                mg.m[wt * NQ + n1] = s.m[j][1];
+                mg.l[wt * NQ + n1] = l1;
+            }
+        }
+    }
+}
+
+// Merged (sum O, max m, sum l) of column n at head-dim index d.
+template <int NQ, int WT>
+__device__ __forceinline__ void merge_get(const Merge<NQ, WT>& mg, int n, int d, float& acc, float& M, float& lsum) {
+    M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WT; ++w) M = fmaxf(M, mg.m[w * NQ + n]);
+    acc = 0.f;
+    lsum = 0.f;
+    if (M == -INFINITY) return;  // no token for this query in the segment
+#pragma unroll
+    for (int w = 0; w < WT; ++w) {
+        const float f = exp2f(mg.m[w * NQ + n] - M);  // token groups without rows: 2^-inf = 0
+        acc += f * mg.o[(w * NQ + n) * kD + d];
+        lsum += f * mg.l[w * NQ + n];
+    }
+}
+
+// Output row of column n of (sequence b, KV head h): query q_first + n / gh,
+// head h * gh + n % gh.
+__device__ __forceinline__ size_t out_row(const DecodeArgs& a, int b, int h, int n, int gh) {
+    return (static_cast<size_t>(b) * a.q_total + a.q_first + n / gh) * a.num_q_heads + static_cast<size_t>(h) * gh +
+           n % gh;
+}
+
+// ---------------------------------------------------------------- producer
+// Stage s <- tile ti: tile info, the query rows at a segment's first tile,
+// and one TMA box per KV block (K and V).  All 32 producer lanes call it
+// (they share the block-table window); lane 0 issues.
+template <int DT, int NQ>
+__device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                            uint8_t* smem, uint64_t* full, int s, const TileInfo& ti,
+                                            const int32_t* table, int& cache, int& cache_base, int lane, int gh) {
+    using Lt = Layout<DT, NQ>;
+    const int bs = a.block_size;
+    uint8_t* kst = smem + s * Lt::kStageBytes;
+    uint8_t* vst = kst + Lt::kTensorBytes;
+    const uint32_t fb = smem_u32(&full[s]);
+    const int nblk = (ti.n + bs - 1) / bs;
+    const bool need_q = (ti.flags & kSegFirst) != 0;
+    if (lane == 0) {
+        reinterpret_cast<TileInfo*>(smem + Lt::kInfoOff)[s] = ti;
+        const uint32_t qbytes = static_cast<uint32_t>(a.num_queries * gh * kD * 2);
+        mbar_expect_tx(fb, static_cast<uint32_t>(nblk * bs * kBoxRowBytes * Lt::kHalves * 2) + (need_q ? qbytes : 0u));
+        if (need_q) {  // query rows n = c * gh + g: one copy of gh contiguous rows per query
+            for (int c = 0; c < a.num_queries; ++c) {
+                const __nv_bfloat16* qsrc = static_cast<const __nv_bfloat16*>(a.q) + out_row(a, ti.b, ti.h, c * gh, gh) * kD;
+                bulk_load(smem_u32(smem + Lt::kQOff + s * Lt::kQBytes + c * gh * kD * 2), qsrc,
+                          static_cast<uint32_t>(gh * kD * 2), fb);
+            }
+        }
+    }
+    const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
+    for (int k = 0; k < nblk; ++k) {
+        const int j = ti.tok0 / bs + k;  // block index within the sequence
+        if (cache_base < 0 || j - cache_base >= 32 || j < cache_base) {
+            cache_base = j & ~31;
+            const int idx = cache_base + lane;
+            cache = idx < a.max_blocks ? table[idx] : -1;
+        }
+        int blk = __shfl_sync(0xFFFFFFFFu, cache, j - cache_base);
+        if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks)) {
+            if (lane == 0 && a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
+            blk = 0;  // read an in-bounds block; the flag marks the output invalid
+        }
+        if (lane == 0) {
+            const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + ti.h) * bs);
+            const uint32_t off = k * Lt::kHalves * bs * kBoxRowBytes;
+            if (Lt::kHalves == 2 && a.tma_3d) {  // one box: both 128-byte halves of every row
+                tma_load_3d(smem_u32(kst + off), tmk, 0, y, 0, fb);
+                tma_load_3d(smem_u32(vst + off), tmv, 0, y, 0, fb);
+            } else {
+                for (int hf = 0; hf < Lt::kHalves; ++hf) {
+                    const uint32_t o2 = off + hf * bs * kBoxRowBytes;
+                    tma_load_2d(smem_u32(kst + o2), tmk, hf * 64, y, fb);
+                    tma_load_2d(smem_u32(vst + o2), tmv, hf * 64, y, fb);
+                }
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Tiles of sequence b (kTT tokens each), 0 past the batch.
+template <int kTT>
+__device__ __forceinline__ int seq_tiles(const DecodeArgs& a, int b) {
+    return b < a.num_seqs ? (visible_len(a, b, false) + kTT - 1) / kTT : 0;
+}
+
+// kBal: balanced persistent schedule (grid = P CTAs); otherwise one CTA per
+// (split, KV head, sequence) with grid (num_splits, num_kv_heads, num_seqs).
+template <int DT, int NQ, bool kBal>
+__global__ void __launch_bounds__(kMmaThreads, Layout<DT, NQ>::kMinBlocks)
+decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const DecodeArgs a) {
+    using Lt = Layout<DT, NQ>;
+    constexpr int kStages = Lt::kStages;
+    constexpr int kHalves = Lt::kHalves;
+    constexpr int kMT = Lt::kMT;
+    constexpr int kTT = Lt::kTT;
+    constexpr int kWC = Lt::kWC;
+    constexpr int kWT = Lt::kWT;
+    constexpr int kNT = Lt::kNT;
+    constexpr int kSteps = Lt::kSteps;
+    constexpr bool kInStage = Lt::kMergeInStage;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lt::kBarOff);
+    uint64_t* empty = full + kStages;
+    uint64_t* csync_bar = empty + kStages;  // the 4 consumer warps meet here at segment ends
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(csync_bar + 1);
+    const TileInfo* info = reinterpret_cast<const TileInfo*>(smem + Lt::kInfoOff);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gh = a.num_q_heads / a.num_kv_heads;  // query heads per KV head
+    const int nq = a.num_queries * gh;              // real query rows (<= NQ)
+
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream (the append): nothing is read before that grid has finished.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
+    // fixed schedule: this CTA's one segment
+    int fb_ = 0, fh_ = 0, fsplit = 0, t_begin = 0, t_end = 0, fL = 0;
+    if constexpr (!kBal) {
+        fsplit = blockIdx.x;
+        fh_ = blockIdx.y;
+        fb_ = blockIdx.z;
+        const int L = visible_len(a, fb_, fsplit == 0 && fh_ == 0 && threadIdx.x == 0);
+        fL = L;
+        t_begin = fsplit * a.split_tokens;
+        t_end = min(L, t_begin + a.split_tokens);
+        if (t_begin >= t_end) {
+            if (a.num_splits == 1) {  // nothing visible: zero output rows
+                for (int i = threadIdx.x; i < nq * kD; i += kMmaThreads)
+                    static_cast<__nv_bfloat16*>(a.out)[out_row(a, fb_, fh_, i / kD, gh) * kD + i % kD] =
+                        __float2bfloat16_rn(0.f);
+            }
+            return;
+        }
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), kCWarps);
+        }
+        mbar_init(smem_u32(csync_bar), kCWarps);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == kCWarps) {
+        // ------------------------------------------------------------ producer
+        int cache = -1, cache_base = -1;
+        long long k = 0;  // stages issued
+        bool ok = true;
+        auto acquire = [&](long long kk) -> int {  // stage for the kk-th issue, after it is free
+            const int s = static_cast<int>(kk % kStages);
+            if (kk >= kStages && ok) ok = mbar_wait(smem_u32(&empty[s]), static_cast<uint32_t>(((kk / kStages) - 1) & 1));
+            if (*abort_flag) ok = false;
+            return s;
+        };
+        if constexpr (kBal) {
+            const int B = a.num_seqs, Hkv = a.num_kv_heads;
+            long long T = 0;
+#pragma unroll 4
+            for (int b0 = 0; b0 < B; b0 += 32) T += warp_sum_ll(seq_tiles<kTT>(a, b0 + lane));
+            T *= Hkv;
+            // CTA c < P owns tiles [c*T/P, (c+1)*T/P); P <= T keeps every range non-empty
+            const long long P = T < static_cast<long long>(gridDim.x) ? T : static_cast<long long>(gridDim.x);
+            const long long c = blockIdx.x;
+            const long long g0 = c < P ? c * T / P : T, g1 = c < P ? (c + 1) * T / P : T;
+            if (g0 < g1) {
+                // locate tile g0: sequence b, and cum = tiles before b (x Hkv)
+                long long cum = 0;
+                int b = 0;
+                for (int b0 = 0; b0 < B; b0 += 32) {
+                    const long long u = static_cast<long long>(seq_tiles<kTT>(a, b0 + lane)) * Hkv;
+                    long long incl = u;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                        if (lane >= o) incl += t;
+                    }
+                    const long long tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+                    if (g0 < cum + tot) {
+                        const unsigned m = __ballot_sync(0xFFFFFFFFu, cum + incl > g0);
+                        const int l = __ffs(m) - 1;
+                        cum += __shfl_sync(0xFFFFFFFFu, incl - u, l);
+                        b = b0 + l;
+                        break;
+                    }
+                    cum += tot;
+                }
+                int L = visible_len(a, b, false);
+                int nt = (L + kTT - 1) / kTT;
+                const long long off = g0 - cum;
+                int h = static_cast<int>(off / nt), t = static_cast<int>(off % nt);
+                const int32_t* table = a.tables + static_cast<size_t>(b) * a.max_blocks;
+                auto owner = [&](long long g) { return ((g + 1) * P - 1) / T; };
+                TileInfo ti;
+                for (long long g = g0; g < g1 && ok; ++g, ++k) {
+                    const int s = acquire(k);
+                    if (!ok) break;
+                    const long long pstart = cum + static_cast<long long>(h) * nt, pend = pstart + nt;
+                    if (g == g0 || t == 0) {  // a new segment: who shares this (sequence, KV head)
+                        const long long cf = owner(pstart);
+                        ti.b = b;
+                        ti.h = h;
+                        ti.c_first = static_cast<int>(cf);
+                        ti.pieces = static_cast<int>(owner(pend - 1) - cf + 1);
+                        ti.s_first = (cf * T / P < pstart) ? 1 : 0;
+                    }
+                    ti.L = L;
+                    ti.tok0 = t * kTT;
+                    ti.n = min(kTT, L - ti.tok0);
+                    ti.flags = ((g == g0 || t == 0) ? kSegFirst : 0) | ((g == g1 - 1 || t == nt - 1) ? kSegLast : 0) |
+                               ((pstart >= g0 && pend <= g1) ? kSegWhole : 0) | (pstart <= g0 ? kCtaFirst : 0) |
+                               (g == g1 - 1 ? kCtaLast : 0);
+                    issue_stage<DT, NQ>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh);
+                    if (++t == nt) {  // next (sequence, KV head)
+                        t = 0;
+                        if (++h == Hkv) {
+                            h = 0;
+                            cum += static_cast<long long>(nt) * Hkv;
+                            ++b;
+                            while (b < B) {
+                                L = visible_len(a, b, false);
+                                if (L > 0) break;
+                                ++b;
+                            }
+                            if (b < B) {
+                                nt = (L + kTT - 1) / kTT;
+                                table = a.tables + static_cast<size_t>(b) * a.max_blocks;
+                                cache_base = -1;
+                            }
+                        }
+                    }
+                }
+            }
+        } else {
+            const int32_t* table = a.tables + static_cast<size_t>(fb_) * a.max_blocks;
+            const int ntiles = (t_end - t_begin + kTT - 1) / kTT;
+            for (int t = 0; t < ntiles && ok; ++t, ++k) {
+                const int s = acquire(k);
+                if (!ok) break;
+                TileInfo ti;
+                ti.b = fb_;
+                ti.h = fh_;
+                ti.L = fL;
+                ti.tok0 = t_begin + t * kTT;
+                ti.n = min(kTT, t_end - ti.tok0);
+                ti.flags = (t == 0 ? kSegFirst : 0) | (t == ntiles - 1 ? kSegLast | kCtaLast : 0) |
+                           (a.num_splits == 1 ? kSegWhole : 0) | kCtaFirst;
+                ti.pieces = 1;
+                ti.c_first = 0;
+                ti.s_first = 0;
+                issue_stage<DT, NQ>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh);
+            }
+        }
+        if (ok && k == 0) {  // a CTA without tiles: tell the consumers
+            if (lane == 0) {
+                TileInfo* ti = reinterpret_cast<TileInfo*>(smem + Lt::kInfoOff);
+                ti->flags = kEnd;
+                mbar_arrive(smem_u32(&full[0]));
+            }
+            k = 1;
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            if (a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
+        }
+        // drain: every issued copy has landed before the CTA may exit
+        if (lane == 0) {
+            for (long long kk = k - 1; kk >= 0 && kk >= k - kStages; --kk)
+                (void)mbar_wait(smem_u32(&full[kk % kStages]), static_cast<uint32_t>((kk / kStages) & 1));
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int wc = warp % kWC, wt = warp / kWC;
+    const int col0 = wc * kNT * 8;               // this warp's first query column
+    const int rbase = wt * Lt::kRowsPerWarp;     // and its first row of a stage
+    const float qk = a.qk_scale_log2;
+    const int bsz = a.block_size;
+    const uint32_t half_stride = static_cast<uint32_t>(bsz * kBoxRowBytes);
+    // m-tile i of step k: rows rbase+16(k*kMT+i).. = block row/bs of the tile, rows row%bs.. of it
+    uint32_t wb[kSteps][kMT];
+#pragma unroll
+    for (int st = 0; st < kSteps; ++st)
+#pragma unroll
+        for (int i = 0; i < kMT; ++i) {
+            const int row = rbase + 16 * (st * kMT + i);
+            wb[st][i] = static_cast<uint32_t>((row / bsz) * kHalves * bsz * kBoxRowBytes + (row % bsz) * kBoxRowBytes);
+        }
+    // causal offset of this lane's columns: query c sees positions < L - C + c + 1
+    // (padding columns see the whole tile; decode: offset 0)
+    int coff[kNT][2];
+#pragma unroll
+    for (int j = 0; j < kNT; ++j)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int n = col0 + 8 * j + 2 * (lane & 3) + hh;
+            coff[j][hh] = n < nq ? n / gh + 1 - a.num_queries : 0;
+        }
+    const int d = threadIdx.x;  // 128 consumer threads = 128 head-dim entries
+    const LaneOffsets lane_off = lane_offsets<DT>(lane);
+    Acc<kNT> acc;
+    bool aborted = false;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    // Bounded meeting point of the 4 consumer warps (an mbarrier, so that a
+    // warp that gave up on a wait cannot leave the others blocked forever).
+    uint32_t cphase = 0;
+    auto csync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(csync_bar));
+        const bool okw = mbar_wait(smem_u32(csync_bar), cphase);
+        cphase ^= 1u;
+        __syncwarp();
+        if (!okw) {
+            aborted = true;
+            if (lane == 0) {
+                *abort_flag = 1;
+                if (a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
+            }
+        }
+        return okw;
+    };
+    auto release = [&](int s) {
+        if constexpr (kInStage) fence_proxy_async();  // generic merge writes before the next TMA fill
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    };
+
+    for (long long k = 0;; ++k) {
+        const int s = static_cast<int>(k % kStages);
+        if (!mbar_wait(smem_u32(&full[s]), static_cast<uint32_t>((k / kStages) & 1))) {
+            aborted = true;
+            if (lane == 0) {
+                *abort_flag = 1;
+                if (a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
+            }
+            break;
+        }
+        const TileInfo ti = info[s];
+        if (ti.flags & kEnd) break;
+        uint8_t* kst = smem + s * Lt::kStageBytes;
+        if (ti.flags & kSegFirst)
+            acc_begin<DT, kNT>(acc, reinterpret_cast<const __nv_bfloat16*>(smem + Lt::kQOff + s * Lt::kQBytes), lane,
+                               col0, nq);
+        int lim[kNT][2];
+#pragma unroll
+        for (int j = 0; j < kNT; ++j) {
+            lim[j][0] = min(ti.n, ti.L + coff[j][0] - ti.tok0);
+            lim[j][1] = min(ti.n, ti.L + coff[j][1] - ti.tok0);
+        }
+#pragma unroll
+        for (int st = 0; st < kSteps; ++st)
+            consume_tile<DT, kMT, kNT>(acc, kst, kst + Lt::kTensorBytes, ti.n, rbase + 16 * kMT * st, lane, wb[st],
+                                       half_stride, qk, lane_off, lim);
+        const bool seg_last = (ti.flags & kSegLast) != 0;
+        if (!kInStage || !seg_last) release(s);
+        if (!seg_last) continue;
+
+        // ---- segment end: merge the token groups, emit
+        if constexpr (kInStage) {  // the stage becomes the merge area once every warp is done reading it
+            if (!csync()) break;
+        }
+        const Merge<NQ, kWT> mg(kInStage ? kst : smem + Lt::kMergeOff, smem + Lt::kMlOff);
+        merge_put<DT, NQ, kWT, kNT>(acc, mg, wt, col0, lane);
+        if (!csync()) break;
+        if (ti.flags & kSegWhole) {
+#pragma unroll 4
+            for (int n = 0; n < nq; ++n) {
+                float v, M, l;
+                merge_get<NQ, kWT>(mg, n, d, v, M, l);
+                out[out_row(a, ti.b, ti.h, n, gh) * kD + d] = __float2bfloat16_rn(l > 0.f ? v * (a.v_scale / l) : 0.f);
+            }
+        } else if constexpr (!kBal) {
+#pragma unroll 4
+            for (int n = 0; n < nq; ++n) {
+                float v, M, l;
+                merge_get<NQ, kWT>(mg, n, d, v, M, l);
+                // partial rows of this launch: (sequence, query n / gh, head)
+                const size_t prow = (static_cast<size_t>(ti.b) * a.num_queries + n / gh) * a.num_q_heads +
+                                    static_cast<size_t>(ti.h) * gh + n % gh;
+                a.o_part[(prow * a.num_splits + fsplit) * kD + d] = l > 0.f ? v * (a.v_scale / l) : 0.f;
+                if (d == 0) a.lse_part[prow * a.num_splits + fsplit] = l > 0.f ? M + log2f(l) : -INFINITY;
+            }
+        } else {
+            // partial of a (sequence, KV head) shared with other CTAs
+            const int slot = (ti.flags & kCtaFirst) ? 0 : 1;
+            const size_t pbase = (static_cast<size_t>(blockIdx.x) * 2 + slot) * NQ;
+#pragma unroll 4
+            for (int n = 0; n < nq; ++n) {
+                float v, M, l;
+                merge_get<NQ, kWT>(mg, n, d, v, M, l);
+                a.bal_o[(pbase + n) * kD + d] = l > 0.f ? v * (a.v_scale / l) : 0.f;
+                if (d == 0) a.bal_lse[pbase + n] = l > 0.f ? M + log2f(l) : -INFINITY;
+            }
+            if constexpr (kInStage) release(s);
+            // Publish: after the consumer barrier one GPU-scope acq_rel atomic by
+            // thread 0 orders every consumer's partial writes before the count,
+            // and (for the last arriver) the other pieces' writes before our reads.
+            if (!csync()) break;
+            int* counter = a.counters + static_cast<size_t>(ti.b) * a.num_kv_heads + ti.h;
+            if (threadIdx.x == 0) *mg.flag = (atom_add_acq_rel(counter, 1) == ti.pieces - 1) ? 1 : 0;
+            if (!csync()) break;
+            if (*mg.flag) {  // every other piece is published: merge them all in one pass
+#pragma unroll 4
+                for (int n = 0; n < nq; ++n) {
+                    float M = -INFINITY, v = 0.f, z = 0.f;
+#pragma unroll 4
+                    for (int j = 0; j < ti.pieces; ++j) {
+                        const size_t pj = (static_cast<size_t>(ti.c_first + j) * 2 + (j == 0 ? ti.s_first : 0)) * NQ + n;
+                        const float lj = __ldcg(a.bal_lse + pj), oj = __ldcg(a.bal_o + pj * kD + d);
+                        if (lj == -INFINITY) continue;  // a piece with no token for this query
+                        const float Mn = fmaxf(M, lj);
+                        const float c = exp2f(M - Mn), w = exp2f(lj - Mn);
+                        v = fmaf(v, c, w * oj);
+                        z = fmaf(z, c, w);
+                        M = Mn;
+                    }
+                    out[out_row(a, ti.b, ti.h, n, gh) * kD + d] = __float2bfloat16_rn(z > 0.f ? v / z : 0.f);
+                }
+                if (threadIdx.x == 0) *counter = 0;  // ready for the next call
+            }
+            // every consumer read the merge area before the second barrier, so
+            // the next segment may overwrite it without another barrier
+            if (ti.flags & kCtaLast) break;
+            continue;
+        }
+        if constexpr (kInStage) {
+            release(s);  // the next segment merges in another stage, or in this one once refilled
+        } else {
+            if (!csync()) break;  // the dedicated merge area is reused by the next segment
+        }
+        if (ti.flags & kCtaLast) break;
+    }
+    if (aborted || *abort_flag) return;
+    if constexpr (kBal) {  // zero the rows of sequences with nothing visible (and report bad lengths once)
+        const int per_seq = a.num_queries * a.num_q_heads;
+        for (int b = blockIdx.x; b < a.num_seqs; b += gridDim.x) {
+            if (visible_len(a, b, threadIdx.x == 0) == 0) {
+                __nv_bfloat16* o = out + (static_cast<size_t>(b) * a.q_total + a.q_first) * a.num_q_heads * kD;
+                for (int i = threadIdx.x; i < per_seq * kD; i += kCWarps * 32) o[i] = __float2bfloat16_rn(0.f);
+            }
+        }
+    }
+}
+
+template <int DT, int NQ, bool kBal>
+cudaError_t launch_nq(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+    using Lt = Layout<DT, NQ>;
+    constexpr size_t smem = Lt::kAlloc;
+    auto kern = decode_mma_kernel<DT, NQ, kBal>;
+    static int configured_mask = 0;
+    static int ctas_per_sm[32] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 31) return cudaErrorNotSupported;
+    if (!(configured_mask & (1 << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        // ask for the largest shared-memory carveout so that two CTAs fit per SM
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kMmaThreads, smem);
+        if (e != cudaSuccess) return e;
+        ctas_per_sm[dev] = occ > 0 ? occ : 1;
+        configured_mask |= 1 << dev;
+    }
+    dim3 grid;
+    if constexpr (kBal) {
+        const int P = num_sms() * ctas_per_sm[dev];
+        grid = dim3(P < a.bal_max_ctas ? P : a.bal_max_ctas);
+    } else {
+        grid = dim3(a.num_splits, a.num_kv_heads, a.num_seqs);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the previous kernel drains
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
+}
+
+// Smallest template row bound that holds this launch's query rows.
+template <int DT, bool kBal>
+cudaError_t launch_rows(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+    const int rows = a.num_queries * (a.num_q_heads / a.num_kv_heads);
+    if (rows <= 1) return launch_nq<DT, 1, kBal>(a, tk, tv, stream);
+    if (rows <= 2) return launch_nq<DT, 2, kBal>(a, tk, tv, stream);
+    if (rows <= 4) return launch_nq<DT, 4, kBal>(a, tk, tv, stream);
+    if (rows <= 8) return launch_nq<DT, 8, kBal>(a, tk, tv, stream);
+    if (rows <= 16) return launch_nq<DT, 16, kBal>(a, tk, tv, stream);
+    if (rows <= 32) return launch_nq<DT, 32, kBal>(a, tk, tv, stream);
+    if (rows <= 64) return launch_nq<DT, 64, kBal>(a, tk, tv, stream);
+    return cudaErrorNotSupported;
+}
+
+template <int DT>
+cudaError_t launch_dt(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+    return a.bal_max_ctas > 0 ? launch_rows<DT, true>(a, tk, tv, stream) : launch_rows<DT, false>(a, tk, tv, stream);
+}
+
+}  // namespace
+}  // namespace pkv

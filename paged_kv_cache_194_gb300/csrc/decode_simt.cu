@@ -82,16 +82,18 @@ decode_simt_kernel(const DecodeArgs a) {
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int L = clamped_len(a, b, split == 0 && h == 0 && tid == 0);
+    const int L = visible_len(a, b, split == 0 && h == 0 && tid == 0);
     const int t_begin = split * a.split_tokens;
     const int t_end = min(L, t_begin + a.split_tokens);
     const bool direct = a.num_splits == 1;
 
-    // The G rows served here are C queries x gh heads: row g is query g / gh
-    // (position L - C + g / gh, attending causally) of head h*gh + g % gh.
+    // The G rows served here are C queries x gh heads: row g is query
+    // q_first + g / gh of the sequence (position L - C + g / gh of the
+    // visible length L, attending causally) and head h*gh + g % gh.
     const int Cq = a.num_queries, gh = G / Cq;
     auto qrow = [&](int g) -> size_t {
-        return (static_cast<size_t>(b) * Cq + g / gh) * a.num_q_heads + static_cast<size_t>(h) * gh + g % gh;
+        return (static_cast<size_t>(b) * a.q_total + a.q_first + g / gh) * a.num_q_heads + static_cast<size_t>(h) * gh +
+               g % gh;
     };
     if (t_begin >= t_end) {
         if (direct) {  // empty sequence: zero output rows
@@ -268,10 +270,10 @@ decode_simt_kernel(const DecodeArgs a) {
         for (int t = 0; t < NTG; ++t) sum += red[(t * G + g) * D + d];
         const float l = sL[g];
         const float o = l > 0.f ? sum * (a.v_scale / l) : 0.f;
-        const size_t row = qrow(g);
         if (direct) {
-            static_cast<QT*>(a.out)[row * D + d] = to_out<QT>(o);
-        } else {
+            static_cast<QT*>(a.out)[qrow(g) * D + d] = to_out<QT>(o);
+        } else {  // partial rows of this launch: (b, query g / gh, head)
+            const size_t row = (static_cast<size_t>(b) * Cq + g / gh) * a.num_q_heads + static_cast<size_t>(h) * gh + g % gh;
             a.o_part[(row * a.num_splits + split) * D + d] = o;
             if (d == 0) a.lse_part[row * a.num_splits + split] = l > 0.f ? sM[g] + log2f(l) : -INFINITY;
         }
@@ -284,12 +286,14 @@ template <int D, typename QT>
 __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     constexpr int PER = D / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 4 + warp;  // (b * C + c) * Hq + hq
+    const int row = blockIdx.x * 4 + warp;  // partial row of this launch: (b * C + c) * Hq + hq
     if (row >= a.num_seqs * a.num_queries * a.num_q_heads) return;
-    const int b = row / (a.num_queries * a.num_q_heads);
-    const int L = clamped_len(a, b, false);
+    const int per_seq = a.num_queries * a.num_q_heads;
+    const int b = row / per_seq;
+    const int L = visible_len(a, b, false);
     const int ns = (L + a.split_tokens - 1) / a.split_tokens;
-    QT* o = static_cast<QT*>(a.out) + static_cast<size_t>(row) * D + lane * PER;
+    const size_t orow = (static_cast<size_t>(b) * a.q_total + a.q_first) * a.num_q_heads + row % per_seq;
+    QT* o = static_cast<QT*>(a.out) + orow * D + lane * PER;
     if (ns == 0) {
 #pragma unroll
         for (int i = 0; i < PER; ++i) o[i] = to_out<QT>(0.f);
@@ -383,11 +387,11 @@ bool ok_dim(int d, int g) {
 
 }  // namespace
 
-bool decode_simt_supported(pkv_dtype kv, int head_dim, int group) {
+bool decode_simt_supported(pkv_dtype kv, int head_dim, int rows) {
     switch (kv) {
-        case PKV_F32: return ok_dim<PKV_F32>(head_dim, group);
-        case PKV_BF16: return ok_dim<PKV_BF16>(head_dim, group);
-        case PKV_FP8_E4M3: return ok_dim<PKV_FP8_E4M3>(head_dim, group);
+        case PKV_F32: return ok_dim<PKV_F32>(head_dim, rows);
+        case PKV_BF16: return ok_dim<PKV_BF16>(head_dim, rows);
+        case PKV_FP8_E4M3: return ok_dim<PKV_FP8_E4M3>(head_dim, rows);
     }
     return false;
 }

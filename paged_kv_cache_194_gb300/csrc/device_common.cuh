@@ -108,6 +108,13 @@ __device__ __forceinline__ int clamped_len(const DecodeArgs& a, int b, bool repo
     return L;
 }
 
+// Tokens a launch may read for sequence b: the clamped length minus the
+// positions after this launch's last query.
+__device__ __forceinline__ int visible_len(const DecodeArgs& a, int b, bool report) {
+    const int L = clamped_len(a, b, report) - a.len_trim;
+    return L > 0 ? L : 0;
+}
+
 template <typename QT>
 __device__ __forceinline__ float load_q(const QT* p);
 template <>

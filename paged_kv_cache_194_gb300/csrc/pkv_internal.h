@@ -43,11 +43,11 @@ struct DecodeArgs {
     const uint8_t* v_layer;
     const int32_t* tables;
     const int32_t* lens;
-    float* o_part;            // [B][Hq][num_splits][D] fp32 (split partials)
-    float* lse_part;          // [B][Hq][num_splits] log2-domain log-sum-exp
+    float* o_part;            // [B][num_queries][Hq][num_splits][D] fp32 (split partials)
+    float* lse_part;          // [B][num_queries][Hq][num_splits] log2-domain log-sum-exp
     int32_t* counters;        // [B][Hkv] finished pieces per (sequence, KV head); zero between calls
-    float* bal_o;             // balanced schedule: [CTA][2 slots][G][D] fp32 partials
-    float* bal_lse;           // balanced schedule: [CTA][2 slots][G] log2-sum-exp
+    float* bal_o;             // balanced schedule: [CTA][2 slots][NQ][D] fp32 partials (NQ query rows per KV head)
+    float* bal_lse;           // balanced schedule: [CTA][2 slots][NQ] log2-sum-exp
     int bal_max_ctas;         // > 0 selects the balanced persistent schedule (grid <= this)
     int32_t* err;             // optional error word
     int layer;
@@ -55,18 +55,27 @@ struct DecodeArgs {
     int max_blocks;
     int max_len;              // host bound of seq_lens (<= max_blocks * block_size)
     int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
-    int num_queries;          // queries per sequence: the last num_queries tokens, causal (1 = decode)
+    // Queries: q/out hold q_total queries per sequence, the last q_total
+    // positions, each attending causally.  One launch serves queries
+    // [q_first, q_first + num_queries); every token it may read lies before
+    // seq_len - len_trim (len_trim = q_total - q_first - num_queries).
+    // Decode: q_total = num_queries = 1, q_first = len_trim = 0.
+    int num_queries;
+    int q_total, q_first, len_trim;
     int split_tokens, num_splits;
     float qk_scale_log2;      // scale * k_scale * log2(e)
     float v_scale;            // v_scale (FP8) or 1
 };
 
-// Returns cudaErrorNotSupported when no kernel matches (dtype, D, G).
+// Returns cudaErrorNotSupported when no kernel matches (dtype, D, query rows
+// per KV head).
 cudaError_t launch_decode_simt(pkv_dtype kv, const DecodeArgs& a, cudaStream_t stream);
-bool decode_simt_supported(pkv_dtype kv, int head_dim, int group);
+bool decode_simt_supported(pkv_dtype kv, int head_dim, int rows);
 cudaError_t launch_decode_mma(pkv_dtype kv, const DecodeArgs& a, const void* tmap_k, const void* tmap_v,
                               cudaStream_t stream);
-bool decode_mma_supported(pkv_dtype kv, int head_dim, int group, int block_size);
+bool decode_mma_supported(pkv_dtype kv, int head_dim, int rows, int block_size);
+constexpr int kMmaMaxRows = 64;   // query rows per KV head one tensor-core launch serves
+constexpr int kSimtMaxRows = 16;  // the same for the SIMT design
 cudaError_t launch_combine(pkv_dtype q_dtype, const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace pkv

@@ -29,19 +29,28 @@ def _filled(w):
     return inst, batch
 
 
-CASES = [  # (G, C, kv, designs)
+CASES = [  # (G, C, kv, designs); launches: tensor cores take up to 64 query rows per KV head
     (4, 2, "bf16", ("mma", "simt")),
     (4, 2, "fp8", ("mma",)),
     (2, 4, "bf16", ("mma", "simt")),
     (1, 8, "bf16", ("mma", "simt")),
     (2, 4, "f32", ("simt",)),
+    (4, 4, "bf16", ("mma", "simt")),    # 16 rows: two column groups of warps
+    (4, 8, "bf16", ("mma", "simt")),    # 32 rows; SIMT in two launches
+    (4, 8, "fp8", ("mma",)),
+    (4, 16, "bf16", ("mma",)),          # 64 rows: two n-tiles per warp
+    (4, 16, "fp8", ("mma",)),
+    (4, 40, "bf16", ("mma", "simt")),   # chunks 16 + 16 + 8 (tensor cores)
+    (8, 8, "bf16", ("mma",)),           # 64 rows
+    (1, 100, "bf16", ("mma",)),         # chunks 64 + 36 (36 rows in the 64-row kernel)
+    (3, 5, "bf16", ("mma",)),           # 3 query heads per KV head: 15 rows padded to 16
 ]
 
 
 @pytest.mark.parametrize("split", [0, 64])
 @pytest.mark.parametrize("G,C,kv,algos", CASES, ids=lambda x: str(x))
 def test_multi_query_parity(G, C, kv, algos, split):
-    lens = (C - 1, C, C + 1, 17, 64, 65, 300, 1000)
+    lens = (C - 1, C, C + 1, 17, 64, 65, 300, 1000) if C < 64 else (C - 1, C, C + 1, 17, 130, 300, 1000, 1500)
     w = _w("mq_%s_g%d_c%d" % (kv, G, C), G, 2, kv, "f32" if kv == "f32" else "bf16", lens,
            D=64 if kv == "f32" else 128)
     inst, batch = _filled(w)
