@@ -136,7 +136,10 @@ struct Layout {
     static constexpr int kWT = kCWarps / kWC;
     static constexpr int kNT = NQ <= 8 ? 1 : NQ / (8 * kWC);  // n-tiles (8 columns) per warp
     static constexpr int kRowsPerWarp = kTT / kWT;
-    static constexpr int kSteps = kRowsPerWarp / (16 * kMT);  // consume steps per warp per stage
+    // A warp's rows of a stage are consumed kCallMT m-tiles at a time: their
+    // QK chains interleave and share one softmax reduction.
+    static constexpr int kCallMT = (kRowsPerWarp / 16) < 4 ? (kRowsPerWarp / 16) : 4;
+    static constexpr int kCalls = kRowsPerWarp / (16 * kCallMT);
     // Up to 32 rows: 2 CTAs per SM (the register cap is then 168 per thread).
     // 64 rows need two n-tiles of accumulators per warp: 1 CTA per SM with
     // twice the stages keeps as many bytes in flight.
@@ -159,7 +162,7 @@ struct Layout {
     static constexpr size_t kBytes = kBarOff + kCtl;
     static constexpr size_t kAlloc = kBytes + 1024;  // + alignment slack
     static_assert(kMergeOBytes <= static_cast<size_t>(kStageBytes), "the merge area must fit in a stage");
-    static_assert(kNT * 8 * kWC >= NQ && kSteps >= 1, "warp grid must cover the rows");
+    static_assert(kNT * 8 * kWC >= NQ && kCalls * kCallMT * 16 == kRowsPerWarp, "warp grid must cover the rows");
     static_assert(kAlloc <= kBudget, "shared memory budget");
 };
 
@@ -721,12 +724,12 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     using Lt = Layout<DT, NQ>;
     constexpr int kStages = Lt::kStages;
     constexpr int kHalves = Lt::kHalves;
-    constexpr int kMT = Lt::kMT;
     constexpr int kTT = Lt::kTT;
     constexpr int kWC = Lt::kWC;
     constexpr int kWT = Lt::kWT;
     constexpr int kNT = Lt::kNT;
-    constexpr int kSteps = Lt::kSteps;
+    constexpr int kCallMT = Lt::kCallMT;
+    constexpr int kCalls = Lt::kCalls;
     constexpr bool kInStage = Lt::kMergeInStage;
 
     extern __shared__ uint8_t smem_raw[];
@@ -912,13 +915,13 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const float qk = a.qk_scale_log2;
     const int bsz = a.block_size;
     const uint32_t half_stride = static_cast<uint32_t>(bsz * kBoxRowBytes);
-    // m-tile i of step k: rows rbase+16(k*kMT+i).. = block row/bs of the tile, rows row%bs.. of it
-    uint32_t wb[kSteps][kMT];
+    // m-tile i of call k: rows rbase+16(k*kCallMT+i).. = block row/bs of the tile, rows row%bs.. of it
+    uint32_t wb[kCalls][kCallMT];
 #pragma unroll
-    for (int st = 0; st < kSteps; ++st)
+    for (int st = 0; st < kCalls; ++st)
 #pragma unroll
-        for (int i = 0; i < kMT; ++i) {
-            const int row = rbase + 16 * (st * kMT + i);
+        for (int i = 0; i < kCallMT; ++i) {
+            const int row = rbase + 16 * (st * kCallMT + i);
             wb[st][i] = static_cast<uint32_t>((row / bsz) * kHalves * bsz * kBoxRowBytes + (row % bsz) * kBoxRowBytes);
         }
     // causal offset of this lane's columns: query c sees positions < L - C + c + 1
@@ -983,9 +986,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             lim[j][1] = min(ti.n, ti.L + coff[j][1] - ti.tok0);
         }
 #pragma unroll
-        for (int st = 0; st < kSteps; ++st)
-            consume_tile<DT, kMT, kNT>(acc, kst, kst + Lt::kTensorBytes, ti.n, rbase + 16 * kMT * st, lane, wb[st],
-                                       half_stride, qk, lane_off, lim);
+        for (int st = 0; st < kCalls; ++st)
+            consume_tile<DT, kCallMT, kNT>(acc, kst, kst + Lt::kTensorBytes, ti.n, rbase + 16 * kCallMT * st, lane,
+                                           wb[st], half_stride, qk, lane_off, lim);
         const bool seg_last = (ti.flags & kSegLast) != 0;
         if (!kInStage || !seg_last) release(s);
         if (!seg_last) continue;
@@ -1034,22 +1037,66 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             int* counter = a.counters + static_cast<size_t>(ti.b) * a.num_kv_heads + ti.h;
             if (threadIdx.x == 0) *mg.flag = (atom_add_acq_rel(counter, 1) == ti.pieces - 1) ? 1 : 0;
             if (!csync()) break;
-            if (*mg.flag) {  // every other piece is published: merge them all in one pass
-#pragma unroll 4
-                for (int n = 0; n < nq; ++n) {
-                    float M = -INFINITY, v = 0.f, z = 0.f;
-#pragma unroll 4
-                    for (int j = 0; j < ti.pieces; ++j) {
-                        const size_t pj = (static_cast<size_t>(ti.c_first + j) * 2 + (j == 0 ? ti.s_first : 0)) * NQ + n;
-                        const float lj = __ldcg(a.bal_lse + pj), oj = __ldcg(a.bal_o + pj * kD + d);
-                        if (lj == -INFINITY) continue;  // a piece with no token for this query
-                        const float Mn = fmaxf(M, lj);
-                        const float c = exp2f(M - Mn), w = exp2f(lj - Mn);
-                        v = fmaf(v, c, w * oj);
-                        z = fmaf(z, c, w);
-                        M = Mn;
+            if (*mg.flag) {  // every other piece is published: merge them all
+                // pass 1: per row, the largest log-sum-exp M and 1/z, z = sum_j 2^(lse_j - M)
+                float* fm = mg.m;  // the merge m/l area is free again: [NQ] M, [NQ] 1/z
+                float* fz = mg.m + NQ;
+                if (threadIdx.x < nq) {
+                    const int n = threadIdx.x;
+                    float M = -INFINITY, z = 0.f;
+                    for (int j0 = 0; j0 < ti.pieces; j0 += 4) {
+                        float l4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int j = j0 + u;
+                            l4[u] = j < ti.pieces
+                                        ? __ldcg(a.bal_lse + (static_cast<size_t>(ti.c_first + j) * 2 +
+                                                              (j == 0 ? ti.s_first : 0)) * NQ + n)
+                                        : -INFINITY;
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if (l4[u] == -INFINITY) continue;  // a piece with no token for this query
+                            const float Mn = fmaxf(M, l4[u]);
+                            z = z * exp2f(M - Mn) + exp2f(l4[u] - Mn);
+                            M = Mn;
+                        }
                     }
-                    out[out_row(a, ti.b, ti.h, n, gh) * kD + d] = __float2bfloat16_rn(z > 0.f ? v / z : 0.f);
+                    fm[n] = M;
+                    fz[n] = z > 0.f ? 1.f / z : 0.f;
+                }
+                if (!csync()) break;
+                // pass 2: thread t owns 4-float chunks t, t+128, ... of the rows
+                // (32 chunks per row); one round of independent loads per piece
+                constexpr int kC = (NQ * (kD / 4) + kCWarps * 32 - 1) / (kCWarps * 32);
+                float4 acc4[kC];
+#pragma unroll
+                for (int c = 0; c < kC; ++c) acc4[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < ti.pieces; ++j) {
+                    const size_t pb = (static_cast<size_t>(ti.c_first + j) * 2 + (j == 0 ? ti.s_first : 0)) * NQ;
+#pragma unroll
+                    for (int c = 0; c < kC; ++c) {
+                        const int idx = threadIdx.x + c * kCWarps * 32, n = idx >> 5, d4 = idx & 31;
+                        if (n >= nq) continue;
+                        const float lj = __ldcg(a.bal_lse + pb + n);
+                        const float4 o4 = __ldcg(reinterpret_cast<const float4*>(a.bal_o + (pb + n) * kD) + d4);
+                        const float w = lj == -INFINITY ? 0.f : exp2f(lj - fm[n]) * fz[n];
+                        acc4[c].x = fmaf(w, o4.x, acc4[c].x);
+                        acc4[c].y = fmaf(w, o4.y, acc4[c].y);
+                        acc4[c].z = fmaf(w, o4.z, acc4[c].z);
+                        acc4[c].w = fmaf(w, o4.w, acc4[c].w);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < kC; ++c) {
+                    const int idx = threadIdx.x + c * kCWarps * 32, n = idx >> 5, d4 = idx & 31;
+                    if (n >= nq) continue;
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc4[c].x, acc4[c].y);
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc4[c].z, acc4[c].w);
+                    uint2 pk;
+                    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(out + out_row(a, ti.b, ti.h, n, gh) * kD + 4 * d4) = pk;
                 }
                 if (threadIdx.x == 0) *counter = 0;  // ready for the next call
             }
