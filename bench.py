@@ -51,6 +51,15 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _tensor_peak():
+    """bf16 dense tensor peak (TFLOP/s): the measured cuBLAS burst figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def _profile_traffic(kernel_tag: str, src_hash: str):
     """DRAM bytes per launch recorded by an ncu capture in profiles/, if the
     kernel source has not changed since (same sha256)."""
@@ -140,6 +149,25 @@ class Clocks:
                 "reasons": reasons, "samples": len(inside)}
 
 
+def query_chunks(C: int, gh: int, algo: str, kv_dtype: str) -> int:
+    """Attention launches per call: query chunks of at most 64 rows per KV
+    head (tensor-core design) or a power of two of rows the SIMT design holds."""
+    if C <= 1:
+        return 1
+    if algo == "mma":
+        cq = max(1, 64 // gh)
+    else:
+        rows = {"f32": 16, "bf16": 8, "fp8": 4}[kv_dtype]
+        cq = 1
+        while cq * 2 * gh <= rows and cq * 2 <= C:
+            cq *= 2
+    n, c0 = 0, 0
+    while c0 < C:
+        c0 += min(cq, C - c0)
+        n += 1
+    return n
+
+
 def workload_bytes(w, lens):
     import torch
     kvb = {"f32": 4, "bf16": 2, "fp8": 1}[w.kv_dtype]
@@ -181,15 +209,23 @@ def run_ours(args):
     slots = torch.from_numpy(slots_h).to(dev)
     tables, lens = tables_h.to(dev), lens_h.to(dev)
     out = torch.empty_like(qs[0])
-    S, NS, wsb = pk.decode_plan(batch.pool, w.num_seqs, w.num_q_heads, max_len, split)
+    C = max(1, w.queries)  # queries per sequence (1 = decode)
+    if C > 1:
+        S, NS, wsb = pk.multi_query_plan(batch.pool, w.num_seqs, C, w.num_q_heads, max_len, split)
+    else:
+        S, NS, wsb = pk.decode_plan(batch.pool, w.num_seqs, w.num_q_heads, max_len, split)
     algo = pk.decode_algo(batch.pool, w.num_q_heads, args.algo)
     schedule = "balanced" if (algo == "mma" and split == 0) else "fixed splits"
     work = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def attend(l):
-        pk.paged_decode_attention(qs[l], batch.pool, l, tables, lens, max_len, w.scale, out=out, workspace=work,
-                                  split_tokens=split, algo=args.algo, stream=stream)
+        if C > 1:
+            pk.paged_multi_query_attention(qs[l], batch.pool, l, tables, lens, max_len, w.scale, out=out,
+                                           workspace=work, split_tokens=split, algo=args.algo, stream=stream)
+        else:
+            pk.paged_decode_attention(qs[l], batch.pool, l, tables, lens, max_len, w.scale, out=out, workspace=work,
+                                      split_tokens=split, algo=args.algo, stream=stream)
 
     def step():
         for l in layers:
@@ -244,13 +280,19 @@ def run_ours(args):
     part = 0
     if combine:
         nsplit = int(((inst.lens.long() + S - 1) // S).sum())
-        part = 2 * nsplit * Hq * (D + 1) * 4  # partials written then read
-    att_bytes = kv_layer + B * Hq * D * qb * 2 + blocks_read * 4 + B * 4 + part
+        part = 2 * nsplit * C * Hq * (D + 1) * 4  # partials written then read
+    # algorithmic bytes: every KV byte once, q read and out written once
+    att_bytes = kv_layer + B * C * Hq * D * qb * 2 + blocks_read * 4 + B * 4 + part
+    # multiply-adds of QK^T and PV: query c of sequence b sees L_b - C + c + 1 tokens
+    Lq = inst.lens.long()
+    seen = sum(int(max(0, L - C + c + 1)) for L in Lq.tolist() for c in range(C))
+    att_flops = 4 * D * Hq * seen
     value = all_kv_bytes / (ms_step * 1e-3) / 1e9
     achieved = att_bytes / (att_ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
     traffic = _profile_traffic("%s/%s/%s" % (args.workload, algo, w.kv_dtype), kernel_hash(algo))
-    launches = args.steps * len(layers) * (2 + (1 if combine else 0))
+    chunks = query_chunks(C, Hq // Hkv, algo, w.kv_dtype)
+    launches = args.steps * len(layers) * (1 + chunks * (2 if combine else 1))
 
     # ---- end to end through the public API: pinned host buffers in, result out
     pin = lambda t: t.pin_memory()
@@ -279,26 +321,41 @@ def run_ours(args):
     e2e_s = replicas.max_over_ranks((time.perf_counter() - t0) / e2e_steps, dev)
     e2e_value = all_kv_bytes / e2e_s / 1e9
 
+    # the bound: HBM unless the call's flops per algorithmic byte exceed the
+    # ridge point of the measured peaks (tensor peak / HBM peak)
+    tpeak, tpeak_kind = _tensor_peak()
+    tflops = att_flops / (att_ms * 1e-3) / 1e12
+    tensor_bound = att_flops / att_bytes > tpeak * 1e12 / (peak * 1e9)
+    roof = {"bound": "tensor" if tensor_bound else "hbm",
+            "achieved": round(tflops, 2) if tensor_bound else round(achieved, 1),
+            "peak": tpeak if tensor_bound else peak, "unit": "TFLOP/s" if tensor_bound else "GB/s",
+            "frac": round((tflops / tpeak) if tensor_bound else (achieved / peak), 4),
+            "traffic": traffic,
+            "kernel": "paged_decode_attention call (decode_%s_kernel%s)" % (algo, " + combine" if combine else ""),
+            "ms_per_launch": round(att_ms, 5), "bytes_per_launch": att_bytes, "flops_per_launch": att_flops,
+            "hbm_gbs": round(achieved, 1), "hbm_frac": round(achieved / peak, 4), "tflops": round(tflops, 2),
+            "kernel_launches_per_call": chunks * (2 if combine else 1),
+            "peak_kind": ("%s (MEASURED_PEAKS.json %s)" % (tpeak_kind if tensor_bound else peak_kind,
+                                                          "bf16_tflops" if tensor_bound else "hbm_gbs"))}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
         "tokens_per_s": round(all_len * len(layers) / (ms_step * 1e-3), 1),
-        "decode_tokens_per_s_32_layers": round(ws * B / (ms_step * 1e-3 * LAYERS / len(layers)), 1),
-        "config": {"workload": "%s: %d seqs, lens %s, %dq/%dkv heads, head_dim %d, block %d, %s KV%s"
+        "decode_tokens_per_s_32_layers": round(ws * B * C / (ms_step * 1e-3 * LAYERS / len(layers)), 1),
+        "config": {"workload": "%s: %d seqs, lens %s, %dq/%dkv heads, head_dim %d, block %d, %s KV%s%s"
                    % (w.name, B, _lens_desc(w), Hq, Hkv, D, w.block_size, w.kv_dtype,
-                      ", %d layers per step" % len(layers) if len(layers) > 1 else ""),
+                      ", %d layers per step" % len(layers) if len(layers) > 1 else "",
+                      ", %d causal queries per sequence (the last %d positions)" % (C, C) if C > 1 else ""),
+                   "queries_per_seq": C,
                    "sum_seq_len": sum_len, "kv_bytes_per_step": kv_bytes,
                    "split_tokens": S if schedule != "balanced" else None,
                    "num_splits": NS if schedule != "balanced" else None, "schedule": schedule, "algo": algo,
                    "parallelism": "replica per GPU" if ws > 1 else "1 GPU",
                    "l2": "inputs exceed L2 (%.0f MB KV per layer vs 129 MB L2); no flush" % (kv_layer / 1e6)},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
+        "roofline": roof,
                      "kernel": "paged_decode_attention call (decode_%s_kernel%s)" % (algo, " + combine" if combine else ""),
-                     "ms_per_launch": round(att_ms, 5), "bytes_per_launch": att_bytes,
-                     "peak_kind": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured"
-                     else "fallback 6.8 TB/s"},
+
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4), "steps": e2e_steps},
         "gpu_launches": launches,
@@ -337,6 +394,18 @@ def _oracle_sample(w, inst, seqs):
     return pool, q, sub_t, sub_l
 
 
+def _oracle_attend(w, pool, q, t, l, window=None, threads=0):
+    """The oracle's attention for the workload's query shape; returns the
+    thread count it used."""
+    import oracle
+    if w.queries > 1:
+        return oracle.paged_attention_mq(q, w.query_dtype, pool, 0, t, l, w.scale, threads=threads,
+                                         return_threads=True)[2]
+    kw = {} if window is None else {"window": window}
+    return oracle.paged_attention(q, w.query_dtype, pool, 0, t, l, w.scale, threads=threads, return_threads=True,
+                                  **kw)[2]
+
+
 def _kv_bytes(w, tokens):
     return tokens * w.num_kv_heads * w.head_dim * 2 * {"f32": 4, "bf16": 2, "fp8": 1}[w.kv_dtype]
 
@@ -351,13 +420,13 @@ def cpu_baseline(w, inst, budget_s=15.0):
     reps, spent, threads = 0, 0.0, 0
     while spent < budget_s and reps < 50:
         t0 = time.perf_counter()
-        _, _, threads = oracle.paged_attention(q, w.query_dtype, pool, 0, t, l, w.scale, return_threads=True)
+        threads = _oracle_attend(w, pool, q, t, l)
         spent += time.perf_counter() - t0
         reps += 1
     # one thread, on the first sequence only (a few seconds)
     one = [0]
     t0 = time.perf_counter()
-    oracle.paged_attention(q[one], w.query_dtype, pool, 0, t[one], l[one], w.scale, threads=1)
+    _oracle_attend(w, pool, q[one], t[one], l[one], threads=1)
     one_s = time.perf_counter() - t0
     return {"value": round(reps * kv_bytes / spent / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "value_1_thread": round(_kv_bytes(w, int(l[0])) / one_s / 1e9, 4),
@@ -381,7 +450,7 @@ def run_reference(args):
     # calibrate on sequence 0
     pool, q, t, l = _oracle_sample(w, inst, [0])
     t0 = time.perf_counter()
-    oracle.paged_attention(q, w.query_dtype, pool, 0, t, l, w.scale)
+    _oracle_attend(w, pool, q, t, l)
     per_token = (time.perf_counter() - t0) / max(1, lens[0])
     want = max(16, int(args.ref_budget / (args.steps + args.warmup) / per_token))
     seqs, window, acc = [], 2**31 - 1, 0
@@ -392,15 +461,16 @@ def run_reference(args):
         acc += L
     if not seqs:
         seqs, window, acc = [0], min(lens[0], want), min(lens[0], want)
+        if w.queries > 1:  # no window for multi-query: the whole first sequence
+            window, acc = 2**31 - 1, lens[0]
     pool, q, t, l = _oracle_sample(w, inst, seqs)
     kv_bytes = _kv_bytes(w, acc)
     for _ in range(args.warmup):
-        oracle.paged_attention(q, w.query_dtype, pool, 0, t, l, w.scale, window=(0, window))
+        _oracle_attend(w, pool, q, t, l, window=(0, window))
     threads = 0
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _, _, threads = oracle.paged_attention(q, w.query_dtype, pool, 0, t, l, w.scale, window=(0, window),
-                                               return_threads=True)
+        threads = _oracle_attend(w, pool, q, t, l, window=(0, window))
     dt = (time.perf_counter() - t0) / max(1, args.steps)
     value = kv_bytes / dt / 1e9
     sample = ("first %d of %d sequences (%d tokens) of the %s batch per step" % (len(seqs), w.num_seqs, acc, w.name)

@@ -67,7 +67,7 @@ def _load():
         lib.or_paged_attention_mq.argtypes = [P, c.c_int, P, P, c.c_int, c.c_int, c.c_int, c.c_int,
                                               c.c_int, c.c_int, c.c_int, c.c_float, c.c_float, P,
                                               c.c_int, P, c.c_int, c.c_int, c.c_int, c.c_float, P, P,
-                                              c.c_int]
+                                              c.c_int, c.POINTER(c.c_int)]
         lib.or_lse_combine.restype = None
         lib.or_lse_combine.argtypes = [P, P, c.c_int, c.c_int, P, P]
         for name, t_in, t_out in (("or_e4m3_encode_array", P, P), ("or_e4m3_decode_array", P, P),
@@ -205,10 +205,10 @@ def paged_attention(q, q_dtype: str, pool: OraclePool, layer: int, block_tables,
 
 
 def paged_attention_mq(q, q_dtype: str, pool: OraclePool, layer: int, block_tables, seq_lens,
-                       scale: float, threads: int = 0):
+                       scale: float, threads: int = 0, return_threads: bool = False):
     """fp64 multi-query attention: q [B][C][Hq][D], query c of sequence b at
     position L_b - C + c attends causally to tokens 0..L_b - C + c.
-    Returns (out [B][C][Hq][D], lse [B][C][Hq])."""
+    Returns (out [B][C][Hq][D], lse [B][C][Hq]) (+ the thread count used)."""
     qq = to_numpy_bits(q, q_dtype)
     B, C, Hq, D = qq.shape
     assert D == pool.head_dim
@@ -216,12 +216,16 @@ def paged_attention_mq(q, q_dtype: str, pool: OraclePool, layer: int, block_tabl
     sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
     out = np.zeros((B, C, Hq, D), dtype=np.float64)
     lse = np.zeros((B, C, Hq), dtype=np.float64)
+    used = ctypes.c_int(0)
     rc = _load().or_paged_attention_mq(
         _ptr(qq), _DT[q_dtype], _ptr(pool.k), _ptr(pool.v), _DT[pool.dtype], pool.num_layers,
         pool.num_blocks, pool.block_size, pool.kv_heads, pool.head_dim, layer, pool.k_scale,
-        pool.v_scale, _ptr(bt), bt.shape[1], _ptr(sl), B, C, Hq, scale, _ptr(out), _ptr(lse), int(threads))
+        pool.v_scale, _ptr(bt), bt.shape[1], _ptr(sl), B, C, Hq, scale, _ptr(out), _ptr(lse), int(threads),
+        ctypes.byref(used))
     if rc != 0:
         raise IndexError("oracle paged_attention_mq: bad block table or length (rc=%d)" % rc)
+    if return_threads:
+        return out, lse, used.value
     return out, lse
 
 

@@ -408,7 +408,7 @@ int or_paged_attention_mq(const void* q, int q_dtype, const void* k_pool, const 
                           int kv_heads, int head_dim, int layer, float k_scale, float v_scale,
                           const int32_t* block_tables, int max_blocks_per_seq,
                           const int32_t* seq_lens, int num_seqs, int num_queries, int num_q_heads,
-                          float scale, double* out, double* lse, int num_threads) {
+                          float scale, double* out, double* lse, int num_threads, int* threads_used) {
     if (layer < 0 || layer >= num_layers || kv_heads <= 0 || num_q_heads % kv_heads != 0 ||
         num_queries < 1)
         return OR_BAD_ARG;
@@ -424,6 +424,7 @@ int or_paged_attention_mq(const void* q, int q_dtype, const void* k_pool, const 
     num_threads = 1;
 #endif
     const int64_t rows = (int64_t)num_seqs * C * num_q_heads;
+    if (threads_used) *threads_used = num_threads;
 #pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
     for (int64_t pr = 0; pr < rows; ++pr) {
         const int b = (int)(pr / ((int64_t)C * num_q_heads));

@@ -10,6 +10,9 @@ restricted to the attention layer):
 * decode step: one more slot per sequence (a new block when the last one is
   full), ``kv_append`` of the step's new K/V row, then
   ``paged_decode_attention`` over seq_lens[b] tokens.
+* with C = w.queries > 1 the prefill stops at seq_lens[b] - C and a step
+  appends the last C positions of every sequence (drafted tokens to verify,
+  or a prompt chunk), then runs ``paged_multi_query_attention``.
 
 Inputs come from ``workloads`` (seeded, synthetic).  Nothing here computes
 attention or conversions itself.
@@ -47,10 +50,11 @@ class DecodeBatch:
         self.seq_ids = list(range(self.B))
         for b in self.seq_ids:
             self.bm.add(b)
-        # prefill slots (positions 0 .. L-2), identical for every layer
+        self.C = max(1, w.queries)
+        # prefill slots (positions 0 .. L-C-1), identical for every layer
         self.prefill_slots: Dict[int, np.ndarray] = {}
         for b in self.seq_ids:
-            n = max(0, self.lens[b] - 1)
+            n = max(0, self.lens[b] - self.C)
             self.prefill_slots[b] = self.bm.grow(b, n) if n else np.zeros(0, np.int64)
         self._prefill(chunk_tokens)
         self.step = 0
@@ -97,7 +101,16 @@ class DecodeBatch:
     # -------------------------------------------------------------- step
     def next_token_slots(self) -> np.ndarray:
         """Slots of each sequence's next token (the last of its seq_lens);
-        sequences that started empty stay empty and get slot -1."""
+        sequences that started empty stay empty and get slot -1.  With C > 1:
+        [B * C] slots of positions L-C .. L-1 (-1 where the position is
+        negative)."""
+        if self.C > 1:
+            slots = np.full((self.B, self.C), -1, dtype=np.int64)
+            for b in self.seq_ids:
+                n = min(self.C, self.lens[b])
+                if n > 0:
+                    slots[b, self.C - n:] = self.bm.grow(b, n)
+            return slots.reshape(-1)
         slots = np.full(self.B, -1, dtype=np.int64)
         active = [b for b in self.seq_ids if self.lens[b] > 0]
         if active:
@@ -106,9 +119,24 @@ class DecodeBatch:
 
     def step_inputs(self, layer: int, step: int = 0):
         """Host tensors of a decode step: q, k_new, v_new (the rows of
-        position seq_lens[b] - 1 + step; zeros for empty sequences)."""
+        position seq_lens[b] - 1 + step; zeros for empty sequences).  With
+        C > 1: q [B, C, Hq, D] and the rows of positions L-C .. L-1, [B*C, Hkv, D]
+        (zeros at negative positions)."""
         w = self.w
         q = wl.query(w, layer, step)
+        if self.C > 1:
+            ks, vs = [], []
+            z = torch.zeros((1, w.num_kv_heads, w.head_dim), dtype=wl.DTYPES[w.in_dtype])
+            for b in self.seq_ids:
+                L = self.lens[b]
+                n = min(self.C, L)
+                ks += [z] * (self.C - n)
+                vs += [z] * (self.C - n)
+                if n > 0:
+                    k, v = wl.seq_kv(w, layer, b, n, start=L - n)
+                    ks.append(k)
+                    vs.append(v)
+            return q, torch.cat(ks), torch.cat(vs)
         ks, vs = [], []
         for b in self.seq_ids:
             if self.lens[b] > 0:

@@ -28,10 +28,22 @@ The five workloads restate the ones the measurements are quoted on:
 5. ``long``: 4 sequences at 131072 tokens; 64-token blocks; BF16; 32 layers in
    one pool (8192 blocks per layer); 2048-token splits.
 
+Two multi-query workloads (several queries per sequence, each attending
+causally to the positions up to its own):
+
+6. ``specverify``: the ``llama`` batch verifying k = 4 drafted tokens per
+   sequence in one pass ("How does TensorRT-LLM work?", "Speculative
+   decoding": guess several tokens, let the model check them together).
+7. ``prefill``: 16 sequences whose last 256 prompt tokens arrive as one chunk
+   over a cached prefix, total lengths ~ U[1024, 8192] ("How does
+   TensorRT-LLM work?", "In-flight batching": long prompts are split into
+   chunks mixed with decoding); 32-token blocks.
+
 Convention used throughout: ``seq_lens[b]`` is the number of tokens a decode
 step attends over, and the last of them (position ``seq_lens[b] - 1``) is the
 token that step appends.  A prefill therefore writes positions
-``0 .. seq_lens[b] - 2`` first.
+``0 .. seq_lens[b] - 2`` first.  With C queries per sequence the step appends
+(and queries) the last C positions, ``seq_lens[b] - C .. seq_lens[b] - 1``.
 """
 from __future__ import annotations
 
@@ -68,6 +80,7 @@ class Workload:
     split_tokens: int = 0    # 0: let the library choose
     steps: int = 1           # decode steps (each appends one token per sequence)
     q_dtype: str = ""        # query dtype when it differs from in_dtype
+    queries: int = 1         # queries per sequence per step (1 = decode)
 
     @property
     def query_dtype(self) -> str:
@@ -90,6 +103,10 @@ WORKLOADS: Dict[str, Workload] = {
     "long": Workload("long", 5, 4, 32, 8, 128, 64, "bf16", "bf16", 1.0 / math.sqrt(128.0),
                      num_layers=32, lens="fixed", fixed_lens=(131072,) * 4, pool_blocks=8192,
                      split_tokens=2048),
+    "specverify": Workload("specverify", 2, 64, 32, 8, 128, 16, "bf16", "bf16", 1.0 / math.sqrt(128.0),
+                           lens="uniform", len_lo=128, len_hi=4096, queries=4),
+    "prefill": Workload("prefill", 7, 16, 32, 8, 128, 32, "bf16", "bf16", 1.0 / math.sqrt(128.0),
+                        lens="uniform", len_lo=1024, len_hi=8192, queries=256),
 }
 
 # workload order as the measurements list them
@@ -155,9 +172,14 @@ def chunk_tables(order: torch.Tensor, lens: torch.Tensor, block_size: int,
 
 
 def query(w: Workload, layer: int = 0, step: int = 0) -> torch.Tensor:
-    """q [B, Hq, D] in the workload's input dtype (CPU)."""
-    g = _gen(w.seed, 3, layer, step)
-    shape = (w.num_seqs, w.num_q_heads, w.head_dim)
+    """q [B, Hq, D] (decode) or [B, C, Hq, D] (C = w.queries > 1) in the
+    workload's query dtype (CPU)."""
+    if w.queries > 1:
+        g = _gen(w.seed, 6, layer, step)
+        shape = (w.num_seqs, w.queries, w.num_q_heads, w.head_dim)
+    else:
+        g = _gen(w.seed, 3, layer, step)
+        shape = (w.num_seqs, w.num_q_heads, w.head_dim)
     return _draw(w, shape, g, w.query_dtype)
 
 

@@ -78,3 +78,25 @@ def test_one_query_equals_decode():
         b = pk.paged_decode_attention(q[:, 0].contiguous(), batch.pool, 0, tables, lens, int(lens.max()), w.scale,
                                       algo=algo)
         assert torch.equal(a[:, 0], b)
+
+
+@pytest.mark.parametrize("name,sample", [("specverify", (0, 1, 17, 33, 63)), ("prefill", (0, 9))])
+def test_multi_query_workload_full_size(name, sample, record_property):
+    """The benchmark's multi-query step at full size (append the last C
+    positions, then attend), checked on sampled sequences against the oracle."""
+    w = wl.WORKLOADS[name]
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    slots = batch.next_token_slots()
+    q, kn, vn = batch.step_inputs(0)
+    pk.kv_append(batch.pool, 0, kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda())
+    tables, lens = batch.tables(), batch.seq_lens()
+    assert torch.equal(lens, inst.lens)
+    out = pk.paged_multi_query_attention(q.cuda(), batch.pool, 0, tables.cuda(), lens.cuda(), int(lens.max()),
+                                         w.scale)
+    torch.cuda.synchronize()
+    ref, _ = oracle_reference_mq(w, inst.k_scale, inst.v_scale, 0, q, tables, lens.tolist(), list(sample))
+    max_abs, max_rel = compare(out[list(sample)], ref, TOL[w.kv_dtype], name)
+    record_property("max_abs_err", max_abs)
+    record_property("max_rel_err", max_rel)
+    assert batch.pool.errors() == 0
