@@ -66,6 +66,13 @@ int row_bound(int rows) {
     return p;
 }
 constexpr int kMaxQueries = 1 << 20;
+// Rows of one balanced-schedule partial slot: the template row bound of the
+// largest launch (a KV-head pair's 2 * gh rows for decode).
+int bal_rows(int gh, int C) {
+    const int r = row_bound(mma_chunk(gh, C) * gh);
+    const int pair = (C == 1 && 2 * gh <= 8) ? row_bound(2 * gh) : 0;
+    return r > pair ? r : pair;
+}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -118,6 +125,21 @@ bool ensure_tmaps(pkv_pool* p) {
         if (ok3) {
             p->tmap_3d = 1;
             p->tmap_state = 1;
+            // Boxes of two adjacent KV heads of a block (the rows of head h+1
+            // follow those of head h): 8 KB per box at 16-token blocks.
+            p->tmap_pair = 0;
+            if (d.block_size == 16 && d.num_kv_heads % 2 == 0) {
+                const cuuint32_t box2[3] = {64, static_cast<cuuint32_t>(2 * d.block_size), 2};
+                bool ok2 = true;
+                for (int i = 0; i < 2 && ok2; ++i) {
+                    CUresult r = enc(i == 0 ? &p->tmap_k2 : &p->tmap_v2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                                     i == 0 ? d.k_base : d.v_base, dims3, strides3, box2, estr3,
+                                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    ok2 = r == CUDA_SUCCESS;
+                }
+                p->tmap_pair = ok2 ? 1 : 0;
+            }
             return true;
         }
     }
@@ -271,7 +293,7 @@ pkv_status paged_multi_query_plan(const pkv_pool* p, int32_t num_seqs, int32_t n
     const int cq = mma_chunk(gh, num_queries);
     size_t body = fixed_bytes(num_seqs, cq * num_q_heads, p->d.head_dim, ns);
     if (split_tokens == 0 && num_seqs <= kMaxBalancedSeqs) {
-        const size_t bb = bal_bytes(bal_ctas(), row_bound(cq * gh), p->d.head_dim);
+        const size_t bb = bal_bytes(bal_ctas(), bal_rows(gh, num_queries), p->d.head_dim);
         if (bb > body) body = bb;
     }
     size_t ws = body > 0 ? counters_bytes(num_seqs, p->d.num_kv_heads) + body : 0;
@@ -373,7 +395,7 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
         if (balanced) {
             a.bal_max_ctas = bal_ctas();
             a.bal_o = reinterpret_cast<float*>(body);
-            a.bal_lse = reinterpret_cast<float*>(body + bal_o_bytes(a.bal_max_ctas, row_bound(cq_mma * gh),
+            a.bal_lse = reinterpret_cast<float*>(body + bal_o_bytes(a.bal_max_ctas, bal_rows(gh, num_queries),
                                                                     p->d.head_dim));
         } else if (NS > 1) {
             const size_t rows = static_cast<size_t>(num_seqs) * cq_mma * num_q_heads * NS;
@@ -381,6 +403,13 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
             a.lse_part = reinterpret_cast<float*>(body + round_up(rows * p->d.head_dim * sizeof(float), 256));
         }
     }
+    // Decode on BF16 pools of 16-token blocks: one CTA serves two adjacent KV
+    // heads, so each block arrives as one 8 KB box instead of two 4 KB ones
+    // (per-box cost dominates at 4 KB).
+    const bool pair = use_mma && num_queries == 1 && p->tmap_pair == 1 && p->tmap_3d == 1 && 2 * gh <= 8;
+    a.heads_per_cta = pair ? 2 : 1;
+    const void* tk = pair ? &p->tmap_k2 : &p->tmap_k;
+    const void* tv = pair ? &p->tmap_v2 : &p->tmap_v;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // one launch (plus combine) per query chunk; a chunk reads only the tokens
     // its last query can see
@@ -389,8 +418,7 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
         a.q_first = c0;
         a.num_queries = cq;
         a.len_trim = num_queries - c0 - cq;
-        cudaError_t e = use_mma ? launch_decode_mma(p->d.kv_dtype, a, &p->tmap_k, &p->tmap_v, s)
-                                : launch_decode_simt(p->d.kv_dtype, a, s);
+        cudaError_t e = use_mma ? launch_decode_mma(p->d.kv_dtype, a, tk, tv, s) : launch_decode_simt(p->d.kv_dtype, a, s);
         if (e != cudaSuccess) return cuda_status(e);
         if (!balanced && NS > 1) {
             e = launch_combine(q_dtype, a, s);

@@ -126,15 +126,16 @@ constexpr int kCtaLast = 32;  // the CTA's last tile
 //   merge m, l [kWT][NQ] + one flag word,
 //   merge O [kWT][NQ][128] fp32 (dedicated, or in the segment's last stage),
 //   barriers full[kStages], empty[kStages], consumer sync, abort word.
-template <int DT, int NQ>
+template <int DT, int NQ, int HP = 1>
 struct Layout {
     static constexpr int kHalves = MmaCfg<DT>::kHalves;
     static constexpr int kMT = MmaCfg<DT>::kMT;
-    static constexpr int kTT = 16 * kCWarps * kMT;  // tokens per stage
-    // warp grid: kWC column groups x kWT token groups
-    static constexpr int kWC = NQ <= 8 ? 1 : (NQ / 8 < kCWarps ? NQ / 8 : kCWarps);
-    static constexpr int kWT = kCWarps / kWC;
-    static constexpr int kNT = NQ <= 8 ? 1 : NQ / (8 * kWC);  // n-tiles (8 columns) per warp
+    static constexpr int kTT = 16 * kCWarps * kMT / HP;  // tokens per stage (of each of the HP KV heads)
+    // warp grid: HP head groups x kWC column groups x kWT token groups
+    static constexpr int kNQH = NQ / HP;  // column bound per KV head
+    static constexpr int kWC = kNQH <= 8 ? 1 : (kNQH / 8 < kCWarps / HP ? kNQH / 8 : kCWarps / HP);
+    static constexpr int kWT = kCWarps / (HP * kWC);
+    static constexpr int kNT = kNQH <= 8 ? 1 : kNQH / (8 * kWC);  // n-tiles (8 columns) per warp
     static constexpr int kRowsPerWarp = kTT / kWT;
     // A warp's rows of a stage are consumed kCallMT m-tiles at a time: their
     // QK chains interleave and share one softmax reduction.
@@ -146,7 +147,7 @@ struct Layout {
     static constexpr int kMinBlocks = NQ <= 32 ? 2 : 1;
     static constexpr size_t kBudget = kMinBlocks == 2 ? kTwoCtaSmem : kOneCtaSmem;
     static constexpr int kStages = NQ <= 16 ? 3 : (kMinBlocks == 2 ? 2 : 4);
-    static constexpr int kTensorBytes = kHalves * kTT * kBoxRowBytes;
+    static constexpr int kTensorBytes = kHalves * kTT * HP * kBoxRowBytes;
     static constexpr int kStageBytes = 2 * kTensorBytes;
     static constexpr int kQBytes = NQ * kD * 2;
     static constexpr size_t kQOff = static_cast<size_t>(kStages) * kStageBytes;
@@ -162,7 +163,8 @@ struct Layout {
     static constexpr size_t kBytes = kBarOff + kCtl;
     static constexpr size_t kAlloc = kBytes + 1024;  // + alignment slack
     static_assert(kMergeOBytes <= static_cast<size_t>(kStageBytes), "the merge area must fit in a stage");
-    static_assert(kNT * 8 * kWC >= NQ && kCalls * kCallMT * 16 == kRowsPerWarp, "warp grid must cover the rows");
+    static_assert(kNT * 8 * kWC * HP >= NQ && kCalls * kCallMT * 16 == kRowsPerWarp, "warp grid must cover the rows");
+    static_assert(HP == 1 || (HP == 2 && NQ <= 8), "KV-head pairs serve decode only");
     static_assert(kAlloc <= kBudget, "shared memory budget");
 };
 
@@ -308,9 +310,9 @@ struct Acc {
 
 // Start a segment: clear the state and build the Q^T fragments of columns
 // [col0, col0 + 8*NT) from the stage's query rows qs[NQ][128] (BF16, shared
-// memory); columns >= nq are zero padding.
+// memory); columns >= col_end are zero padding.
 template <int DT, int NT>
-__device__ __forceinline__ void acc_begin(Acc<NT>& s, const __nv_bfloat16* qs, int lane, int col0, int nq) {
+__device__ __forceinline__ void acc_begin(Acc<NT>& s, const __nv_bfloat16* qs, int lane, int col0, int col_end) {
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         s.m[j][0] = s.m[j][1] = -INFINITY;
@@ -324,7 +326,7 @@ __device__ __forceinline__ void acc_begin(Acc<NT>& s, const __nv_bfloat16* qs, i
         const int n = col0 + 8 * j + r;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            if (n >= nq) {
+            if (n >= col_end) {
                 s.bq[ks][j][0] = s.bq[ks][j][1] = 0u;
                 continue;
             }
@@ -585,9 +587,11 @@ struct Merge {
     }
 };
 
-// Publish this warp's (m, l, O) for its columns [col0, col0 + 8*NT) as token group wt.
+// Publish this warp's (m, l, O) for its columns [col0, min(col0 + 8*NT, col_end)) as token group wt.
 template <int DT, int NQ, int WT, int NT>
-__device__ __forceinline__ void merge_put(const Acc<NT>& s, const Merge<NQ, WT>& mg, int wt, int col0, int lane) {
+__device__ __forceinline__ void merge_put(const Acc<NT>& s, const Merge<NQ, WT>& mg, int wt, int col0, int col_end,
+                                          int lane) {
+    const int cend = col_end < NQ ? col_end : NQ;
     const int r = lane >> 2, q = lane & 3;
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -600,21 +604,21 @@ __device__ __forceinline__ void merge_put(const Acc<NT>& s, const Merge<NQ, WT>&
         const int n0 = col0 + 8 * j + 2 * q, n1 = n0 + 1;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-            if (n0 < NQ) {
+            if (n0 < cend) {
                 mg.o[(wt * NQ + n0) * kD + o_dim<DT>(mt, r)] = s.o[mt][j][0];
                 mg.o[(wt * NQ + n0) * kD + o_dim<DT>(mt, r + 8)] = s.o[mt][j][2];
             }
-            if (n1 < NQ) {
+            if (n1 < cend) {
                 mg.o[(wt * NQ + n1) * kD + o_dim<DT>(mt, r)] = s.o[mt][j][1];
                 mg.o[(wt * NQ + n1) * kD + o_dim<DT>(mt, r + 8)] = s.o[mt][j][3];
             }
         }
         if (lane < 4) {
-            if (n0 < NQ) {
+            if (n0 < cend) {
                 mg.m[wt * NQ + n0] = s.m[j][0];
                 mg.l[wt * NQ + n0] = l0;
             }
-            if (n1 < NQ) {
+            if (n1 < cend) {
                 mg.m[wt * NQ + n1] = s.m[j][1];
                 mg.l[wt * NQ + n1] = l1;
             }
@@ -639,22 +643,27 @@ __device__ __forceinline__ void merge_get(const Merge<NQ, WT>& mg, int n, int d,
     }
 }
 
-// Output row of column n of (sequence b, KV head h): query q_first + n / gh,
-// head h * gh + n % gh.
+// Output row of column n of (sequence b, KV head unit h): query q_first +
+// n / gh, head h * gh + n % gh; for a KV-head pair (decode) unit h is heads
+// 2h, 2h+1 and column n is query head 2h * gh + n.
+template <int HP = 1>
 __device__ __forceinline__ size_t out_row(const DecodeArgs& a, int b, int h, int n, int gh) {
-    return (static_cast<size_t>(b) * a.q_total + a.q_first + n / gh) * a.num_q_heads + static_cast<size_t>(h) * gh +
-           n % gh;
+    if constexpr (HP == 1)
+        return (static_cast<size_t>(b) * a.q_total + a.q_first + n / gh) * a.num_q_heads +
+               static_cast<size_t>(h) * gh + n % gh;
+    else
+        return (static_cast<size_t>(b) * a.q_total + a.q_first) * a.num_q_heads + static_cast<size_t>(HP * h) * gh + n;
 }
 
 // ---------------------------------------------------------------- producer
 // Stage s <- tile ti: tile info, the query rows at a segment's first tile,
 // and one TMA box per KV block (K and V).  All 32 producer lanes call it
 // (they share the block-table window); lane 0 issues.
-template <int DT, int NQ>
+template <int DT, int NQ, int HP>
 __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                             uint8_t* smem, uint64_t* full, int s, const TileInfo& ti,
                                             const int32_t* table, int& cache, int& cache_base, int lane, int gh) {
-    using Lt = Layout<DT, NQ>;
+    using Lt = Layout<DT, NQ, HP>;
     const int bs = a.block_size;
     uint8_t* kst = smem + s * Lt::kStageBytes;
     uint8_t* vst = kst + Lt::kTensorBytes;
@@ -664,12 +673,19 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorM
     if (lane == 0) {
         reinterpret_cast<TileInfo*>(smem + Lt::kInfoOff)[s] = ti;
         const uint32_t qbytes = static_cast<uint32_t>(a.num_queries * gh * kD * 2);
-        mbar_expect_tx(fb, static_cast<uint32_t>(nblk * bs * kBoxRowBytes * Lt::kHalves * 2) + (need_q ? qbytes : 0u));
-        if (need_q) {  // query rows n = c * gh + g: one copy of gh contiguous rows per query
-            for (int c = 0; c < a.num_queries; ++c) {
-                const __nv_bfloat16* qsrc = static_cast<const __nv_bfloat16*>(a.q) + out_row(a, ti.b, ti.h, c * gh, gh) * kD;
-                bulk_load(smem_u32(smem + Lt::kQOff + s * Lt::kQBytes + c * gh * kD * 2), qsrc,
-                          static_cast<uint32_t>(gh * kD * 2), fb);
+        mbar_expect_tx(fb, static_cast<uint32_t>(nblk * HP * bs * kBoxRowBytes * Lt::kHalves * 2) +
+                               (need_q ? static_cast<uint32_t>(HP) * qbytes : 0u));
+        if (need_q) {
+            if constexpr (HP == 1) {  // query rows n = c * gh + g: one copy of gh contiguous rows per query
+                for (int c = 0; c < a.num_queries; ++c) {
+                    const __nv_bfloat16* qsrc =
+                        static_cast<const __nv_bfloat16*>(a.q) + out_row(a, ti.b, ti.h, c * gh, gh) * kD;
+                    bulk_load(smem_u32(smem + Lt::kQOff + s * Lt::kQBytes + c * gh * kD * 2), qsrc,
+                              static_cast<uint32_t>(gh * kD * 2), fb);
+                }
+            } else {  // a pair's HP * gh query heads are contiguous
+                const __nv_bfloat16* qsrc = static_cast<const __nv_bfloat16*>(a.q) + out_row<HP>(a, ti.b, ti.h, 0, gh) * kD;
+                bulk_load(smem_u32(smem + Lt::kQOff + s * Lt::kQBytes), qsrc, HP * qbytes, fb);
             }
         }
     }
@@ -686,15 +702,15 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorM
             if (lane == 0 && a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
             blk = 0;  // read an in-bounds block; the flag marks the output invalid
         }
-        if (lane == 0) {
-            const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + ti.h) * bs);
-            const uint32_t off = k * Lt::kHalves * bs * kBoxRowBytes;
+        if (lane == 0) {  // a box holds the block's rows of the HP adjacent KV heads
+            const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + HP * ti.h) * bs);
+            const uint32_t off = k * Lt::kHalves * HP * bs * kBoxRowBytes;
             if (Lt::kHalves == 2 && a.tma_3d) {  // one box: both 128-byte halves of every row
                 tma_load_3d(smem_u32(kst + off), tmk, 0, y, 0, fb);
                 tma_load_3d(smem_u32(vst + off), tmv, 0, y, 0, fb);
             } else {
-                for (int hf = 0; hf < Lt::kHalves; ++hf) {
-                    const uint32_t o2 = off + hf * bs * kBoxRowBytes;
+                for (int hf = 0; hf < Lt::kHalves; ++hf) {  // (never with HP = 2: the host requires 3D boxes)
+                    const uint32_t o2 = off + hf * HP * bs * kBoxRowBytes;
                     tma_load_2d(smem_u32(kst + o2), tmk, hf * 64, y, fb);
                     tma_load_2d(smem_u32(vst + o2), tmv, hf * 64, y, fb);
                 }
@@ -717,11 +733,11 @@ __device__ __forceinline__ int seq_tiles(const DecodeArgs& a, int b) {
 
 // kBal: balanced persistent schedule (grid = P CTAs); otherwise one CTA per
 // (split, KV head, sequence) with grid (num_splits, num_kv_heads, num_seqs).
-template <int DT, int NQ, bool kBal>
-__global__ void __launch_bounds__(kMmaThreads, Layout<DT, NQ>::kMinBlocks)
+template <int DT, int NQ, bool kBal, int HP>
+__global__ void __launch_bounds__(kMmaThreads, Layout<DT, NQ, HP>::kMinBlocks)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
-    using Lt = Layout<DT, NQ>;
+    using Lt = Layout<DT, NQ, HP>;
     constexpr int kStages = Lt::kStages;
     constexpr int kHalves = Lt::kHalves;
     constexpr int kTT = Lt::kTT;
@@ -742,7 +758,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gh = a.num_q_heads / a.num_kv_heads;  // query heads per KV head
-    const int nq = a.num_queries * gh;              // real query rows (<= NQ)
+    const int nq = HP * a.num_queries * gh;         // real query rows (<= NQ)
+    const int Hu = a.num_kv_heads / HP;             // KV-head units per sequence
 
     // Launched as a programmatic dependent of the previous kernel in the
     // stream (the append): nothing is read before that grid has finished.
@@ -761,7 +778,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (t_begin >= t_end) {
             if (a.num_splits == 1) {  // nothing visible: zero output rows
                 for (int i = threadIdx.x; i < nq * kD; i += kMmaThreads)
-                    static_cast<__nv_bfloat16*>(a.out)[out_row(a, fb_, fh_, i / kD, gh) * kD + i % kD] =
+                    static_cast<__nv_bfloat16*>(a.out)[out_row<HP>(a, fb_, fh_, i / kD, gh) * kD + i % kD] =
                         __float2bfloat16_rn(0.f);
             }
             return;
@@ -791,7 +808,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             return s;
         };
         if constexpr (kBal) {
-            const int B = a.num_seqs, Hkv = a.num_kv_heads;
+            const int B = a.num_seqs, Hkv = Hu;
             long long T = 0;
 #pragma unroll 4
             for (int b0 = 0; b0 < B; b0 += 32) T += warp_sum_ll(seq_tiles<kTT>(a, b0 + lane));
@@ -847,7 +864,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     ti.flags = ((g == g0 || t == 0) ? kSegFirst : 0) | ((g == g1 - 1 || t == nt - 1) ? kSegLast : 0) |
                                ((pstart >= g0 && pend <= g1) ? kSegWhole : 0) | (pstart <= g0 ? kCtaFirst : 0) |
                                (g == g1 - 1 ? kCtaLast : 0);
-                    issue_stage<DT, NQ>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh);
+                    issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh);
                     if (++t == nt) {  // next (sequence, KV head)
                         t = 0;
                         if (++h == Hkv) {
@@ -885,7 +902,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 ti.pieces = 1;
                 ti.c_first = 0;
                 ti.s_first = 0;
-                issue_stage<DT, NQ>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh);
+                issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh);
             }
         }
         if (ok && k == 0) {  // a CTA without tiles: tell the consumers
@@ -909,20 +926,25 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
 
     // ---------------------------------------------------------------- consumers
-    const int wc = warp % kWC, wt = warp / kWC;
-    const int col0 = wc * kNT * 8;               // this warp's first query column
-    const int rbase = wt * Lt::kRowsPerWarp;     // and its first row of a stage
+    // warp = (KV head hp of the unit, column group wc, token group wt)
+    const int hp = warp / (kCWarps / HP), wi = warp % (kCWarps / HP);
+    const int wc = wi % kWC, wt = wi / kWC;
+    // this warp's query columns [col0, col_end) and first token of a stage
+    const int col0 = HP == 1 ? wc * kNT * 8 : hp * gh;
+    const int col_end = HP == 1 ? nq : col0 + gh;
+    const int rbase = wt * Lt::kRowsPerWarp;
     const float qk = a.qk_scale_log2;
     const int bsz = a.block_size;
-    const uint32_t half_stride = static_cast<uint32_t>(bsz * kBoxRowBytes);
+    const uint32_t half_stride = static_cast<uint32_t>(HP * bsz * kBoxRowBytes);
     // m-tile i of call k: rows rbase+16(k*kCallMT+i).. = block row/bs of the tile, rows row%bs.. of it
     uint32_t wb[kCalls][kCallMT];
 #pragma unroll
     for (int st = 0; st < kCalls; ++st)
 #pragma unroll
         for (int i = 0; i < kCallMT; ++i) {
-            const int row = rbase + 16 * (st * kCallMT + i);
-            wb[st][i] = static_cast<uint32_t>((row / bsz) * kHalves * bsz * kBoxRowBytes + (row % bsz) * kBoxRowBytes);
+            const int row = rbase + 16 * (st * kCallMT + i);  // token of the tile; head hp's rows follow head 0's
+            wb[st][i] = static_cast<uint32_t>((row / bsz) * kHalves * HP * bsz * kBoxRowBytes +
+                                              (hp * bsz + row % bsz) * kBoxRowBytes);
         }
     // causal offset of this lane's columns: query c sees positions < L - C + c + 1
     // (padding columns see the whole tile; decode: offset 0)
@@ -932,7 +954,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int n = col0 + 8 * j + 2 * (lane & 3) + hh;
-            coff[j][hh] = n < nq ? n / gh + 1 - a.num_queries : 0;
+            coff[j][hh] = (HP == 1 && n < nq) ? n / gh + 1 - a.num_queries : 0;
         }
     const int d = threadIdx.x;  // 128 consumer threads = 128 head-dim entries
     const LaneOffsets lane_off = lane_offsets<DT>(lane);
@@ -978,7 +1000,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         uint8_t* kst = smem + s * Lt::kStageBytes;
         if (ti.flags & kSegFirst)
             acc_begin<DT, kNT>(acc, reinterpret_cast<const __nv_bfloat16*>(smem + Lt::kQOff + s * Lt::kQBytes), lane,
-                               col0, nq);
+                               col0, col_end);
         int lim[kNT][2];
 #pragma unroll
         for (int j = 0; j < kNT; ++j) {
@@ -998,23 +1020,25 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             if (!csync()) break;
         }
         const Merge<NQ, kWT> mg(kInStage ? kst : smem + Lt::kMergeOff, smem + Lt::kMlOff);
-        merge_put<DT, NQ, kWT, kNT>(acc, mg, wt, col0, lane);
+        merge_put<DT, NQ, kWT, kNT>(acc, mg, wt, col0, col_end, lane);
         if (!csync()) break;
         if (ti.flags & kSegWhole) {
 #pragma unroll 4
             for (int n = 0; n < nq; ++n) {
                 float v, M, l;
                 merge_get<NQ, kWT>(mg, n, d, v, M, l);
-                out[out_row(a, ti.b, ti.h, n, gh) * kD + d] = __float2bfloat16_rn(l > 0.f ? v * (a.v_scale / l) : 0.f);
+                out[out_row<HP>(a, ti.b, ti.h, n, gh) * kD + d] =
+                    __float2bfloat16_rn(l > 0.f ? v * (a.v_scale / l) : 0.f);
             }
         } else if constexpr (!kBal) {
 #pragma unroll 4
             for (int n = 0; n < nq; ++n) {
                 float v, M, l;
                 merge_get<NQ, kWT>(mg, n, d, v, M, l);
-                // partial rows of this launch: (sequence, query n / gh, head)
-                const size_t prow = (static_cast<size_t>(ti.b) * a.num_queries + n / gh) * a.num_q_heads +
-                                    static_cast<size_t>(ti.h) * gh + n % gh;
+                // partial rows of this launch: (sequence, query, head)
+                const size_t prow = HP == 1 ? (static_cast<size_t>(ti.b) * a.num_queries + n / gh) * a.num_q_heads +
+                                                  static_cast<size_t>(ti.h) * gh + n % gh
+                                            : static_cast<size_t>(ti.b) * a.num_q_heads + static_cast<size_t>(HP * ti.h) * gh + n;
                 a.o_part[(prow * a.num_splits + fsplit) * kD + d] = l > 0.f ? v * (a.v_scale / l) : 0.f;
                 if (d == 0) a.lse_part[prow * a.num_splits + fsplit] = l > 0.f ? M + log2f(l) : -INFINITY;
             }
@@ -1096,7 +1120,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     uint2 pk;
                     pk.x = *reinterpret_cast<const uint32_t*>(&lo);
                     pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-                    *reinterpret_cast<uint2*>(out + out_row(a, ti.b, ti.h, n, gh) * kD + 4 * d4) = pk;
+                    *reinterpret_cast<uint2*>(out + out_row<HP>(a, ti.b, ti.h, n, gh) * kD + 4 * d4) = pk;
                 }
                 if (threadIdx.x == 0) *counter = 0;  // ready for the next call
             }
@@ -1124,11 +1148,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
 }
 
-template <int DT, int NQ, bool kBal>
+template <int DT, int NQ, bool kBal, int HP = 1>
 cudaError_t launch_nq(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-    using Lt = Layout<DT, NQ>;
+    using Lt = Layout<DT, NQ, HP>;
     constexpr size_t smem = Lt::kAlloc;
-    auto kern = decode_mma_kernel<DT, NQ, kBal>;
+    auto kern = decode_mma_kernel<DT, NQ, kBal, HP>;
     static int configured_mask = 0;
     static int ctas_per_sm[32] = {0};
     int dev = 0;
@@ -1151,7 +1175,7 @@ cudaError_t launch_nq(const DecodeArgs& a, const CUtensorMap& tk, const CUtensor
         const int P = num_sms() * ctas_per_sm[dev];
         grid = dim3(P < a.bal_max_ctas ? P : a.bal_max_ctas);
     } else {
-        grid = dim3(a.num_splits, a.num_kv_heads, a.num_seqs);
+        grid = dim3(a.num_splits, a.num_kv_heads / HP, a.num_seqs);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -1170,6 +1194,16 @@ cudaError_t launch_nq(const DecodeArgs& a, const CUtensorMap& tk, const CUtensor
 template <int DT, bool kBal>
 cudaError_t launch_rows(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
     const int rows = a.num_queries * (a.num_q_heads / a.num_kv_heads);
+    if constexpr (DT == PKV_BF16) {
+        if (a.heads_per_cta == 2) {  // a KV-head pair: 2 * rows columns
+            if (a.num_queries != 1 || a.num_kv_heads % 2 != 0) return cudaErrorNotSupported;
+            if (rows <= 1) return launch_nq<DT, 2, kBal, 2>(a, tk, tv, stream);
+            if (rows <= 2) return launch_nq<DT, 4, kBal, 2>(a, tk, tv, stream);
+            if (rows <= 4) return launch_nq<DT, 8, kBal, 2>(a, tk, tv, stream);
+            return cudaErrorNotSupported;
+        }
+    }
+    if (a.heads_per_cta != 1) return cudaErrorNotSupported;
     if (rows <= 1) return launch_nq<DT, 1, kBal>(a, tk, tv, stream);
     if (rows <= 2) return launch_nq<DT, 2, kBal>(a, tk, tv, stream);
     if (rows <= 4) return launch_nq<DT, 4, kBal>(a, tk, tv, stream);

@@ -20,6 +20,9 @@ struct pkv_pool {
     int tmap_3d;             // BF16: 1 = one 3D box per block row pair, 0 = two 2D boxes
     CUtensorMap tmap_k;      // TMA descriptors of the whole K / V pool (2D: head_dim x rows)
     CUtensorMap tmap_v;
+    int tmap_pair;           // 1: tmap_k2 / tmap_v2 are ready (3D boxes of two adjacent KV heads of a block)
+    CUtensorMap tmap_k2;
+    CUtensorMap tmap_v2;
 };
 
 namespace pkv {
@@ -62,6 +65,7 @@ struct DecodeArgs {
     // Decode: q_total = num_queries = 1, q_first = len_trim = 0.
     int num_queries;
     int q_total, q_first, len_trim;
+    int heads_per_cta;        // tensor-core design: 1, or 2 (adjacent KV heads share a CTA; decode, 16-token blocks)
     int split_tokens, num_splits;
     float qk_scale_log2;      // scale * k_scale * log2(e)
     float v_scale;            // v_scale (FP8) or 1

@@ -41,6 +41,10 @@ SMALL = [
     _w("f32_g4_d128_bs32", 4, 2, 128, 32, "f32", "f32", (1, 70, 190), dist="uniform"),
     _w("f32_g16_d64_bs16", 16, 1, 64, 16, "f32", "f32", (17, 99), dist="uniform"),
     _w("with_empty_seq", 4, 2, 128, 16, "bf16", "bf16", (0, 5, 0, 77)),
+    # KV-head pairs (tensor-core decode at 16-token blocks, even KV-head count)
+    _w("pair_g1_bs16", 1, 4, 128, 16, "bf16", "bf16", (1, 16, 33, 200, 0, 511)),
+    _w("pair_g2_bs16", 2, 2, 128, 16, "bf16", "bf16", EDGE_LENS),
+    _w("pair_g3_bs16", 3, 2, 128, 16, "bf16", "bf16", (2, 17, 64, 129, 700)),
 ]
 
 
@@ -58,9 +62,12 @@ def _run_step(batch, layer=0, split=0, algo="auto", step=0):
 
 def _algos(w):
     """Every kernel design that serves the workload."""
-    if w.kv_dtype != "f32" and w.head_dim == 128 and w.group in (1, 2, 4, 8):
-        return ["simt", "mma"]
-    return ["simt"]
+    designs = []
+    if pk.lib() and w.kv_dtype != "f32" and w.head_dim == 128 and w.block_size in (16, 32, 64) and w.group <= 64:
+        designs.append("mma")
+    if w.group in (1, 2, 4, 8, 16) and w.group * {"f32": 4, "bf16": 8, "fp8": 16}[w.kv_dtype] <= 64:
+        designs.append("simt")
+    return designs
 
 
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
