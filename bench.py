@@ -1,9 +1,11 @@
 """Benchmark: paged decode attention KV GB/s and tokens/s on GB300.
 
 One step = one pass of the decode hot path over the batch: the host block
-manager's slot for each sequence's newest token, ``kv_append`` of that token's
-K/V row, then ``paged_decode_attention`` (split-K + log-sum-exp combine) over
-seq_lens[b] tokens.  Every step re-appends the same positions, so the bytes
+manager's slot for each sequence's newest token, the append of that token's
+K/V row, then attention (split-K + log-sum-exp combine) over seq_lens[b]
+tokens.  With the tensor-core design the append runs inside the attention
+launch (``paged_decode_append_attention``, one launch per layer-step);
+``--unfused`` times ``kv_append`` + ``paged_decode_attention`` instead.  Every step re-appends the same positions, so the bytes
 per step are fixed.  Default workload: one Llama-3-8B attention layer, 64
 sequences with lengths U[128, 4096], 32 query / 8 KV heads, head_dim 128,
 16-token blocks, BF16.  KV per step (~0.56 GB) exceeds the 129 MB L2, so no
@@ -215,6 +217,7 @@ def run_ours(args):
     else:
         S, NS, wsb = pk.decode_plan(batch.pool, w.num_seqs, w.num_q_heads, max_len, split)
     algo = pk.decode_algo(batch.pool, w.num_q_heads, args.algo)
+    fused = (not args.unfused) and C == 1 and algo == "mma" and w.group <= 8
     schedule = "balanced" if (algo == "mma" and split == 0) else "fixed splits"
     work = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -227,10 +230,17 @@ def run_ours(args):
             pk.paged_decode_attention(qs[l], batch.pool, l, tables, lens, max_len, w.scale, out=out, workspace=work,
                                       split_tokens=split, algo=args.algo, stream=stream)
 
+    def fused_step(l):
+        pk.paged_decode_append_attention(qs[l], kns[l], vns[l], batch.pool, l, tables, lens, max_len, w.scale,
+                                         out=out, workspace=work, split_tokens=split, algo=args.algo, stream=stream)
+
     def step():
         for l in layers:
-            pk.kv_append(batch.pool, l, kns[l], vns[l], slots, stream)
-            attend(l)
+            if fused:
+                fused_step(l)
+            else:
+                pk.kv_append(batch.pool, l, kns[l], vns[l], slots, stream)
+                attend(l)
 
     for _ in range(args.warmup):
         step()
@@ -254,10 +264,15 @@ def run_ours(args):
     i = 0
     for _ in range(args.steps):
         for l in layers:
-            pk.kv_append(batch.pool, l, kns[l], vns[l], slots, stream)
-            att[i][0].record(stream)
-            attend(l)
-            att[i][1].record(stream)
+            if fused:
+                att[i][0].record(stream)
+                fused_step(l)
+                att[i][1].record(stream)
+            else:
+                pk.kv_append(batch.pool, l, kns[l], vns[l], slots, stream)
+                att[i][0].record(stream)
+                attend(l)
+                att[i][1].record(stream)
             i += 1
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -283,6 +298,8 @@ def run_ours(args):
         part = 2 * nsplit * C * Hq * (D + 1) * 4  # partials written then read
     # algorithmic bytes: every KV byte once, q read and out written once
     att_bytes = kv_layer + B * C * Hq * D * qb * 2 + blocks_read * 4 + B * 4 + part
+    if fused:  # the new rows: read in the input dtype, written in the pool's
+        att_bytes += B * Hkv * D * 2 * ({"f32": 4, "bf16": 2}[w.in_dtype] + kvb)
     # multiply-adds of QK^T and PV: query c of sequence b sees L_b - C + c + 1 tokens
     Lq = inst.lens.long()
     seen = sum(int(max(0, L - C + c + 1)) for L in Lq.tolist() for c in range(C))
@@ -292,7 +309,7 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     traffic = _profile_traffic("%s/%s/%s" % (args.workload, algo, w.kv_dtype), kernel_hash(algo))
     chunks = query_chunks(C, Hq // Hkv, algo, w.kv_dtype)
-    launches = args.steps * len(layers) * (1 + chunks * (2 if combine else 1))
+    launches = args.steps * len(layers) * ((0 if fused else 1) + chunks * (2 if combine else 1))
 
     # ---- end to end through the public API: pinned host buffers in, result out
     pin = lambda t: t.pin_memory()
@@ -301,7 +318,7 @@ def run_ours(args):
     hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     e2e_steps = max(1, min(args.steps, max(1, 2000 // len(layers))))
     h2d = sum(t.numel() * t.element_size() for x in hin for t in x) + sum(
-        t.numel() * t.element_size() for t in (hs_, ht_, hl_))
+        t.numel() * t.element_size() for t in ((ht_, hl_) if fused else (hs_, ht_, hl_)))
     d2h = hout.numel() * hout.element_size()
     torch.cuda.synchronize()
     if ws > 1:
@@ -312,7 +329,8 @@ def run_ours(args):
             qs[l].copy_(hin[l][0], non_blocking=True)
             kns[l].copy_(hin[l][1], non_blocking=True)
             vns[l].copy_(hin[l][2], non_blocking=True)
-        slots.copy_(hs_, non_blocking=True)
+        if not fused:  # the fused launch takes each new token's slot from the table
+            slots.copy_(hs_, non_blocking=True)
         tables.copy_(ht_, non_blocking=True)
         lens.copy_(hl_, non_blocking=True)
         step()
@@ -331,7 +349,9 @@ def run_ours(args):
             "peak": tpeak if tensor_bound else peak, "unit": "TFLOP/s" if tensor_bound else "GB/s",
             "frac": round((tflops / tpeak) if tensor_bound else (achieved / peak), 4),
             "traffic": traffic,
-            "kernel": "paged_decode_attention call (decode_%s_kernel%s)" % (algo, " + combine" if combine else ""),
+            "kernel": "%s call (decode_%s_kernel%s)" % ("paged_decode_append_attention" if fused else
+                                                        "paged_decode_attention", algo,
+                                                        " + combine" if combine else ""),
             "ms_per_launch": round(att_ms, 5), "bytes_per_launch": att_bytes, "flops_per_launch": att_flops,
             "hbm_gbs": round(achieved, 1), "hbm_frac": round(achieved / peak, 4), "tflops": round(tflops, 2),
             "kernel_launches_per_call": chunks * (2 if combine else 1),
@@ -348,14 +368,14 @@ def run_ours(args):
                       ", %d layers per step" % len(layers) if len(layers) > 1 else "",
                       ", %d causal queries per sequence (the last %d positions)" % (C, C) if C > 1 else ""),
                    "queries_per_seq": C,
+                   "step": ("append fused into the attention launch" if fused else
+                            "kv_append launch + attention launch"),
                    "sum_seq_len": sum_len, "kv_bytes_per_step": kv_bytes,
                    "split_tokens": S if schedule != "balanced" else None,
                    "num_splits": NS if schedule != "balanced" else None, "schedule": schedule, "algo": algo,
                    "parallelism": "replica per GPU" if ws > 1 else "1 GPU",
                    "l2": "inputs exceed L2 (%.0f MB KV per layer vs 129 MB L2); no flush" % (kv_layer / 1e6)},
         "roofline": roof,
-                     "kernel": "paged_decode_attention call (decode_%s_kernel%s)" % (algo, " + combine" if combine else ""),
-
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4), "steps": e2e_steps},
         "gpu_launches": launches,
@@ -498,6 +518,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true", help="time kv_append + attention as two launches")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

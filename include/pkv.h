@@ -215,6 +215,33 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
                                        void* out, void* stream);
 
 /*
+ * One decode step of one layer in a single launch: append each sequence's
+ * newest token, then attend ("How does TensorRT-LLM work?", "In-flight
+ * batching": every decode step adds one token's keys and values to the cache
+ * and attends over all of them).  Same result, bit for bit, as kv_append of
+ * k_new / v_new at the slot of position seq_lens[b] - 1 (taken from the block
+ * table) followed by paged_decode_attention.
+ *   k_new, v_new  device [num_seqs][num_kv_heads][head_dim] of in_dtype
+ *                 (PKV_BF16 or PKV_F32), 16-byte aligned; row b is written
+ *                 at position seq_lens[b] - 1 (nothing for seq_lens[b] = 0).
+ * other arguments as paged_decode_attention (workspace from
+ * paged_decode_plan).  Served by the tensor-core design only (BF16/FP8 pools,
+ * head_dim 128, block size 16/32/64, at most 8 query heads per KV head);
+ * otherwise PKV_ERR_UNSUPPORTED before anything is enqueued.  A table entry
+ * outside the pool at the newest position skips the pool write and sets
+ * PKV_ERRBIT_BLOCK_ID; a length above max_seq_len skips it and sets
+ * PKV_ERRBIT_SEQ_LEN.
+ */
+pkv_status paged_decode_append_attention(const void* q, pkv_dtype q_dtype, const void* k_new,
+                                         const void* v_new, pkv_dtype in_dtype, const pkv_pool* pool,
+                                         int32_t layer, const int32_t* block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                         int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len,
+                                         float scale, int32_t split_tokens, pkv_algo algo,
+                                         void* workspace, size_t workspace_bytes, void* out,
+                                         void* stream);
+
+/*
  * paged_decode_attention without a caller-provided workspace, for callers that
  * may not allocate device memory where they run decode attention (plug-ins
  * whose device memory the host application plans once up front, loops that

@@ -25,7 +25,7 @@ ERRBIT_BLOCK_ID, ERRBIT_SLOT, ERRBIT_SEQ_LEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
 # Every symbol include/pkv.h declares.
 EXPORTS = ("kv_pool_create", "kv_pool_destroy", "kv_pool_tensor_bytes", "kv_bytes_per_token",
            "kv_append", "paged_decode_plan", "paged_decode_algo", "paged_decode_attention",
-           "paged_multi_query_plan", "paged_multi_query_attention",
+           "paged_multi_query_plan", "paged_multi_query_attention", "paged_decode_append_attention",
            "paged_decode_attention_static_ws", "pkv_status_string", "pkv_last_cuda_error",
            "kv_block_manager_create", "kv_block_manager_destroy", "kv_bm_num_free", "kv_bm_add_sequence",
            "kv_bm_free_sequence", "kv_bm_grow", "kv_bm_decode_slots", "kv_bm_match_prefix", "kv_bm_seq_len",
@@ -88,6 +88,10 @@ def lib() -> ctypes.CDLL:
     L.paged_multi_query_attention.argtypes = [P, c.c_int, P, c.c_int32, P, c.c_int32, P, c.c_int32, c.c_int32,
                                               c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int, P,
                                               c.c_size_t, P, P]
+    L.paged_decode_append_attention.restype = c.c_int
+    L.paged_decode_append_attention.argtypes = [P, c.c_int, P, P, c.c_int, P, c.c_int32, P, c.c_int32, P,
+                                                c.c_int32, c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int,
+                                                P, c.c_size_t, P, P]
     L.paged_decode_attention_static_ws.restype = c.c_int
     L.paged_decode_attention_static_ws.argtypes = [P, c.c_int, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                                    c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int, P, P]
@@ -246,6 +250,32 @@ def paged_decode_attention(q: torch.Tensor, pool: KVPool, layer: int, block_tabl
         block_tables.shape[1], _dev(seq_lens, "seq_lens", torch.int32), B, Hq, max_seq_len, float(scale),
         split_tokens, ALGOS[algo], ws_ptr, ws_bytes, _dev(out, "out", q.dtype), _stream_ptr(stream))
     _check(rc, "paged_decode_attention")
+    return out
+
+
+def paged_decode_append_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, pool: KVPool,
+                                  layer: int, block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                                  scale: float, out: Optional[torch.Tensor] = None,
+                                  workspace: Optional[torch.Tensor] = None, split_tokens: int = 0,
+                                  algo: str = "auto", stream=None) -> torch.Tensor:
+    """One launch: write k_new / v_new [B, Hkv, D] (bf16 or f32) at position
+    seq_lens[b] - 1 of each sequence, then paged_decode_attention over
+    seq_lens[b] tokens (tensor-core design only)."""
+    B, Hq, D = q.shape
+    if tuple(k_new.shape) != (B, pool.num_kv_heads, D) or k_new.shape != v_new.shape or k_new.dtype != v_new.dtype:
+        raise ValueError("k_new / v_new must both be [num_seqs, num_kv_heads, head_dim] of one dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = workspace_for(pool, B, Hq, max_seq_len, split_tokens)
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else ctypes.c_void_p()
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().paged_decode_append_attention(
+        _dev(q, "q"), _dtype_code(q.dtype), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dtype_code(k_new.dtype),
+        pool.handle, layer, _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(seq_lens, "seq_lens", torch.int32), B, Hq, max_seq_len, float(scale), split_tokens, ALGOS[algo],
+        ws_ptr, ws_bytes, _dev(out, "out", q.dtype), _stream_ptr(stream))
+    _check(rc, "paged_decode_append_attention")
     return out
 
 

@@ -321,12 +321,17 @@ int32_t paged_decode_algo(const pkv_pool* p, int32_t G, pkv_algo algo) {
     return simt_ok ? PKV_ALGO_SIMT : -1;
 }
 
-pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,
-                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                       const int32_t* seq_lens, int32_t num_seqs, int32_t num_queries,
-                                       int32_t num_q_heads, int32_t max_seq_len, float scale, int32_t split_tokens,
-                                       pkv_algo algo, void* workspace, size_t workspace_bytes, void* out,
-                                       void* stream) {
+}  // extern "C"
+
+namespace pkv {
+namespace {
+// Attention for C queries per sequence; with new_k != nullptr (decode only)
+// the kernel also appends each sequence's newest token.
+pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                          int32_t num_seqs, int32_t num_queries, int32_t num_q_heads, int32_t max_seq_len,
+                          float scale, int32_t split_tokens, pkv_algo algo, void* workspace, size_t workspace_bytes,
+                          void* out, void* stream, const void* new_k, const void* new_v, pkv_dtype new_dtype) {
     if (!p || layer < 0 || layer >= p->d.num_layers) return PKV_ERR_INVALID_ARG;
     if (num_queries < 1 || num_queries > kMaxQueries) return PKV_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 || max_seq_len < 0) return PKV_ERR_INVALID_ARG;
@@ -355,6 +360,7 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
         use_mma = mma_fits && ensure_tmaps(mp);
     }
     if (!use_mma && !decode_simt_supported(p->d.kv_dtype, p->d.head_dim, cq_simt * gh)) return PKV_ERR_UNSUPPORTED;
+    if (new_k && (!use_mma || num_queries != 1 || gh > 8)) return PKV_ERR_UNSUPPORTED;
 
     int32_t S = 0, NS = 0;
     size_t need = 0;
@@ -388,6 +394,15 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
     const float log2e = 1.4426950408889634f;
     a.qk_scale_log2 = scale * p->d.k_scale * log2e;
     a.v_scale = p->d.v_scale;
+    if (new_k) {
+        a.new_k = static_cast<const uint8_t*>(new_k);
+        a.new_v = static_cast<const uint8_t*>(new_v);
+        a.new_dtype = new_dtype;
+        a.k_inv_scale = p->k_inv_scale;
+        a.v_inv_scale = p->v_inv_scale;
+        a.k_layer_w = static_cast<uint8_t*>(p->d.k_base) + static_cast<size_t>(layer) * p->layer_bytes;
+        a.v_layer_w = static_cast<uint8_t*>(p->d.v_base) + static_cast<size_t>(layer) * p->layer_bytes;
+    }
     if (need > 0) {
         uint8_t* w = static_cast<uint8_t*>(workspace);
         a.counters = reinterpret_cast<int32_t*>(w);
@@ -427,6 +442,35 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
         c0 += cq;
     }
     return PKV_OK;
+}
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, int32_t num_seqs, int32_t num_queries,
+                                       int32_t num_q_heads, int32_t max_seq_len, float scale, int32_t split_tokens,
+                                       pkv_algo algo, void* workspace, size_t workspace_bytes, void* out,
+                                       void* stream) {
+    return pkv::attention_call(q, q_dtype, p, layer, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                               num_queries, num_q_heads, max_seq_len, scale, split_tokens, algo, workspace,
+                               workspace_bytes, out, stream, nullptr, nullptr, PKV_BF16);
+}
+
+pkv_status paged_decode_append_attention(const void* q, pkv_dtype q_dtype, const void* k_new, const void* v_new,
+                                         pkv_dtype in_dtype, const pkv_pool* p, int32_t layer,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_seq_len, float scale, int32_t split_tokens, pkv_algo algo,
+                                         void* workspace, size_t workspace_bytes, void* out, void* stream) {
+    if (!p) return PKV_ERR_INVALID_ARG;
+    if (in_dtype != PKV_BF16 && in_dtype != PKV_F32) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > 0 && (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16))) return PKV_ERR_INVALID_ARG;
+    return pkv::attention_call(q, q_dtype, p, layer, block_tables, max_blocks_per_seq, seq_lens, num_seqs, 1,
+                               num_q_heads, max_seq_len, scale, split_tokens, algo, workspace, workspace_bytes, out,
+                               stream, num_seqs > 0 ? k_new : nullptr, v_new, in_dtype);
 }
 
 pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,

@@ -655,6 +655,59 @@ __device__ __forceinline__ size_t out_row(const DecodeArgs& a, int b, int h, int
         return (static_cast<size_t>(b) * a.q_total + a.q_first) * a.num_q_heads + static_cast<size_t>(HP * h) * gh + n;
 }
 
+// Fused append (decode), done by the producer warp: the rows [K, V] x [HP
+// heads] x [chunks] of a unit's newest token, lane `lane` owning output chunks
+// lane + 32 j.  prefetch() issues the input loads when a segment that ends
+// the unit starts; write() encodes them exactly as kv_append does and stores
+// them at the position's slot just before the TMA copy of that block, with a
+// proxy fence so that the copy reads the new bytes.
+template <int DT, int HP>
+struct NewRows {
+    static constexpr int kPoolBytes = DT == PKV_BF16 ? 2 : 1;
+    static constexpr int kPer = 16 / kPoolBytes;          // pool elements per 16-byte chunk
+    static constexpr int kChunksRow = kD / kPer;          // 16 (BF16) or 8 (FP8) chunks per row
+    static constexpr int kTotal = 2 * HP * kChunksRow;    // K and V rows of the HP heads
+    static constexpr int kOut = (kTotal + 31) / 32;       // output chunks per lane
+    static constexpr int kInMax = DT == PKV_BF16 ? 2 : 4; // 16-byte input chunks per output chunk (f32 input)
+    uint4 x[kOut][kInMax];
+
+    __device__ __forceinline__ void prefetch(const DecodeArgs& a, int b, int h, int lane) {
+        const bool f32 = a.new_dtype == PKV_F32;
+        const int nin = f32 ? kInMax : kInMax / 2;
+#pragma unroll
+        for (int j = 0; j < kOut; ++j) {
+            const int oc = lane + 32 * j;
+            if (oc >= kTotal) continue;
+            const int tensor = oc / (HP * kChunksRow), head = (oc / kChunksRow) % HP, c = oc % kChunksRow;
+            const uint4* src = reinterpret_cast<const uint4*>(
+                (tensor ? a.new_v : a.new_k) +
+                ((static_cast<size_t>(b) * a.num_kv_heads + HP * h + head) * kD + c * kPer) * (f32 ? 4 : 2));
+#pragma unroll
+            for (int i = 0; i < kInMax; ++i)
+                if (i < nin) x[j][i] = __ldg(src + i);
+        }
+    }
+
+    __device__ __forceinline__ void write(const DecodeArgs& a, int h, int blk, int row, int lane) {
+        const bool f32 = a.new_dtype == PKV_F32;
+#pragma unroll
+        for (int j = 0; j < kOut; ++j) {
+            const int oc = lane + 32 * j;
+            if (oc >= kTotal) continue;
+            const int tensor = oc / (HP * kChunksRow), head = (oc / kChunksRow) % HP, c = oc % kChunksRow;
+            const float inv = tensor ? a.v_inv_scale : a.k_inv_scale;
+            const uint4 w = f32 ? AppendChunk<DT, PKV_F32>::convert(x[j], inv)
+                                : AppendChunk<DT, PKV_BF16>::convert(x[j], inv);
+            uint8_t* dst = (tensor ? a.v_layer_w : a.k_layer_w) +
+                           ((static_cast<size_t>(blk) * a.num_kv_heads + HP * h + head) * a.block_size + row) * kD *
+                               kPoolBytes +
+                           c * 16;
+            *reinterpret_cast<uint4*>(dst) = w;
+        }
+        asm volatile("fence.proxy.async.global;\n" ::: "memory");
+    }
+};
+
 // ---------------------------------------------------------------- producer
 // Stage s <- tile ti: tile info, the query rows at a segment's first tile,
 // and one TMA box per KV block (K and V).  All 32 producer lanes call it
@@ -662,7 +715,8 @@ __device__ __forceinline__ size_t out_row(const DecodeArgs& a, int b, int h, int
 template <int DT, int NQ, int HP>
 __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                             uint8_t* smem, uint64_t* full, int s, const TileInfo& ti,
-                                            const int32_t* table, int& cache, int& cache_base, int lane, int gh) {
+                                            const int32_t* table, int& cache, int& cache_base, int lane, int gh,
+                                            NewRows<DT, HP>& nr, bool append) {
     using Lt = Layout<DT, NQ, HP>;
     const int bs = a.block_size;
     uint8_t* kst = smem + s * Lt::kStageBytes;
@@ -701,6 +755,9 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorM
         if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks)) {
             if (lane == 0 && a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
             blk = 0;  // read an in-bounds block; the flag marks the output invalid
+        } else if (append && k == nblk - 1) {  // the block holding the unit's newest position
+            nr.write(a, ti.h, blk, (ti.L - 1) % bs, lane);
+            __syncwarp();
         }
         if (lane == 0) {  // a box holds the block's rows of the HP adjacent KV heads
             const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + HP * ti.h) * bs);
@@ -846,11 +903,17 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const int32_t* table = a.tables + static_cast<size_t>(b) * a.max_blocks;
                 auto owner = [&](long long g) { return ((g + 1) * P - 1) / T; };
                 TileInfo ti;
+                NewRows<DT, HP> nr;
+                bool app = false;  // this CTA appends the current unit's newest token
                 for (long long g = g0; g < g1 && ok; ++g, ++k) {
                     const int s = acquire(k);
                     if (!ok) break;
                     const long long pstart = cum + static_cast<long long>(h) * nt, pend = pstart + nt;
                     if (g == g0 || t == 0) {  // a new segment: who shares this (sequence, KV head)
+                        if constexpr (NQ <= 8) {  // fused append: the segment holds the unit's last tile
+                            app = a.new_k != nullptr && pend <= g1 && a.lens[b] == L;
+                            if (app) nr.prefetch(a, b, h, lane);
+                        }
                         const long long cf = owner(pstart);
                         ti.b = b;
                         ti.h = h;
@@ -864,7 +927,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     ti.flags = ((g == g0 || t == 0) ? kSegFirst : 0) | ((g == g1 - 1 || t == nt - 1) ? kSegLast : 0) |
                                ((pstart >= g0 && pend <= g1) ? kSegWhole : 0) | (pstart <= g0 ? kCtaFirst : 0) |
                                (g == g1 - 1 ? kCtaLast : 0);
-                    issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh);
+                    issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh, nr,
+                                            app && t == nt - 1);
                     if (++t == nt) {  // next (sequence, KV head)
                         t = 0;
                         if (++h == Hkv) {
@@ -888,6 +952,12 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         } else {
             const int32_t* table = a.tables + static_cast<size_t>(fb_) * a.max_blocks;
             const int ntiles = (t_end - t_begin + kTT - 1) / kTT;
+            NewRows<DT, HP> nr;
+            bool app = false;
+            if constexpr (NQ <= 8) {  // fused append: this split holds the newest position
+                app = a.new_k != nullptr && t_end == fL && a.lens[fb_] == fL;
+                if (app) nr.prefetch(a, fb_, fh_, lane);
+            }
             for (int t = 0; t < ntiles && ok; ++t, ++k) {
                 const int s = acquire(k);
                 if (!ok) break;
@@ -902,7 +972,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 ti.pieces = 1;
                 ti.c_first = 0;
                 ti.s_first = 0;
-                issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh);
+                issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh, nr,
+                                        app && t == ntiles - 1);
             }
         }
         if (ok && k == 0) {  // a CTA without tiles: tell the consumers

@@ -84,6 +84,83 @@ struct KvTraits<PKV_FP8_E4M3> {
     }
 };
 
+// Pool encoding of new K/V rows, shared by the append kernel and the fused
+// append of the tensor-core attention kernel (so both write the same bytes).
+// AppendChunk<pool, input>: kIn 16-byte input chunks -> one 16-byte chunk of
+// pool elements; run() loads them from `src`, convert() takes them from
+// registers.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// 4 inputs -> 4 E4M3 codes: e4m3_rn_satfinite(fp32(x) * inv_scale).
+__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float inv) {
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(a, inv), __fmul_rn(b, inv)), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(c, inv), __fmul_rn(d, inv)), __NV_SATFINITE, __NV_E4M3);
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+template <int PDT, int IDT>
+struct AppendChunk;
+
+template <>
+struct AppendChunk<PKV_F32, PKV_F32> {  // 4 floats
+    static constexpr int kIn = 1;
+    __device__ static uint4 convert(const uint4* x, float) { return x[0]; }
+};
+template <>
+struct AppendChunk<PKV_BF16, PKV_BF16> {  // 8 bf16
+    static constexpr int kIn = 1;
+    __device__ static uint4 convert(const uint4* x, float) { return x[0]; }
+};
+template <>
+struct AppendChunk<PKV_BF16, PKV_F32> {  // 8 floats -> 8 bf16 (RN)
+    static constexpr int kIn = 2;
+    __device__ static uint4 convert(const uint4* x, float) {
+        return make_uint4(pack_bf16x2_rn(__uint_as_float(x[0].x), __uint_as_float(x[0].y)),
+                          pack_bf16x2_rn(__uint_as_float(x[0].z), __uint_as_float(x[0].w)),
+                          pack_bf16x2_rn(__uint_as_float(x[1].x), __uint_as_float(x[1].y)),
+                          pack_bf16x2_rn(__uint_as_float(x[1].z), __uint_as_float(x[1].w)));
+    }
+};
+template <>
+struct AppendChunk<PKV_FP8_E4M3, PKV_F32> {  // 16 floats -> 16 E4M3
+    static constexpr int kIn = 4;
+    __device__ static uint4 convert(const uint4* x, float inv) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = quant4(__uint_as_float(x[i].x), __uint_as_float(x[i].y), __uint_as_float(x[i].z),
+                          __uint_as_float(x[i].w), inv);
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+template <>
+struct AppendChunk<PKV_FP8_E4M3, PKV_BF16> {  // 16 bf16 -> 16 E4M3
+    static constexpr int kIn = 2;
+    __device__ static uint4 convert(const uint4* x, float inv) {
+        const uint32_t in[8] = {x[0].x, x[0].y, x[0].z, x[0].w, x[1].x, x[1].y, x[1].z, x[1].w};
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = quant4(bf16_lo(in[2 * i]), bf16_hi(in[2 * i]), bf16_lo(in[2 * i + 1]),
+                          bf16_hi(in[2 * i + 1]), inv);
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+// Load the kIn input chunks at src and convert them.
+template <int PDT, int IDT>
+__device__ __forceinline__ uint4 append_chunk(const uint8_t* src, float inv) {
+    uint4 x[AppendChunk<PDT, IDT>::kIn];
+#pragma unroll
+    for (int i = 0; i < AppendChunk<PDT, IDT>::kIn; ++i) x[i] = reinterpret_cast<const uint4*>(src)[i];
+    return AppendChunk<PDT, IDT>::convert(x, inv);
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));

@@ -12,72 +12,6 @@ namespace {
 
 constexpr int kAppendThreads = 256;
 
-// Convert 16 bytes' worth of pool elements from the input at `src`.
-template <int PDT, int IDT>
-struct AppendChunk;
-
-template <>
-struct AppendChunk<PKV_F32, PKV_F32> {  // 4 floats
-    __device__ static uint4 run(const uint8_t* src, float) { return *reinterpret_cast<const uint4*>(src); }
-};
-template <>
-struct AppendChunk<PKV_BF16, PKV_BF16> {  // 8 bf16
-    __device__ static uint4 run(const uint8_t* src, float) { return *reinterpret_cast<const uint4*>(src); }
-};
-template <>
-struct AppendChunk<PKV_BF16, PKV_F32> {  // 8 floats -> 8 bf16 (RN)
-    __device__ static uint4 run(const uint8_t* src, float) {
-        const float4 a = reinterpret_cast<const float4*>(src)[0];
-        const float4 b = reinterpret_cast<const float4*>(src)[1];
-        const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(f[2 * i]));
-            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(f[2 * i + 1]));
-            w[i] = lo | (hi << 16);
-        }
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-};
-
-// 16 inputs -> 16 E4M3 codes: e4m3_rn_satfinite(fp32(x) * inv_scale).
-__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float inv) {
-    const __nv_fp8x2_storage_t lo =
-        __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(a, inv), __fmul_rn(b, inv)), __NV_SATFINITE, __NV_E4M3);
-    const __nv_fp8x2_storage_t hi =
-        __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(c, inv), __fmul_rn(d, inv)), __NV_SATFINITE, __NV_E4M3);
-    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
-
-template <>
-struct AppendChunk<PKV_FP8_E4M3, PKV_F32> {
-    __device__ static uint4 run(const uint8_t* src, float inv) {
-        const float4* p = reinterpret_cast<const float4*>(src);
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float4 x = p[i];
-            w[i] = quant4(x.x, x.y, x.z, x.w, inv);
-        }
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-};
-template <>
-struct AppendChunk<PKV_FP8_E4M3, PKV_BF16> {
-    __device__ static uint4 run(const uint8_t* src, float inv) {
-        const uint4 a = reinterpret_cast<const uint4*>(src)[0];
-        const uint4 b = reinterpret_cast<const uint4*>(src)[1];
-        const uint32_t in[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            w[i] = quant4(bf16_lo(in[2 * i]), bf16_hi(in[2 * i]), bf16_lo(in[2 * i + 1]),
-                          bf16_hi(in[2 * i + 1]), inv);
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-};
-
 template <int PDT, int IDT>
 __global__ void __launch_bounds__(kAppendThreads)
 kv_append_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
@@ -113,7 +47,7 @@ kv_append_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
         uint8_t* dst = (is_v ? v_layer : k_layer) +
                        (((blk * kv_heads + h) * block_size + off) * head_dim + static_cast<int64_t>(c) * kPer) *
                            kPoolBytes;
-        *reinterpret_cast<uint4*>(dst) = AppendChunk<PDT, IDT>::run(src, is_v ? v_inv : k_inv);
+        *reinterpret_cast<uint4*>(dst) = append_chunk<PDT, IDT>(src, is_v ? v_inv : k_inv);
     }
 }
 

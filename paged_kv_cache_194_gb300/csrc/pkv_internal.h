@@ -66,6 +66,17 @@ struct DecodeArgs {
     int num_queries;
     int q_total, q_first, len_trim;
     int heads_per_cta;        // tensor-core design: 1, or 2 (adjacent KV heads share a CTA; decode, 16-token blocks)
+    // Fused append (tensor-core decode): the newest token of sequence b
+    // (position seq_lens[b] - 1) has rows new_k / new_v [B][Hkv][D] of dtype
+    // new_dtype (PKV_BF16 or PKV_F32); the CTA whose tile holds that position
+    // encodes them like kv_append, writes them to the pool and into its
+    // staged tile.  new_k == nullptr: no append.
+    const uint8_t* new_k;
+    const uint8_t* new_v;
+    int new_dtype;
+    float k_inv_scale, v_inv_scale;  // FP8 pools: binary32 1/scale, as kv_append uses
+    uint8_t* k_layer_w;       // writable views of k_layer / v_layer (fused append only)
+    uint8_t* v_layer_w;
     int split_tokens, num_splits;
     float qk_scale_log2;      // scale * k_scale * log2(e)
     float v_scale;            // v_scale (FP8) or 1

@@ -1,0 +1,87 @@
+"""GPU: the fused decode step (append the newest token inside the attention
+kernel) against the two-launch step (kv_append, then attention) -- output
+and the whole pool bit for bit -- and against the oracle."""
+import math
+
+import pytest
+import torch
+
+from paged_kv_cache_194_gb300 import binding as pk
+from paged_kv_cache_194_gb300 import workloads as wl
+from paged_kv_cache_194_gb300.decode import DecodeBatch
+
+from parity import TOL, compare, oracle_reference
+
+pytestmark = pytest.mark.gpu
+
+EDGE = (0, 1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 300, 1000)
+
+
+def _w(name, G, Hkv, bs, kv, ind, lens, qd=""):
+    return wl.Workload(name, 61, len(lens), G * Hkv, Hkv, 128, bs, kv, ind, 1.0 / math.sqrt(128), lens="fixed",
+                       fixed_lens=tuple(lens), q_dtype=qd)
+
+
+CASES = [
+    _w("bf16_pair_g4_bs16", 4, 2, 16, "bf16", "bf16", EDGE),         # KV-head pairs
+    _w("bf16_pair_g1_bs16", 1, 4, 16, "bf16", "bf16", (1, 16, 17, 90, 0)),
+    _w("bf16_g2_bs32", 2, 3, 32, "bf16", "bf16", (1, 31, 32, 33, 700, 0)),
+    _w("bf16_from_f32_g8_bs16", 8, 1, 16, "bf16", "f32", (40, 100, 1), qd="bf16"),
+    _w("fp8_g4_bs64", 4, 2, 64, "fp8", "bf16", EDGE),
+    _w("fp8_from_f32_g4_bs16", 4, 1, 16, "fp8", "f32", (40, 100, 1, 16), qd="bf16"),
+]
+
+
+@pytest.mark.parametrize("split", [0, 64])
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_fused_equals_two_launches(w, split):
+    inst = wl.instance(w)
+    a, b = DecodeBatch(inst, fill_byte=0x3C), DecodeBatch(inst, fill_byte=0x3C)  # identical pools and tables
+    assert torch.equal(a.pool.k, b.pool.k) and torch.equal(a.pool.v, b.pool.v)
+    slots = a.next_token_slots()
+    b.next_token_slots()  # same block-manager growth, slots unused: the kernel takes them from the table
+    q, kn, vn = a.step_inputs(0)
+    tables, lens = a.tables().cuda(), a.seq_lens().cuda()
+    assert torch.equal(tables.cpu(), b.tables())
+    max_len = int(lens.max())
+    pk.kv_append(a.pool, 0, kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda())
+    out_a = pk.paged_decode_attention(q.cuda(), a.pool, 0, tables, lens, max_len, w.scale, split_tokens=split,
+                                      algo="mma")
+    out_b = pk.paged_decode_append_attention(q.cuda(), kn.cuda(), vn.cuda(), b.pool, 0, tables, lens, max_len,
+                                             w.scale, split_tokens=split, algo="mma")
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(a.pool.k, b.pool.k) and torch.equal(a.pool.v, b.pool.v)
+    assert a.pool.errors() == 0 and b.pool.errors() == 0
+    ref, _ = oracle_reference(w, inst.k_scale, inst.v_scale, 0, q, tables.cpu(), lens.cpu().tolist(),
+                              list(range(w.num_seqs)))
+    compare(out_b, ref, TOL[w.kv_dtype], w.name)
+
+
+def test_fused_full_size_llama(record_property):
+    """The bench's decode step in one launch, at full size, on sampled sequences."""
+    w = wl.WORKLOADS["llama"]
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    batch.next_token_slots()
+    q, kn, vn = batch.step_inputs(0)
+    tables, lens = batch.tables(), batch.seq_lens()
+    out = pk.paged_decode_append_attention(q.cuda(), kn.cuda(), vn.cuda(), batch.pool, 0, tables.cuda(),
+                                           lens.cuda(), int(lens.max()), w.scale)
+    torch.cuda.synchronize()
+    seqs = [0, 7, 31, 63]
+    ref, _ = oracle_reference(w, inst.k_scale, inst.v_scale, 0, q, tables, lens.tolist(), seqs)
+    max_abs, max_rel = compare(out[seqs], ref, TOL["bf16"], "llama fused")
+    record_property("max_abs_err", max_abs)
+    record_property("max_rel_err", max_rel)
+    assert batch.pool.errors() == 0
+
+
+def test_fused_unsupported_designs():
+    w = _w("f32_pool", 2, 1, 16, "f32", "f32", (5, 9))
+    batch = DecodeBatch(wl.instance(w))
+    batch.next_token_slots()
+    q, kn, vn = batch.step_inputs(0)
+    with pytest.raises(pk.PkvError):
+        pk.paged_decode_append_attention(q.cuda(), kn.cuda(), vn.cuda(), batch.pool, 0, batch.tables().cuda(),
+                                         batch.seq_lens().cuda(), 9, w.scale)
