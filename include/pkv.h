@@ -64,7 +64,10 @@ typedef enum pkv_dtype { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype
 typedef enum pkv_algo {
     PKV_ALGO_AUTO = 0, /* best available for the pool's dtype and geometry */
     PKV_ALGO_SIMT = 1, /* CUDA-core dot products (every dtype) */
-    PKV_ALGO_MMA = 2   /* tensor-core QK^T and PV (BF16 / FP8 pools) */
+    PKV_ALGO_MMA = 2,  /* tensor-core QK^T and PV with warp-level mma (BF16 / FP8 pools) */
+    PKV_ALGO_TC = 3    /* multi-query only: tcgen05 MMAs with TMEM accumulators, 128 query
+                          rows per CTA (BF16 pools, head_dim 128, fixed splits not used);
+                          AUTO picks it from 64 query rows per KV head */
 } pkv_algo;
 
 /*

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libpkv.so")
 
 PKV_F32, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
-ALGOS = {"auto": 0, "simt": 1, "mma": 2}
+ALGOS = {"auto": 0, "simt": 1, "mma": 2, "tc": 3}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "cuda error",
           5: "device bounds", 6: "out of blocks", 7: "inconsistent"}
 ERRBIT_BLOCK_ID, ERRBIT_SLOT, ERRBIT_SEQ_LEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
@@ -31,7 +31,7 @@ EXPORTS = ("kv_pool_create", "kv_pool_destroy", "kv_pool_tensor_bytes", "kv_byte
            "kv_bm_free_sequence", "kv_bm_grow", "kv_bm_decode_slots", "kv_bm_match_prefix", "kv_bm_seq_len",
            "kv_bm_block_tables", "kv_bm_free_list", "kv_bm_block_ref", "kv_bm_check")
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
-ALGO_NAMES = {1: "simt", 2: "mma"}
+ALGO_NAMES = {1: "simt", 2: "mma", 3: "tc"}
 
 
 class PkvError(RuntimeError):

@@ -66,6 +66,7 @@ int row_bound(int rows) {
     return p;
 }
 constexpr int kMaxQueries = 1 << 20;
+constexpr int kTcMinRows = 64;  // query rows per KV head from which AUTO takes the tcgen05 design
 // Rows of one balanced-schedule partial slot: the template row bound of the
 // largest launch (a KV-head pair's 2 * gh rows for decode).
 int bal_rows(int gh, int C) {
@@ -125,6 +126,18 @@ bool ensure_tmaps(pkv_pool* p) {
         if (ok3) {
             p->tmap_3d = 1;
             p->tmap_state = 1;
+            // Boxes of one 64-column half of a block (the tcgen05 kernel keeps
+            // the two halves of a tile apart).
+            const cuuint32_t boxh[3] = {64, static_cast<cuuint32_t>(d.block_size), 1};
+            bool okh = true;
+            for (int i = 0; i < 2 && okh; ++i) {
+                CUresult r = enc(i == 0 ? &p->tmap_kh : &p->tmap_vh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                                 i == 0 ? d.k_base : d.v_base, dims3, strides3, boxh, estr3,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                okh = r == CUDA_SUCCESS;
+            }
+            p->tmap_half = okh ? 1 : 0;
             // Boxes of two adjacent KV heads of a block (the rows of head h+1
             // follow those of head h): 8 KB per box at 16-token blocks.
             p->tmap_pair = 0;
@@ -341,7 +354,8 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
     if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     const pkv_dtype want_q = p->d.kv_dtype == PKV_F32 ? PKV_F32 : PKV_BF16;
     if (q_dtype != want_q) return PKV_ERR_UNSUPPORTED;
-    if (algo != PKV_ALGO_AUTO && algo != PKV_ALGO_SIMT && algo != PKV_ALGO_MMA) return PKV_ERR_INVALID_ARG;
+    if (algo != PKV_ALGO_AUTO && algo != PKV_ALGO_SIMT && algo != PKV_ALGO_MMA && algo != PKV_ALGO_TC)
+        return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
     if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
     if (!q || !out || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
@@ -352,6 +366,16 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
 
     bool use_mma = false;
     pkv_pool* mp = const_cast<pkv_pool*>(p);  // the handle caches its TMA descriptors
+    // tcgen05 design: the whole query list in one launch, 128 rows per CTA;
+    // the default from kTcMinRows query rows per KV head (prompt chunks)
+    const bool tc_fits = attention_tc_supported(p->d.kv_dtype, p->d.head_dim, p->d.block_size) && !new_k &&
+                         split_tokens == 0 && static_cast<int64_t>(num_queries) * gh <= (1 << 24);
+    if (algo == PKV_ALGO_TC) {
+        if (!tc_fits || !ensure_tmaps(mp) || p->tmap_half != 1) return PKV_ERR_UNSUPPORTED;
+    }
+    const bool use_tc = algo == PKV_ALGO_TC ||
+                        (algo == PKV_ALGO_AUTO && tc_fits && num_queries > 1 && num_queries * gh >= kTcMinRows &&
+                         ensure_tmaps(mp) && p->tmap_half == 1);
     const bool mma_fits = decode_mma_supported(p->d.kv_dtype, p->d.head_dim, cq_mma * gh, p->d.block_size);
     if (algo == PKV_ALGO_MMA) {
         if (!mma_fits || !ensure_tmaps(mp)) return PKV_ERR_UNSUPPORTED;
@@ -359,7 +383,8 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
     } else if (algo == PKV_ALGO_AUTO) {
         use_mma = mma_fits && ensure_tmaps(mp);
     }
-    if (!use_mma && !decode_simt_supported(p->d.kv_dtype, p->d.head_dim, cq_simt * gh)) return PKV_ERR_UNSUPPORTED;
+    if (!use_tc && !use_mma && !decode_simt_supported(p->d.kv_dtype, p->d.head_dim, cq_simt * gh))
+        return PKV_ERR_UNSUPPORTED;
     if (new_k && (!use_mma || num_queries != 1 || gh > 8)) return PKV_ERR_UNSUPPORTED;
 
     int32_t S = 0, NS = 0;
@@ -367,7 +392,8 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
     pkv_status st =
         paged_multi_query_plan(p, num_seqs, num_queries, num_q_heads, max_seq_len, split_tokens, &S, &NS, &need);
     if (st != PKV_OK) return st;
-    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256))) return PKV_ERR_WORKSPACE;
+    if (!use_tc && need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+        return PKV_ERR_WORKSPACE;
 
     DecodeArgs a{};
     a.q = q;
@@ -426,6 +452,13 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
     const void* tk = pair ? &p->tmap_k2 : &p->tmap_k;
     const void* tv = pair ? &p->tmap_v2 : &p->tmap_v;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (use_tc) {
+        a.heads_per_cta = 1;
+        a.q_first = 0;
+        a.num_queries = num_queries;
+        a.len_trim = 0;
+        return cuda_status(launch_attention_tc(a, &p->tmap_kh, &p->tmap_vh, s));
+    }
     // one launch (plus combine) per query chunk; a chunk reads only the tokens
     // its last query can see
     for (int c0 = 0; c0 < num_queries;) {

@@ -1,0 +1,495 @@
+// Multi-query paged attention on the 5th-generation tensor cores (tcgen05
+// with TMEM accumulators) for long query lists: prompt chunks, where the
+// query rows of one KV head (C queries x gh heads) fill whole 128-row MMA
+// tiles.  BF16 pools, head_dim 128.
+//
+// "How does TensorRT-LLM work?", "In-flight batching": long prompts are
+// processed in chunks that attend to the cached prefix; "Custom attention
+// kernels": the scores stay on chip.  Query c of the C queries of a sequence
+// sits at position L - C + c of its visible length L and attends causally.
+//
+// One CTA per (128 query rows, KV head, sequence); 6 warps:
+//  * warp 4, TMA producer: per 64-token tile, one box {64 columns, bs rows,
+//    1 half} per KV block and half for K and for V, so a stage holds each of
+//    K and V as [half: head_dim 0-63 | 64-127][64 token rows][128 B], 128-byte
+//    swizzled -- the K-major operand layout for K and the MN-major one for V.
+//  * warp 5, MMA issuer (one thread): S_j = Q K_j^T (M 128 rows, N 64 tokens,
+//    K 128) into one of two TMEM score buffers, one tile ahead of the softmax;
+//    then O += P_j V_j (M 128 rows, N 128 head dims, K 64 tokens) into the
+//    TMEM output accumulator.  tcgen05.commit signals mbarriers.
+//  * warps 0-3, softmax and epilogue: thread m owns query row m (TMEM lane m).
+//    It reads its 64 scores with tcgen05.ld (twice: max, then
+//    probabilities), masks causally, and writes P in BF16 to shared memory in
+//    the swizzled K-major layout.  The running max is updated lazily: O (in
+//    TMEM) and the running sum are rescaled only when the row max grows by
+//    more than 8 in log2 units, so probabilities stay below 2^8 and fp32 keeps
+//    full precision; the final division by the sum uses the same base.
+//  * Epilogue: O / l, rounded to BF16, written to the output rows.
+// Shared memory: Q 32 KB, P 16 KB, 2 stages x (K 16 KB + V 16 KB) for 64-token
+// tiles; TMEM: two 64-column score buffers and a 128-column output
+// accumulator (256 allocated); 2 CTAs per SM, so that two softmax warpgroups
+// share each SM.  Every mbarrier wait is bounded; on expiry the CTA
+// sets PKV_ERRBIT_TIMEOUT, waits (bounded) for its copies and MMAs, frees its
+// TMEM and skips its output.
+#include <cuda.h>
+
+#include "device_common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kRows = 128;                 // query rows per CTA
+constexpr int kTok = 64;                   // tokens per tile
+constexpr int kDim = 128;                  // head_dim
+constexpr uint32_t kSpin = 1u << 22;       // polls before a wait gives up
+constexpr int kPBufs = 1;                  // P buffers (the softmax, not the PV, bounds a tile)
+constexpr int kQHalf = kRows * 128;        // one 64-column half of the Q tile: 16 KB
+constexpr int kHalfBytes = kTok * 128;     // one 64-column half of a K or V tile: 8 KB
+constexpr int kPBytes = kRows * kTok * 2;  // P tile: 16 KB
+constexpr int kQOff = 0;
+constexpr int kPOff = 2 * kQHalf;
+constexpr int kKVOff = kPOff + kPBufs * kPBytes;
+constexpr int kStageBytes = 4 * kHalfBytes;  // K (16 KB) + V (16 KB)
+constexpr int kBarOff = kKVOff + 2 * kStageBytes;
+constexpr int kBarBytes = 128;
+constexpr int kSmem = 115712;              // the most that lets 2 CTAs share an SM
+constexpr int kAlignSlack = kSmem - kBarOff - kBarBytes;  // room to align the base to 1024 B
+static_assert(kAlignSlack >= 0, "shared memory budget");
+constexpr uint32_t kTmemCols = 256;        // per CTA: 2 CTAs per SM
+constexpr uint32_t kOCol = 2 * kTok;       // score buffers at columns 0 and kTok
+__device__ __forceinline__ uint32_t s_col(int s) { return s ? static_cast<uint32_t>(kTok) : 0u; }
+
+// mbarriers (8 bytes each) after the tiles
+enum Bar { kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1,
+           kPvDone0, kPvDone1, kQReady, kDone, kNumBars };
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ void bar_init(uint32_t b, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(b), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint32_t b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(b) : "memory");
+}
+__device__ __forceinline__ void bar_expect_tx(uint32_t b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(b), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool bar_wait(uint32_t b, uint32_t parity) {
+    for (uint32_t i = 0; i < kSpin; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(b), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+// The same wait by every lane of a warp, with one verdict for all of them
+// (tcgen05.ld/st that follow are warp-wide).
+__device__ __forceinline__ bool bar_wait_warp(uint32_t b, uint32_t parity) {
+    return __all_sync(0xFFFFFFFFu, bar_wait(b, parity));
+}
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t b) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(b)
+        : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+// Shared-memory operand descriptor: 128-byte swizzle, 8-row groups 1024 B
+// apart (SBO); LBO: byte distance between the two 64-element halves of an
+// MN-major operand (unused for K-major ones).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo) {
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor: BF16 x BF16 -> F32, M 128, N n; B MN-major if b_mn.
+constexpr uint32_t idesc(int n, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn) << 16) |
+           ((static_cast<uint32_t>(n) >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t b) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(b) : "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t a, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(a));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t a, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(a));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t a, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(a),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
+// Byte offset of 16-byte chunk `ch` (8 BF16 each) of row r in a
+// [halves of half_bytes][rows][128 B] 128B-swizzled tile.
+__device__ __forceinline__ uint32_t tile_off(int r, int ch, int half_bytes) {
+    return static_cast<uint32_t>((ch >> 3) * half_bytes + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                    const DecodeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = su32(smem);
+    const uint32_t bars = sbase + kBarOff;
+    auto B = [&](int i) { return bars + 8u * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 8 * kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 8 * kNumBars + 4);
+    static_assert(8 * kNumBars + 8 <= kBarBytes, "barrier area");
+    if (smem - smem_raw > kAlignSlack) {  // the base was not aligned enough for the layout
+        if (threadIdx.x == 0 && a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
+        return;
+    }
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int gh = a.num_q_heads / a.num_kv_heads;
+    const int C = a.num_queries, nq = C * gh;
+    const int row0 = rt * kRows;
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
+    // tokens this row tile may see: up to the last query's position
+    const int L = visible_len(a, b, rt == 0 && h == 0 && threadIdx.x == 0);
+    const int last_row = min(nq, row0 + kRows) - 1;
+    const int t_end = L - C + last_row / gh + 1;
+    if (t_end <= 0) {  // every query of the tile sits at a negative position: zero rows
+        for (int i = threadIdx.x; i < kRows * kDim; i += kThreads) {
+            const int n = row0 + i / kDim;
+            if (n >= nq) continue;
+            const size_t orow = (static_cast<size_t>(b) * a.q_total + a.q_first + n / gh) * a.num_q_heads +
+                                static_cast<size_t>(h) * gh + n % gh;
+            static_cast<__nv_bfloat16*>(a.out)[orow * kDim + i % kDim] = __float2bfloat16_rn(0.f);
+        }
+        return;
+    }
+    const int nt = (t_end + kTok - 1) / kTok;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNumBars; ++i) {
+            const uint32_t cnt = (i == kSFree0 || i == kSFree1 || i == kPFull0 || i == kPFull1 || i == kQReady) ? 4u : 1u;
+            bar_init(B(i), cnt);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        if (a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
+    };
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        const int bs = a.block_size;
+        const int32_t* table = a.tables + static_cast<size_t>(b) * a.max_blocks;
+        const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
+        int issued = 0;
+        for (int j = 0; j < nt && !*abort_flag; ++j) {
+            const int s = j & 1;
+            if (j >= 2 && !bar_wait(B(kKvEmpty0 + s), ((j >> 1) - 1) & 1)) {
+                if (lane == 0) fail();
+                break;
+            }
+            const int tok0 = j * kTok, n = min(kTok, t_end - tok0), nblk = (n + bs - 1) / bs;
+            const uint32_t kst = sbase + kKVOff + s * kStageBytes, vst = kst + 2 * kHalfBytes;
+            if (lane == 0) bar_expect_tx(B(kKvFull0 + s), static_cast<uint32_t>(nblk * bs * 128 * 4));
+            for (int k = 0; k < nblk; ++k) {
+                const int idx = tok0 / bs + k;
+                int blk = (lane == 0 && idx < a.max_blocks) ? table[idx] : 0;
+                if (lane == 0 && static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks)) {
+                    if (a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
+                    blk = 0;  // read an in-bounds block; the flag marks the output invalid
+                }
+                if (lane == 0) {
+                    const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + h) * bs);
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const uint32_t off = hf * kHalfBytes + k * bs * 128;
+                        tma_3d(kst + off, &tmk, 0, y, hf, B(kKvFull0 + s));
+                        tma_3d(vst + off, &tmv, 0, y, hf, B(kKvFull0 + s));
+                    }
+                }
+            }
+            ++issued;
+        }
+        // drain: the copies in flight land before the CTA frees anything
+        if (lane == 0)
+            for (int j = issued - 1; j >= 0 && j >= issued - 2; --j) (void)bar_wait(B(kKvFull0 + (j & 1)), (j >> 1) & 1);
+    } else if (warp == 5) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            bool ok = bar_wait(B(kQReady), 0);
+            fence_after();
+            auto issue_s = [&](int j) -> bool {
+                const int s = j & 1;
+                if (!bar_wait(B(kKvFull0 + s), (j >> 1) & 1)) return false;
+                if (j >= 2 && !bar_wait(B(kSFree0 + s), ((j >> 1) - 1) & 1)) return false;
+                fence_after();
+                const uint32_t kst = sbase + kKVOff + s * kStageBytes;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {  // K = head_dim in 16-wide steps
+                    const uint32_t kin = (ks & 3) * 32;
+                    mma_bf16(tmem + s_col(s), sdesc(sbase + kQOff + (ks >> 2) * kQHalf + kin, 16),
+                             sdesc(kst + (ks >> 2) * kHalfBytes + kin, 16), idesc(kTok, 0), ks > 0 ? 1u : 0u);
+                }
+                mma_commit(B(kSFull0 + s));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; j < nt && ok && !*abort_flag; ++j) {
+                if (j + 1 < nt && !issue_s(j + 1)) {
+                    ok = false;
+                    break;
+                }
+                const int pb = j % kPBufs;  // P buffer of tile j
+                if (!bar_wait(B(kPFull0 + pb), (j / kPBufs) & 1)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                const uint32_t vst = sbase + kKVOff + (j & 1) * kStageBytes + 2 * kHalfBytes;
+                const uint32_t pbase = sbase + kPOff + pb * kPBytes;
+#pragma unroll
+                for (int ks = 0; ks < kTok / 16; ++ks)  // K = tokens in 16-wide steps
+                    mma_bf16(tmem + kOCol, sdesc(pbase + (ks & 3) * 32 + (ks >> 2) * kQHalf, 16),
+                             sdesc(vst + ks * 16 * 128, kHalfBytes), idesc(kDim, 1), (j > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(B(kPvDone0 + pb));
+                mma_commit(B(kKvEmpty0 + (j & 1)));
+            }
+            if (!ok) fail();
+            mma_commit(B(kDone));  // completes once every MMA issued above has finished
+            (void)bar_wait(B(kDone), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------- softmax + epilogue
+        const int m = threadIdx.x;  // query row of the tile = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+        const int n = row0 + m;
+        const bool valid = n < nq;
+        const int qc = valid ? n / gh : 0;
+        // Q row -> shared memory (swizzled K-major layout); padding rows are zero
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const __nv_bfloat16*>(a.q) +
+                ((static_cast<size_t>(b) * a.q_total + a.q_first + qc) * a.num_q_heads + static_cast<size_t>(h) * gh +
+                 (valid ? n % gh : 0)) *
+                    kDim);
+#pragma unroll 4
+            for (int ch = 0; ch < 16; ++ch) {
+                const uint4 v = valid ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(smem + kQOff + tile_off(m, ch, kQHalf)) = v;
+            }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) bar_arrive(B(kQReady));
+
+        const int lim = valid ? L - C + qc + 1 : 0;  // tokens visible to this row
+        const float qk = a.qk_scale_log2;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nt; ++j) {
+            const int s = j & 1, tok0 = j * kTok;
+            if (!bar_wait_warp(B(kSFull0 + s), (j >> 1) & 1) || !bar_wait_warp(B(kKvFull0 + s), (j >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            fence_after();
+            const uint32_t sa = tmem + lane_off + s_col(s);
+            // pass 1: the tile's row max over visible tokens
+            float mx = -INFINITY;
+#pragma unroll 1
+            for (int c4 = 0; c4 < kTok / 32; ++c4) {
+                uint32_t v[32];
+                tmem_ld32(sa + 32 * c4, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (tok0 + 32 * c4 + i < lim) mx = fmaxf(mx, __uint_as_float(v[i]) * qk);
+            }
+            // lazy base: move it (and rescale O and l) only when the max grew by > 8
+            const float m_new = fmaxf(m_used, mx);
+            const bool rescale = m_used != -INFINITY && m_new > m_used + 8.f;
+            const float base_new = m_used == -INFINITY || rescale ? m_new : m_used;
+            const int pb = j % kPBufs;
+            // this P buffer is free once the PV of tile j - kPBufs has finished
+            if (j >= kPBufs) {
+                if (!bar_wait_warp(B(kPvDone0 + pb), ((j - kPBufs) / kPBufs) & 1)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+            }
+            if (__any_sync(0xFFFFFFFFu, rescale)) {  // O is stable once the PV of tile j - 1 has finished
+                if (!bar_wait_warp(B(kPvDone0 + (j - 1) % kPBufs), ((j - 1) / kPBufs) & 1)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                const float alpha = rescale ? exp2f(m_used - m_new) : 1.f;
+                l *= alpha;
+#pragma unroll 1
+                for (int c4 = 0; c4 < 4; ++c4) {  // tcgen05.ld/st are warp-wide
+                    uint32_t o[32];
+                    const uint32_t oa = tmem + lane_off + kOCol + 32 * c4;
+                    tmem_ld32(oa, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(oa, o);
+                }
+            }
+            m_used = base_new;
+            const float base = m_used == -INFINITY ? 0.f : m_used;
+            // pass 2: probabilities -> P (BF16, swizzled K-major rows)
+            uint8_t* pdst = smem + kPOff + pb * kPBytes;
+#pragma unroll 1
+            for (int c4 = 0; c4 < kTok / 32; ++c4) {
+                uint32_t v[32];
+                tmem_ld32(sa + 32 * c4, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t0 = tok0 + 32 * c4 + 2 * i;
+                    const float p0 = t0 < lim ? exp2f(__uint_as_float(v[2 * i]) * qk - base) : 0.f;
+                    const float p1 = t0 + 1 < lim ? exp2f(__uint_as_float(v[2 * i + 1]) * qk - base) : 0.f;
+                    l += p0 + p1;
+                    pk[i] = pack_bf16x2_rn(p0, p1);
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<uint4*>(pdst + tile_off(m, 4 * c4 + q4, kQHalf)) =
+                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(B(kSFree0 + s));  // the score buffer may be overwritten
+            // V rows past the tile's tokens: zero (stale or unwritten rows could hold NaN)
+            const int nvalid = min(kTok, t_end - tok0);
+            if (nvalid < kTok) {
+                uint8_t* vs = smem + kKVOff + s * kStageBytes + 2 * kHalfBytes;
+                for (int e = m; e < 2 * (kTok - nvalid) * 8; e += 128) {
+                    const int hf = e / ((kTok - nvalid) * 8), rem = e % ((kTok - nvalid) * 8);
+                    const int r = nvalid + rem / 8, ch = rem % 8;
+                    *reinterpret_cast<uint4*>(vs + hf * kHalfBytes + r * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }  // (the PV MMA waits for all four warps' P signals, so every zero lands first)
+            fence_async_smem();
+            fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(B(kPFull0 + pb));
+        }
+        // epilogue: O / l -> BF16 output rows
+        if (ok && bar_wait_warp(B(kPvDone0 + (nt - 1) % kPBufs), ((nt - 1) / kPBufs) & 1)) {
+            fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16* orow =
+                static_cast<__nv_bfloat16*>(a.out) +
+                ((static_cast<size_t>(b) * a.q_total + a.q_first + qc) * a.num_q_heads + static_cast<size_t>(h) * gh +
+                 (valid ? n % gh : 0)) *
+                    kDim;
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + kOCol + 32 * c4, v);
+                if (valid) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 w;
+                        w.x = pack_bf16x2_rn(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
+                        w.y = pack_bf16x2_rn(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
+                        w.z = pack_bf16x2_rn(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
+                        w.w = pack_bf16x2_rn(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + 32 * c4 + 8 * q4) = w;
+                    }
+                }
+            }
+        } else if (lane == 0) {
+            fail();
+        }
+    }
+    // teardown: every role has finished its waits (all bounded); free TMEM
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+}  // namespace
+
+bool attention_tc_supported(pkv_dtype kv, int head_dim, int block_size) {
+    return kv == PKV_BF16 && head_dim == kDim && (block_size == 16 || block_size == 32 || block_size == 64);
+}
+
+cudaError_t launch_attention_tc(const DecodeArgs& a, const void* tmap_k, const void* tmap_v, cudaStream_t stream) {
+    static int configured_mask = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 31) return cudaErrorNotSupported;
+    if (!(configured_mask & (1 << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e == cudaSuccess)  // the largest carveout, so that two CTAs fit per SM
+            e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        configured_mask |= 1 << dev;
+    }
+    const int nq = a.num_queries * (a.num_q_heads / a.num_kv_heads);
+    dim3 grid((nq + kRows - 1) / kRows, a.num_kv_heads, a.num_seqs);
+    // (2 CTAs per SM by shared memory; each allocates half of the tensor memory)
+    attention_tc_kernel<<<grid, kThreads, kSmem, stream>>>(*static_cast<const CUtensorMap*>(tmap_k),
+                                                           *static_cast<const CUtensorMap*>(tmap_v), a);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -23,6 +23,9 @@ struct pkv_pool {
     int tmap_pair;           // 1: tmap_k2 / tmap_v2 are ready (3D boxes of two adjacent KV heads of a block)
     CUtensorMap tmap_k2;
     CUtensorMap tmap_v2;
+    int tmap_half;           // 1: tmap_kh / tmap_vh are ready (3D boxes of one 64-column half of a block)
+    CUtensorMap tmap_kh;
+    CUtensorMap tmap_vh;
 };
 
 namespace pkv {
@@ -92,5 +95,8 @@ bool decode_mma_supported(pkv_dtype kv, int head_dim, int rows, int block_size);
 constexpr int kMmaMaxRows = 64;   // query rows per KV head one tensor-core launch serves
 constexpr int kSimtMaxRows = 16;  // the same for the SIMT design
 cudaError_t launch_combine(pkv_dtype q_dtype, const DecodeArgs& a, cudaStream_t stream);
+// tcgen05 multi-query attention (long query lists); one launch for all queries.
+bool attention_tc_supported(pkv_dtype kv, int head_dim, int block_size);
+cudaError_t launch_attention_tc(const DecodeArgs& a, const void* tmap_k, const void* tmap_v, cudaStream_t stream);
 
 }  // namespace pkv

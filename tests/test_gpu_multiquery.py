@@ -29,21 +29,22 @@ def _filled(w):
     return inst, batch
 
 
-CASES = [  # (G, C, kv, designs); launches: tensor cores take up to 64 query rows per KV head
-    (4, 2, "bf16", ("mma", "simt")),
+CASES = [  # (G, C, kv, designs); mma launches take up to 64 query rows per KV head, tc 128 per CTA
+    (4, 2, "bf16", ("mma", "simt", "tc")),
     (4, 2, "fp8", ("mma",)),
     (2, 4, "bf16", ("mma", "simt")),
-    (1, 8, "bf16", ("mma", "simt")),
+    (1, 8, "bf16", ("mma", "simt", "tc")),
     (2, 4, "f32", ("simt",)),
     (4, 4, "bf16", ("mma", "simt")),    # 16 rows: two column groups of warps
     (4, 8, "bf16", ("mma", "simt")),    # 32 rows; SIMT in two launches
     (4, 8, "fp8", ("mma",)),
-    (4, 16, "bf16", ("mma",)),          # 64 rows: two n-tiles per warp
+    (4, 16, "bf16", ("mma", "tc")),     # 64 rows: two n-tiles per warp / half a tcgen05 tile
     (4, 16, "fp8", ("mma",)),
-    (4, 40, "bf16", ("mma", "simt")),   # chunks 16 + 16 + 8 (tensor cores)
-    (8, 8, "bf16", ("mma",)),           # 64 rows
-    (1, 100, "bf16", ("mma",)),         # chunks 64 + 36 (36 rows in the 64-row kernel)
-    (3, 5, "bf16", ("mma",)),           # 3 query heads per KV head: 15 rows padded to 16
+    (4, 40, "bf16", ("mma", "simt", "tc")),  # chunks 16 + 16 + 8 (mma); 160 rows = 2 tcgen05 tiles
+    (8, 8, "bf16", ("mma", "tc")),      # 64 rows
+    (1, 100, "bf16", ("mma", "tc")),    # chunks 64 + 36 (mma)
+    (3, 5, "bf16", ("mma", "tc")),      # 3 query heads per KV head: 15 rows padded to 16
+    (4, 100, "bf16", ("tc",)),          # 400 rows: 4 tcgen05 row tiles, the last partial
 ]
 
 
@@ -51,6 +52,10 @@ CASES = [  # (G, C, kv, designs); launches: tensor cores take up to 64 query row
 @pytest.mark.parametrize("G,C,kv,algos", CASES, ids=lambda x: str(x))
 def test_multi_query_parity(G, C, kv, algos, split):
     lens = (C - 1, C, C + 1, 17, 64, 65, 300, 1000) if C < 64 else (C - 1, C, C + 1, 17, 130, 300, 1000, 1500)
+    if "tc" in algos and split:
+        algos = tuple(x for x in algos if x != "tc")  # the tcgen05 design takes no fixed splits
+        if not algos:
+            pytest.skip("fixed splits: tcgen05 design not used")
     w = _w("mq_%s_g%d_c%d" % (kv, G, C), G, 2, kv, "f32" if kv == "f32" else "bf16", lens,
            D=64 if kv == "f32" else 128)
     inst, batch = _filled(w)
