@@ -19,13 +19,15 @@
 //    TMEM output accumulator.  tcgen05.commit signals mbarriers.
 //  * warps 0-3, softmax and epilogue: thread m owns query row m (TMEM lane m).
 //    It reads its 64 scores with tcgen05.ld (twice: max, then
-//    probabilities), masks causally, and writes P in BF16 to shared memory in
-//    the swizzled K-major layout.  The running max is updated lazily: O (in
+//    probabilities), masks causally, and overwrites the score buffer with P
+//    as BF16 pairs, which the PV MMA reads as its A operand from tensor
+//    memory; no shared-memory P, so a softmax never waits for the previous
+//    PV except to rescale O.  The running max is updated lazily: O (in
 //    TMEM) and the running sum are rescaled only when the row max grows by
 //    more than 8 in log2 units, so probabilities stay below 2^8 and fp32 keeps
 //    full precision; the final division by the sum uses the same base.
 //  * Epilogue: O / l, rounded to BF16, written to the output rows.
-// Shared memory: Q 32 KB, P 16 KB, 2 stages x (K 16 KB + V 16 KB) for 64-token
+// Shared memory: Q 32 KB, 2 stages x (K 16 KB + V 16 KB) for 64-token
 // tiles; TMEM: two 64-column score buffers and a 128-column output
 // accumulator (256 allocated); 2 CTAs per SM, so that two softmax warpgroups
 // share each SM.  Every mbarrier wait is bounded; on expiry the CTA
@@ -43,26 +45,22 @@ constexpr int kRows = 128;                 // query rows per CTA
 constexpr int kTok = 64;                   // tokens per tile
 constexpr int kDim = 128;                  // head_dim
 constexpr uint32_t kSpin = 1u << 22;       // polls before a wait gives up
-constexpr int kPBufs = 1;                  // P buffers (the softmax, not the PV, bounds a tile)
 constexpr int kQHalf = kRows * 128;        // one 64-column half of the Q tile: 16 KB
 constexpr int kHalfBytes = kTok * 128;     // one 64-column half of a K or V tile: 8 KB
-constexpr int kPBytes = kRows * kTok * 2;  // P tile: 16 KB
 constexpr int kQOff = 0;
-constexpr int kPOff = 2 * kQHalf;
-constexpr int kKVOff = kPOff + kPBufs * kPBytes;
+constexpr int kKVOff = 2 * kQHalf;
 constexpr int kStageBytes = 4 * kHalfBytes;  // K (16 KB) + V (16 KB)
 constexpr int kBarOff = kKVOff + 2 * kStageBytes;
 constexpr int kBarBytes = 128;
-constexpr int kSmem = 115712;              // the most that lets 2 CTAs share an SM
-constexpr int kAlignSlack = kSmem - kBarOff - kBarBytes;  // room to align the base to 1024 B
-static_assert(kAlignSlack >= 0, "shared memory budget");
+constexpr int kAlignSlack = 1024;          // room to align the base to 1024 B
+constexpr int kSmem = kBarOff + kBarBytes + kAlignSlack;
+static_assert(kSmem <= 115712, "two CTAs per SM");
 constexpr uint32_t kTmemCols = 256;        // per CTA: 2 CTAs per SM
 constexpr uint32_t kOCol = 2 * kTok;       // score buffers at columns 0 and kTok
 __device__ __forceinline__ uint32_t s_col(int s) { return s ? static_cast<uint32_t>(kTok) : 0u; }
 
 // mbarriers (8 bytes each) after the tiles
-enum Bar { kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1,
-           kPvDone0, kPvDone1, kQReady, kDone, kNumBars };
+enum Bar { kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kSFull0, kSFull1, kPFull, kPvDone, kQReady, kDone, kNumBars };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -121,22 +119,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uin
         "l"(a), "l"(b), "r"(id), "r"(acc)
         : "memory");
 }
+// A from tensor memory (rows on lanes, BF16 pairs per 32-bit column).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t b) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(b) : "memory");
 }
 
-// 32 consecutive TMEM columns of this thread's lane (no wait).
-__device__ __forceinline__ void tmem_ld32_async(uint32_t a, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
-        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
-          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(a));
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 // 32 consecutive TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t a, uint32_t (&v)[32]) {
     asm volatile(
@@ -159,6 +152,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t a, const uint32_t (&v)[32]) {
         "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
+// 2^x on the special-function unit (relative error about 2^-22, flushes
+// subnormal results to zero: probabilities are rounded to BF16 anyway).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // Byte offset of 16-byte chunk `ch` (8 BF16 each) of row r in a
@@ -208,7 +213,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
-            const uint32_t cnt = (i == kSFree0 || i == kSFree1 || i == kPFull0 || i == kPFull1 || i == kQReady) ? 4u : 1u;
+            const uint32_t cnt = (i == kPFull || i == kQReady) ? 4u : 1u;
             bar_init(B(i), cnt);
         }
         *abort_flag = 0;
@@ -270,10 +275,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         if (lane == 0) {
             bool ok = bar_wait(B(kQReady), 0);
             fence_after();
+            // S_j goes to buffer j & 1; the PV of tile j - 2, which read P from
+            // that buffer, was issued before it, and MMAs run in issue order
             auto issue_s = [&](int j) -> bool {
                 const int s = j & 1;
                 if (!bar_wait(B(kKvFull0 + s), (j >> 1) & 1)) return false;
-                if (j >= 2 && !bar_wait(B(kSFree0 + s), ((j >> 1) - 1) & 1)) return false;
                 fence_after();
                 const uint32_t kst = sbase + kKVOff + s * kStageBytes;
 #pragma unroll
@@ -291,19 +297,17 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                     ok = false;
                     break;
                 }
-                const int pb = j % kPBufs;  // P buffer of tile j
-                if (!bar_wait(B(kPFull0 + pb), (j / kPBufs) & 1)) {
+                if (!bar_wait(B(kPFull), j & 1)) {
                     ok = false;
                     break;
                 }
                 fence_after();
                 const uint32_t vst = sbase + kKVOff + (j & 1) * kStageBytes + 2 * kHalfBytes;
-                const uint32_t pbase = sbase + kPOff + pb * kPBytes;
 #pragma unroll
-                for (int ks = 0; ks < kTok / 16; ++ks)  // K = tokens in 16-wide steps
-                    mma_bf16(tmem + kOCol, sdesc(pbase + (ks & 3) * 32 + (ks >> 2) * kQHalf, 16),
-                             sdesc(vst + ks * 16 * 128, kHalfBytes), idesc(kDim, 1), (j > 0 || ks > 0) ? 1u : 0u);
-                mma_commit(B(kPvDone0 + pb));
+                for (int ks = 0; ks < kTok / 16; ++ks)  // K = tokens in 16-wide steps: 8 TMEM columns of P each
+                    mma_bf16_ta(tmem + kOCol, tmem + s_col(j & 1) + 8 * ks, sdesc(vst + ks * 16 * 128, kHalfBytes),
+                                idesc(kDim, 1), (j > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(B(kPvDone));
                 mma_commit(B(kKvEmpty0 + (j & 1)));
             }
             if (!ok) fail();
@@ -341,42 +345,43 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         bool ok = true;
         for (int j = 0; j < nt; ++j) {
             const int s = j & 1, tok0 = j * kTok;
-            if (!bar_wait_warp(B(kSFull0 + s), (j >> 1) & 1) || !bar_wait_warp(B(kKvFull0 + s), (j >> 1) & 1)) {
+            if (!bar_wait_warp(B(kSFull0 + s), (j >> 1) & 1)) {
                 ok = false;
                 break;
             }
             fence_after();
             const uint32_t sa = tmem + lane_off + s_col(s);
-            // pass 1: the tile's row max over visible tokens
+            // the whole warp sees every token of the tile: no causal compares
+            const bool full = __all_sync(0xFFFFFFFFu, tok0 + kTok <= lim);
+            // pass 1: the tile's row max over visible tokens (of the raw
+            // scores when the scale is positive, then scaled once)
             float mx = -INFINITY;
 #pragma unroll 1
             for (int c4 = 0; c4 < kTok / 32; ++c4) {
                 uint32_t v[32];
                 tmem_ld32(sa + 32 * c4, v);
+                if (full && qk > 0.f) {
+                    float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (tok0 + 32 * c4 + i < lim) mx = fmaxf(mx, __uint_as_float(v[i]) * qk);
+                    for (int i = 0; i < 32; ++i) m2[i & 3] = fmaxf(m2[i & 3], __uint_as_float(v[i]));
+                    mx = fmaxf(mx, fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3])) * qk);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (tok0 + 32 * c4 + i < lim) mx = fmaxf(mx, __uint_as_float(v[i]) * qk);
+                }
             }
             // lazy base: move it (and rescale O and l) only when the max grew by > 8
             const float m_new = fmaxf(m_used, mx);
             const bool rescale = m_used != -INFINITY && m_new > m_used + 8.f;
             const float base_new = m_used == -INFINITY || rescale ? m_new : m_used;
-            const int pb = j % kPBufs;
-            // this P buffer is free once the PV of tile j - kPBufs has finished
-            if (j >= kPBufs) {
-                if (!bar_wait_warp(B(kPvDone0 + pb), ((j - kPBufs) / kPBufs) & 1)) {
-                    ok = false;
-                    break;
-                }
-                fence_after();
-            }
             if (__any_sync(0xFFFFFFFFu, rescale)) {  // O is stable once the PV of tile j - 1 has finished
-                if (!bar_wait_warp(B(kPvDone0 + (j - 1) % kPBufs), ((j - 1) / kPBufs) & 1)) {
+                if (!bar_wait_warp(B(kPvDone), (j - 1) & 1)) {
                     ok = false;
                     break;
                 }
                 fence_after();
-                const float alpha = rescale ? exp2f(m_used - m_new) : 1.f;
+                const float alpha = rescale ? ex2(m_used - m_new) : 1.f;
                 l *= alpha;
 #pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {  // tcgen05.ld/st are warp-wide
@@ -390,46 +395,56 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
             }
             m_used = base_new;
             const float base = m_used == -INFINITY ? 0.f : m_used;
-            // pass 2: probabilities -> P (BF16, swizzled K-major rows)
-            uint8_t* pdst = smem + kPOff + pb * kPBytes;
-#pragma unroll 1
+            // pass 2: probabilities -> P as BF16 pairs over the first kTok/2
+            // columns of this score buffer (only columns already read)
+            uint32_t pk[kTok / 2];
+            float l2[2] = {0.f, 0.f};
+#pragma unroll
             for (int c4 = 0; c4 < kTok / 32; ++c4) {
                 uint32_t v[32];
                 tmem_ld32(sa + 32 * c4, v);
-                uint32_t pk[16];
+                if (full) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t0 = tok0 + 32 * c4 + 2 * i;
-                    const float p0 = t0 < lim ? exp2f(__uint_as_float(v[2 * i]) * qk - base) : 0.f;
-                    const float p1 = t0 + 1 < lim ? exp2f(__uint_as_float(v[2 * i + 1]) * qk - base) : 0.f;
-                    l += p0 + p1;
-                    pk[i] = pack_bf16x2_rn(p0, p1);
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(__uint_as_float(v[2 * i]), qk, -base));
+                        const float p1 = ex2(fmaf(__uint_as_float(v[2 * i + 1]), qk, -base));
+                        l2[i & 1] += p0 + p1;
+                        pk[16 * c4 + i] = bf16x2(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int t0 = tok0 + 32 * c4 + 2 * i;
+                        const float p0 = t0 < lim ? ex2(fmaf(__uint_as_float(v[2 * i]), qk, -base)) : 0.f;
+                        const float p1 = t0 + 1 < lim ? ex2(fmaf(__uint_as_float(v[2 * i + 1]), qk, -base)) : 0.f;
+                        l2[i & 1] += p0 + p1;
+                        pk[16 * c4 + i] = bf16x2(p0, p1);
+                    }
                 }
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<uint4*>(pdst + tile_off(m, 4 * c4 + q4, kQHalf)) =
-                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
             }
-            fence_before();
-            __syncwarp();
-            if (lane == 0) bar_arrive(B(kSFree0 + s));  // the score buffer may be overwritten
+            l += l2[0] + l2[1];
+            tmem_st32(sa, pk);
             // V rows past the tile's tokens: zero (stale or unwritten rows could hold NaN)
             const int nvalid = min(kTok, t_end - tok0);
             if (nvalid < kTok) {
+                if (!bar_wait_warp(B(kKvFull0 + s), (j >> 1) & 1)) {  // after the copy into this stage
+                    ok = false;
+                    break;
+                }
                 uint8_t* vs = smem + kKVOff + s * kStageBytes + 2 * kHalfBytes;
                 for (int e = m; e < 2 * (kTok - nvalid) * 8; e += 128) {
                     const int hf = e / ((kTok - nvalid) * 8), rem = e % ((kTok - nvalid) * 8);
                     const int r = nvalid + rem / 8, ch = rem % 8;
                     *reinterpret_cast<uint4*>(vs + hf * kHalfBytes + r * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
-            }  // (the PV MMA waits for all four warps' P signals, so every zero lands first)
-            fence_async_smem();
+                fence_async_smem();  // (the PV MMA waits for all four warps' P signals)
+            }
             fence_before();
             __syncwarp();
-            if (lane == 0) bar_arrive(B(kPFull0 + pb));
+            if (lane == 0) bar_arrive(B(kPFull));
         }
         // epilogue: O / l -> BF16 output rows
-        if (ok && bar_wait_warp(B(kPvDone0 + (nt - 1) % kPBufs), ((nt - 1) / kPBufs) & 1)) {
+        if (ok && bar_wait_warp(B(kPvDone), (nt - 1) & 1)) {
             fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16* orow =
@@ -445,10 +460,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 w;
-                        w.x = pack_bf16x2_rn(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
-                        w.y = pack_bf16x2_rn(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
-                        w.z = pack_bf16x2_rn(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
-                        w.w = pack_bf16x2_rn(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
+                        w.x = bf16x2(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
+                        w.y = bf16x2(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
+                        w.z = bf16x2(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
+                        w.w = bf16x2(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
                         *reinterpret_cast<uint4*>(orow + 32 * c4 + 8 * q4) = w;
                     }
                 }
