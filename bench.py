@@ -81,7 +81,8 @@ def _profile_traffic(kernel_tag: str, src_hash: str):
 
 KERNEL_SOURCES = {"simt": ("decode_simt.cu", "device_common.cuh", "pkv_internal.h"),
                   "mma": ("decode_mma.cuh", "decode_mma.cu", "decode_mma_bf16.cu", "decode_mma_fp8.cu",
-                          "device_common.cuh", "pkv_internal.h")}
+                          "device_common.cuh", "pkv_internal.h"),
+                  "tc": ("attention_tc.cu", "device_common.cuh", "pkv_internal.h")}
 
 
 def kernel_hash(algo: str) -> str:
@@ -154,7 +155,7 @@ class Clocks:
 def query_chunks(C: int, gh: int, algo: str, kv_dtype: str) -> int:
     """Attention launches per call: query chunks of at most 64 rows per KV
     head (tensor-core design) or a power of two of rows the SIMT design holds."""
-    if C <= 1:
+    if C <= 1 or algo == "tc":
         return 1
     if algo == "mma":
         cq = max(1, 64 // gh)
@@ -216,9 +217,11 @@ def run_ours(args):
         S, NS, wsb = pk.multi_query_plan(batch.pool, w.num_seqs, C, w.num_q_heads, max_len, split)
     else:
         S, NS, wsb = pk.decode_plan(batch.pool, w.num_seqs, w.num_q_heads, max_len, split)
-    algo = pk.decode_algo(batch.pool, w.num_q_heads, args.algo)
+    algo = (pk.multi_query_algo(batch.pool, C, w.num_q_heads, split, args.algo) if C > 1
+            else pk.decode_algo(batch.pool, w.num_q_heads, args.algo))
     fused = (not args.unfused) and C == 1 and algo == "mma" and w.group <= 8
-    schedule = "balanced" if (algo == "mma" and split == 0) else "fixed splits"
+    schedule = ("one CTA per 128 query rows" if algo == "tc" else
+                "balanced" if (algo == "mma" and split == 0) else "fixed splits")
     work = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -291,7 +294,7 @@ def run_ours(args):
     B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     # algorithmic bytes of one attention call (one layer)
     blocks_read = int(((inst.lens.long() + w.block_size - 1) // w.block_size).sum())
-    combine = schedule != "balanced" and NS > 1
+    combine = schedule == "fixed splits" and NS > 1
     part = 0
     if combine:
         nsplit = int(((inst.lens.long() + S - 1) // S).sum())
@@ -371,8 +374,8 @@ def run_ours(args):
                    "step": ("append fused into the attention launch" if fused else
                             "kv_append launch + attention launch"),
                    "sum_seq_len": sum_len, "kv_bytes_per_step": kv_bytes,
-                   "split_tokens": S if schedule != "balanced" else None,
-                   "num_splits": NS if schedule != "balanced" else None, "schedule": schedule, "algo": algo,
+                   "split_tokens": S if schedule == "fixed splits" else None,
+                   "num_splits": NS if schedule == "fixed splits" else None, "schedule": schedule, "algo": algo,
                    "parallelism": "replica per GPU" if ws > 1 else "1 GPU",
                    "l2": "inputs exceed L2 (%.0f MB KV per layer vs 129 MB L2); no flush" % (kv_layer / 1e6)},
         "roofline": roof,

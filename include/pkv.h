@@ -209,6 +209,10 @@ pkv_status paged_multi_query_plan(const pkv_pool* pool, int32_t num_seqs, int32_
                                   int32_t num_q_heads, int32_t max_seq_len, int32_t split_tokens,
                                   int32_t* split_tokens_out, int32_t* num_splits_out,
                                   size_t* workspace_bytes_out);
+/* The kernel design paged_multi_query_attention would run for this request:
+ * PKV_ALGO_TC, PKV_ALGO_MMA or PKV_ALGO_SIMT, or -1 when it cannot be served. */
+int32_t paged_multi_query_algo(const pkv_pool* pool, int32_t num_queries, int32_t num_q_heads,
+                               int32_t split_tokens, pkv_algo requested);
 pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const pkv_pool* pool,
                                        int32_t layer, const int32_t* block_tables,
                                        int32_t max_blocks_per_seq, const int32_t* seq_lens,

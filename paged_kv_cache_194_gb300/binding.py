@@ -25,7 +25,8 @@ ERRBIT_BLOCK_ID, ERRBIT_SLOT, ERRBIT_SEQ_LEN, ERRBIT_TIMEOUT = 1, 2, 4, 8
 # Every symbol include/pkv.h declares.
 EXPORTS = ("kv_pool_create", "kv_pool_destroy", "kv_pool_tensor_bytes", "kv_bytes_per_token",
            "kv_append", "paged_decode_plan", "paged_decode_algo", "paged_decode_attention",
-           "paged_multi_query_plan", "paged_multi_query_attention", "paged_decode_append_attention",
+           "paged_multi_query_plan", "paged_multi_query_algo", "paged_multi_query_attention",
+           "paged_decode_append_attention",
            "paged_decode_attention_static_ws", "pkv_status_string", "pkv_last_cuda_error",
            "kv_block_manager_create", "kv_block_manager_destroy", "kv_bm_num_free", "kv_bm_add_sequence",
            "kv_bm_free_sequence", "kv_bm_grow", "kv_bm_decode_slots", "kv_bm_match_prefix", "kv_bm_seq_len",
@@ -88,6 +89,8 @@ def lib() -> ctypes.CDLL:
     L.paged_multi_query_attention.argtypes = [P, c.c_int, P, c.c_int32, P, c.c_int32, P, c.c_int32, c.c_int32,
                                               c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int, P,
                                               c.c_size_t, P, P]
+    L.paged_multi_query_algo.restype = c.c_int32
+    L.paged_multi_query_algo.argtypes = [P, c.c_int32, c.c_int32, c.c_int32, c.c_int]
     L.paged_decode_append_attention.restype = c.c_int
     L.paged_decode_append_attention.argtypes = [P, c.c_int, P, P, c.c_int, P, c.c_int32, P, c.c_int32, P,
                                                 c.c_int32, c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int,
@@ -305,6 +308,15 @@ def multi_query_plan(pool: KVPool, num_seqs: int, num_queries: int, num_q_heads:
                                         ctypes.byref(S), ctypes.byref(NS), ctypes.byref(ws)),
            "paged_multi_query_plan")
     return S.value, NS.value, ws.value
+
+
+def multi_query_algo(pool: KVPool, num_queries: int, num_q_heads: int, split_tokens: int = 0,
+                     algo: str = "auto") -> str:
+    """Name of the kernel design a multi-query call with this request would run."""
+    r = lib().paged_multi_query_algo(pool.handle, num_queries, num_q_heads, split_tokens, ALGOS[algo])
+    if r < 0:
+        raise PkvError(2, "no kernel design serves this request")
+    return ALGO_NAMES[r]
 
 
 def paged_multi_query_attention(q: torch.Tensor, pool: KVPool, layer: int, block_tables: torch.Tensor,

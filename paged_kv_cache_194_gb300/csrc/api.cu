@@ -338,6 +338,35 @@ int32_t paged_decode_algo(const pkv_pool* p, int32_t G, pkv_algo algo) {
 
 namespace pkv {
 namespace {
+// The kernel design a call runs: PKV_ALGO_TC (tcgen05, whole query list in
+// one launch; the default from kTcMinRows query rows per KV head), MMA or
+// SIMT, or -1 when the request cannot be served.  fused: the decode step's
+// append runs inside the launch (tensor-core design only).
+int design_for(const pkv_pool* p, int C, int gh, int split_tokens, pkv_algo algo, bool fused) {
+    pkv_pool* mp = const_cast<pkv_pool*>(p);  // the handle caches its TMA descriptors
+    const bool tc_fits = attention_tc_supported(p->d.kv_dtype, p->d.head_dim, p->d.block_size) && !fused &&
+                         split_tokens == 0 && static_cast<int64_t>(C) * gh <= (1 << 24);
+    const bool mma_fits = decode_mma_supported(p->d.kv_dtype, p->d.head_dim, mma_chunk(gh, C) * gh, p->d.block_size);
+    const bool simt_fits = decode_simt_supported(p->d.kv_dtype, p->d.head_dim, simt_chunk(p, gh, C) * gh);
+    int d = -1;
+    if (algo == PKV_ALGO_TC) {
+        d = tc_fits && ensure_tmaps(mp) && p->tmap_half == 1 ? PKV_ALGO_TC : -1;
+    } else if (algo == PKV_ALGO_MMA) {
+        d = mma_fits && ensure_tmaps(mp) ? PKV_ALGO_MMA : -1;
+    } else if (algo == PKV_ALGO_SIMT) {
+        d = simt_fits ? PKV_ALGO_SIMT : -1;
+    } else if (algo == PKV_ALGO_AUTO) {
+        if (tc_fits && C > 1 && C * gh >= kTcMinRows && ensure_tmaps(mp) && p->tmap_half == 1)
+            d = PKV_ALGO_TC;
+        else if (mma_fits && ensure_tmaps(mp))
+            d = PKV_ALGO_MMA;
+        else if (simt_fits)
+            d = PKV_ALGO_SIMT;
+    }
+    if (fused && (d != PKV_ALGO_MMA || C != 1 || gh > 8)) return -1;
+    return d;
+}
+
 // Attention for C queries per sequence; with new_k != nullptr (decode only)
 // the kernel also appends each sequence's newest token.
 pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,
@@ -364,28 +393,11 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
     const int gh = num_q_heads / p->d.num_kv_heads;  // query heads per KV head
     const int cq_mma = mma_chunk(gh, num_queries), cq_simt = simt_chunk(p, gh, num_queries);
 
-    bool use_mma = false;
-    pkv_pool* mp = const_cast<pkv_pool*>(p);  // the handle caches its TMA descriptors
-    // tcgen05 design: the whole query list in one launch, 128 rows per CTA;
-    // the default from kTcMinRows query rows per KV head (prompt chunks)
-    const bool tc_fits = attention_tc_supported(p->d.kv_dtype, p->d.head_dim, p->d.block_size) && !new_k &&
-                         split_tokens == 0 && static_cast<int64_t>(num_queries) * gh <= (1 << 24);
-    if (algo == PKV_ALGO_TC) {
-        if (!tc_fits || !ensure_tmaps(mp) || p->tmap_half != 1) return PKV_ERR_UNSUPPORTED;
-    }
-    const bool use_tc = algo == PKV_ALGO_TC ||
-                        (algo == PKV_ALGO_AUTO && tc_fits && num_queries > 1 && num_queries * gh >= kTcMinRows &&
-                         ensure_tmaps(mp) && p->tmap_half == 1);
-    const bool mma_fits = decode_mma_supported(p->d.kv_dtype, p->d.head_dim, cq_mma * gh, p->d.block_size);
-    if (algo == PKV_ALGO_MMA) {
-        if (!mma_fits || !ensure_tmaps(mp)) return PKV_ERR_UNSUPPORTED;
-        use_mma = true;
-    } else if (algo == PKV_ALGO_AUTO) {
-        use_mma = mma_fits && ensure_tmaps(mp);
-    }
-    if (!use_tc && !use_mma && !decode_simt_supported(p->d.kv_dtype, p->d.head_dim, cq_simt * gh))
-        return PKV_ERR_UNSUPPORTED;
-    if (new_k && (!use_mma || num_queries != 1 || gh > 8)) return PKV_ERR_UNSUPPORTED;
+    (void)cq_mma;
+    (void)cq_simt;
+    const int design = design_for(p, num_queries, gh, split_tokens, algo, new_k != nullptr);
+    if (design < 0) return PKV_ERR_UNSUPPORTED;
+    const bool use_tc = design == PKV_ALGO_TC, use_mma = design == PKV_ALGO_MMA;
 
     int32_t S = 0, NS = 0;
     size_t need = 0;
@@ -490,6 +502,14 @@ pkv_status paged_multi_query_attention(const void* q, pkv_dtype q_dtype, const p
     return pkv::attention_call(q, q_dtype, p, layer, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                                num_queries, num_q_heads, max_seq_len, scale, split_tokens, algo, workspace,
                                workspace_bytes, out, stream, nullptr, nullptr, PKV_BF16);
+}
+
+int32_t paged_multi_query_algo(const pkv_pool* p, int32_t num_queries, int32_t num_q_heads, int32_t split_tokens,
+                               pkv_algo algo) {
+    if (!p || num_queries < 1 || num_queries > pkv::kMaxQueries || num_q_heads < 1 ||
+        num_q_heads % p->d.num_kv_heads != 0 || split_tokens < 0)
+        return -1;
+    return pkv::design_for(p, num_queries, num_q_heads / p->d.num_kv_heads, split_tokens, algo, false);
 }
 
 pkv_status paged_decode_append_attention(const void* q, pkv_dtype q_dtype, const void* k_new, const void* v_new,
