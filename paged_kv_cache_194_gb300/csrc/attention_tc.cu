@@ -9,8 +9,8 @@
 // sits at position L - C + c of its visible length L and attends causally.
 //
 // One CTA per (128 query rows, KV head, sequence); 6 warps:
-//  * warp 4, TMA producer: per 64-token tile, one box {64 columns, bs rows,
-//    1 half} per KV block and half for K and for V, so a stage holds each of
+//  * warps 4 and 6, TMA producers for K and for V: per 64-token tile, one box
+//    {64 columns, bs rows, 1 half} per KV block and half, so a stage holds each of
 //    K and V as [half: head_dim 0-63 | 64-127][64 token rows][128 B], 128-byte
 //    swizzled -- the K-major operand layout for K and the MN-major one for V.
 //  * warp 5, MMA issuer (one thread): S_j = Q K_j^T (M 128 rows, N 64 tokens,
@@ -40,7 +40,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;              // warps 0-3 softmax, 4 K producer, 5 MMA, 6 V producer
 constexpr int kRows = 128;                 // query rows per CTA
 constexpr int kTok = 64;                   // tokens per tile
 constexpr int kDim = 128;                  // head_dim
@@ -51,7 +51,7 @@ constexpr int kQOff = 0;
 constexpr int kKVOff = 2 * kQHalf;
 constexpr int kStageBytes = 4 * kHalfBytes;  // K (16 KB) + V (16 KB)
 constexpr int kBarOff = kKVOff + 2 * kStageBytes;
-constexpr int kBarBytes = 128;
+constexpr int kBarBytes = 192;
 constexpr int kAlignSlack = 1024;          // room to align the base to 1024 B
 constexpr int kSmem = kBarOff + kBarBytes + kAlignSlack;
 static_assert(kSmem <= 115712, "two CTAs per SM");
@@ -60,7 +60,8 @@ constexpr uint32_t kOCol = 2 * kTok;       // score buffers at columns 0 and kTo
 __device__ __forceinline__ uint32_t s_col(int s) { return s ? static_cast<uint32_t>(kTok) : 0u; }
 
 // mbarriers (8 bytes each) after the tiles
-enum Bar { kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kSFull0, kSFull1, kPFull, kPvDone, kQReady, kDone, kNumBars };
+enum Bar { kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1, kSFull0, kSFull1, kPFull0,
+           kPFull1, kPvDone, kQReady, kDone, kNumBars };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -130,6 +131,17 @@ __device__ __forceinline__ void mma_commit(uint32_t b) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(b) : "memory");
 }
 
+// 32 consecutive TMEM columns of this thread's lane, without waiting.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t a, uint32_t* v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(a));
+}
 // 32 consecutive TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t a, uint32_t (&v)[32]) {
     asm volatile(
@@ -213,7 +225,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
-            const uint32_t cnt = (i == kPFull || i == kQReady) ? 4u : 1u;
+            const uint32_t cnt = (i == kPFull0 || i == kPFull1 || i == kQReady) ? 4u : 1u;
             bar_init(B(i), cnt);
         }
         *abort_flag = 0;
@@ -234,21 +246,26 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         if (a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
     };
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ producer
+    if (warp == 4 || warp == 6) {
+        // ---------------------------------------------- producers: K (warp 4), V (warp 6)
+        // K stage s is free once S of its tile is done, V stage s once PV is,
+        // so K loads run a tile ahead of V loads.
+        const bool is_v = warp == 6;
+        const CUtensorMap* map = is_v ? &tmv : &tmk;
+        const int full0 = is_v ? kVFull0 : kKFull0, empty0 = is_v ? kVEmpty0 : kKEmpty0;
         const int bs = a.block_size;
         const int32_t* table = a.tables + static_cast<size_t>(b) * a.max_blocks;
         const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
         int issued = 0;
         for (int j = 0; j < nt && !*abort_flag; ++j) {
             const int s = j & 1;
-            if (j >= 2 && !bar_wait(B(kKvEmpty0 + s), ((j >> 1) - 1) & 1)) {
+            if (j >= 2 && !bar_wait(B(empty0 + s), ((j >> 1) - 1) & 1)) {
                 if (lane == 0) fail();
                 break;
             }
             const int tok0 = j * kTok, n = min(kTok, t_end - tok0), nblk = (n + bs - 1) / bs;
-            const uint32_t kst = sbase + kKVOff + s * kStageBytes, vst = kst + 2 * kHalfBytes;
-            if (lane == 0) bar_expect_tx(B(kKvFull0 + s), static_cast<uint32_t>(nblk * bs * 128 * 4));
+            const uint32_t dst0 = sbase + kKVOff + s * kStageBytes + (is_v ? 2 * kHalfBytes : 0);
+            if (lane == 0) bar_expect_tx(B(full0 + s), static_cast<uint32_t>(nblk * bs * 128 * 2));
             for (int k = 0; k < nblk; ++k) {
                 const int idx = tok0 / bs + k;
                 int blk = (lane == 0 && idx < a.max_blocks) ? table[idx] : 0;
@@ -258,18 +275,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                 }
                 if (lane == 0) {
                     const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + h) * bs);
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const uint32_t off = hf * kHalfBytes + k * bs * 128;
-                        tma_3d(kst + off, &tmk, 0, y, hf, B(kKvFull0 + s));
-                        tma_3d(vst + off, &tmv, 0, y, hf, B(kKvFull0 + s));
-                    }
+                    for (int hf = 0; hf < 2; ++hf) tma_3d(dst0 + hf * kHalfBytes + k * bs * 128, map, 0, y, hf, B(full0 + s));
                 }
             }
             ++issued;
         }
         // drain: the copies in flight land before the CTA frees anything
         if (lane == 0)
-            for (int j = issued - 1; j >= 0 && j >= issued - 2; --j) (void)bar_wait(B(kKvFull0 + (j & 1)), (j >> 1) & 1);
+            for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
+                if (!bar_wait(B(full0 + (j & 1)), (j >> 1) & 1)) fail();
     } else if (warp == 5) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -279,7 +293,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
             // that buffer, was issued before it, and MMAs run in issue order
             auto issue_s = [&](int j) -> bool {
                 const int s = j & 1;
-                if (!bar_wait(B(kKvFull0 + s), (j >> 1) & 1)) return false;
+                if (!bar_wait(B(kKFull0 + s), (j >> 1) & 1)) return false;
                 fence_after();
                 const uint32_t kst = sbase + kKVOff + s * kStageBytes;
 #pragma unroll
@@ -289,6 +303,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                              sdesc(kst + (ks >> 2) * kHalfBytes + kin, 16), idesc(kTok, 0), ks > 0 ? 1u : 0u);
                 }
                 mma_commit(B(kSFull0 + s));
+                mma_commit(B(kKEmpty0 + s));  // K of this stage no longer needed
                 return true;
             };
             if (ok) ok = issue_s(0);
@@ -297,7 +312,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                     ok = false;
                     break;
                 }
-                if (!bar_wait(B(kPFull), j & 1)) {
+                // one P barrier per score buffer: the signal of tile j + 1 cannot
+                // land on the phase awaited here
+                if (!bar_wait(B(kPFull0 + (j & 1)), (j >> 1) & 1) || !bar_wait(B(kVFull0 + (j & 1)), (j >> 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -308,11 +325,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                     mma_bf16_ta(tmem + kOCol, tmem + s_col(j & 1) + 8 * ks, sdesc(vst + ks * 16 * 128, kHalfBytes),
                                 idesc(kDim, 1), (j > 0 || ks > 0) ? 1u : 0u);
                 mma_commit(B(kPvDone));
-                mma_commit(B(kKvEmpty0 + (j & 1)));
+                mma_commit(B(kVEmpty0 + (j & 1)));
             }
             if (!ok) fail();
             mma_commit(B(kDone));  // completes once every MMA issued above has finished
-            (void)bar_wait(B(kDone), 0);
+            if (!bar_wait(B(kDone), 0)) fail();
         }
         __syncwarp();
     } else {
@@ -353,36 +370,67 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
             const uint32_t sa = tmem + lane_off + s_col(s);
             // the whole warp sees every token of the tile: no causal compares
             const bool full = __all_sync(0xFFFFFFFFu, tok0 + kTok <= lim);
-            // pass 1: the tile's row max over visible tokens (of the raw
-            // scores when the scale is positive, then scaled once)
+            // the row's kTok scores into registers: one round trip to tensor memory
+            uint32_t v[kTok];
+#pragma unroll
+            for (int c4 = 0; c4 < kTok / 32; ++c4) tmem_ld32_nowait(sa + 32 * c4, v + 32 * c4);
+            asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+            // the tile's row max over visible tokens (of the raw scores when
+            // the scale is positive, then scaled once)
             float mx = -INFINITY;
-#pragma unroll 1
-            for (int c4 = 0; c4 < kTok / 32; ++c4) {
-                uint32_t v[32];
-                tmem_ld32(sa + 32 * c4, v);
-                if (full && qk > 0.f) {
-                    float m2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (full && qk > 0.f) {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) m2[i & 3] = fmaxf(m2[i & 3], __uint_as_float(v[i]));
-                    mx = fmaxf(mx, fmaxf(fmaxf(m2[0], m2[1]), fmaxf(m2[2], m2[3])) * qk);
-                } else {
+                for (int i = 0; i < kTok; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(v[i]));
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * qk;
+            } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (tok0 + 32 * c4 + i < lim) mx = fmaxf(mx, __uint_as_float(v[i]) * qk);
-                }
+                for (int i = 0; i < kTok; ++i)
+                    if (tok0 + i < lim) mx = fmaxf(mx, __uint_as_float(v[i]) * qk);
             }
             // lazy base: move it (and rescale O and l) only when the max grew by > 8
             const float m_new = fmaxf(m_used, mx);
             const bool rescale = m_used != -INFINITY && m_new > m_used + 8.f;
             const float base_new = m_used == -INFINITY || rescale ? m_new : m_used;
-            if (__any_sync(0xFFFFFFFFu, rescale)) {  // O is stable once the PV of tile j - 1 has finished
+            const float alpha = rescale ? ex2(m_used - m_new) : 1.f;
+            m_used = base_new;
+            const float base = m_used == -INFINITY ? 0.f : m_used;
+            // probabilities -> P as BF16 pairs over the first kTok/2 columns of
+            // this score buffer (P does not depend on O: this overlaps PV j-1)
+            uint32_t pk[kTok / 2];
+            float l2[2] = {0.f, 0.f};
+            if (full) {
+#pragma unroll
+                for (int i = 0; i < kTok / 2; ++i) {
+                    const float p0 = ex2(fmaf(__uint_as_float(v[2 * i]), qk, -base));
+                    const float p1 = ex2(fmaf(__uint_as_float(v[2 * i + 1]), qk, -base));
+                    l2[i & 1] += p0 + p1;
+                    pk[i] = bf16x2(p0, p1);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kTok / 2; ++i) {
+                    const int t0 = tok0 + 2 * i;
+                    const float p0 = t0 < lim ? ex2(fmaf(__uint_as_float(v[2 * i]), qk, -base)) : 0.f;
+                    const float p1 = t0 + 1 < lim ? ex2(fmaf(__uint_as_float(v[2 * i + 1]), qk, -base)) : 0.f;
+                    l2[i & 1] += p0 + p1;
+                    pk[i] = bf16x2(p0, p1);
+                }
+            }
+            l = l * alpha + (l2[0] + l2[1]);
+            tmem_st32(sa, pk);
+            // Consume every PV phase in order (the PV of tile j - 1 here): a
+            // parity wait is only unambiguous when the barrier is at most one
+            // phase from the one awaited, and PV j cannot finish before this
+            // softmax signals P j.  O is stable from here on until then.
+            if (j > 0) {
                 if (!bar_wait_warp(B(kPvDone), (j - 1) & 1)) {
                     ok = false;
                     break;
                 }
                 fence_after();
-                const float alpha = rescale ? ex2(m_used - m_new) : 1.f;
-                l *= alpha;
+            }
+            if (__any_sync(0xFFFFFFFFu, rescale)) {
 #pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {  // tcgen05.ld/st are warp-wide
                     uint32_t o[32];
@@ -393,41 +441,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                     tmem_st32(oa, o);
                 }
             }
-            m_used = base_new;
-            const float base = m_used == -INFINITY ? 0.f : m_used;
-            // pass 2: probabilities -> P as BF16 pairs over the first kTok/2
-            // columns of this score buffer (only columns already read)
-            uint32_t pk[kTok / 2];
-            float l2[2] = {0.f, 0.f};
-#pragma unroll
-            for (int c4 = 0; c4 < kTok / 32; ++c4) {
-                uint32_t v[32];
-                tmem_ld32(sa + 32 * c4, v);
-                if (full) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(__uint_as_float(v[2 * i]), qk, -base));
-                        const float p1 = ex2(fmaf(__uint_as_float(v[2 * i + 1]), qk, -base));
-                        l2[i & 1] += p0 + p1;
-                        pk[16 * c4 + i] = bf16x2(p0, p1);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int t0 = tok0 + 32 * c4 + 2 * i;
-                        const float p0 = t0 < lim ? ex2(fmaf(__uint_as_float(v[2 * i]), qk, -base)) : 0.f;
-                        const float p1 = t0 + 1 < lim ? ex2(fmaf(__uint_as_float(v[2 * i + 1]), qk, -base)) : 0.f;
-                        l2[i & 1] += p0 + p1;
-                        pk[16 * c4 + i] = bf16x2(p0, p1);
-                    }
-                }
-            }
-            l += l2[0] + l2[1];
-            tmem_st32(sa, pk);
             // V rows past the tile's tokens: zero (stale or unwritten rows could hold NaN)
             const int nvalid = min(kTok, t_end - tok0);
             if (nvalid < kTok) {
-                if (!bar_wait_warp(B(kKvFull0 + s), (j >> 1) & 1)) {  // after the copy into this stage
+                if (!bar_wait_warp(B(kVFull0 + s), (j >> 1) & 1)) {  // after the copy into this stage
                     ok = false;
                     break;
                 }
@@ -441,7 +458,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
             }
             fence_before();
             __syncwarp();
-            if (lane == 0) bar_arrive(B(kPFull));
+            if (lane == 0) bar_arrive(B(kPFull0 + s));
         }
         // epilogue: O / l -> BF16 output rows
         if (ok && bar_wait_warp(B(kPvDone), (nt - 1) & 1)) {
