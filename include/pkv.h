@@ -67,7 +67,7 @@ typedef enum pkv_algo {
     PKV_ALGO_MMA = 2,  /* tensor-core QK^T and PV with warp-level mma (BF16 / FP8 pools) */
     PKV_ALGO_TC = 3    /* multi-query only: tcgen05 MMAs with TMEM accumulators, 128 query
                           rows per CTA (BF16 pools, head_dim 128, fixed splits not used);
-                          AUTO picks it from 64 query rows per KV head */
+                          AUTO picks it from 32 query rows per KV head */
 } pkv_algo;
 
 /*
@@ -196,11 +196,13 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
  *   q    device [num_seqs][C][num_q_heads][head_dim];
  *   out  device [num_seqs][C][num_q_heads][head_dim];
  * other arguments as paged_decode_attention (which is the C = 1 case);
- * 1 <= C <= 2^20.  One launch serves a chunk of consecutive queries: up to
- * 64 query rows per KV head (chunk x num_q_heads / num_kv_heads) for the
- * tensor-core design, a power of two up to 16 (fewer for FP8 and BF16 pools
- * with large groups) for the SIMT design; longer query lists run as several
- * launches on the stream, each reading only the tokens its last query sees.
+ * 1 <= C <= 2^20.  The tcgen05 design (PKV_ALGO_TC) serves every query in
+ * one launch, one CTA per 128 query rows of a KV head.  With the other designs
+ * one launch serves a chunk of consecutive queries: up to 64 query rows per KV
+ * head (chunk x num_q_heads / num_kv_heads) for the warp-level tensor-core
+ * design, a power of two up to 16 (fewer for FP8 and BF16 pools with large
+ * groups) for the SIMT design; longer query lists run as several launches on
+ * the stream, each reading only the tokens its last query sees.
  * Workspace (from paged_multi_query_plan) is shared by those launches in
  * stream order.  A query whose position is negative (seq_lens[b] < C) gets a
  * zero row.

@@ -66,7 +66,7 @@ int row_bound(int rows) {
     return p;
 }
 constexpr int kMaxQueries = 1 << 20;
-constexpr int kTcMinRows = 64;  // query rows per KV head from which AUTO takes the tcgen05 design
+constexpr int kTcMinRows = 32;  // query rows per KV head from which AUTO takes the tcgen05 design
 // Rows of one balanced-schedule partial slot: the template row bound of the
 // largest launch (a KV-head pair's 2 * gh rows for decode).
 int bal_rows(int gh, int C) {

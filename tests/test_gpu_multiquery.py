@@ -105,3 +105,27 @@ def test_multi_query_workload_full_size(name, sample, record_property):
     record_property("max_abs_err", max_abs)
     record_property("max_rel_err", max_rel)
     assert batch.pool.errors() == 0
+
+
+@pytest.mark.parametrize("C", [16, 64])
+def test_tc_back_to_back_launches(C):
+    """Many tcgen05 launches in a row, with nothing between them: no error
+    bits, every call bit-identical to the first and close to the warp-level
+    design (guards the pipeline's barrier protocol)."""
+    w = _w("tc_repeat", 4, 8, "bf16", "bf16", (128, 700, 1500, 4096, 2100, 333, 64 + C, 3000))
+    inst, batch = _filled(w)
+    tables, lens = batch.tables().cuda(), batch.seq_lens().cuda()
+    q = torch.randn(w.num_seqs, C, w.num_q_heads, w.head_dim, generator=torch.Generator().manual_seed(5))
+    q = q.to(torch.bfloat16).cuda()
+    max_len = int(lens.max())
+    first = pk.paged_multi_query_attention(q, batch.pool, 0, tables, lens, max_len, w.scale, algo="tc")
+    outs = [torch.empty_like(first) for _ in range(40)]
+    for o in outs:
+        pk.paged_multi_query_attention(q, batch.pool, 0, tables, lens, max_len, w.scale, out=o, algo="tc")
+    torch.cuda.synchronize()
+    assert batch.pool.errors() == 0
+    for o in outs:
+        assert torch.equal(o, first)
+    ref = pk.paged_multi_query_attention(q, batch.pool, 0, tables, lens, max_len, w.scale, algo="mma")
+    torch.cuda.synchronize()
+    assert (first.float() - ref.float()).abs().max().item() < 2e-2
