@@ -73,6 +73,27 @@ def test_multi_query_parity(G, C, kv, algos, split):
     assert batch.pool.errors() == 0
 
 
+@pytest.mark.parametrize("bs", [32, 64])
+def test_tc_block_sizes(bs):
+    """The tcgen05 design at 32- and 64-token blocks: one TMA box per block
+    half covers 32 or 64 token rows, so a 64-token tile spans 2 or 1 blocks."""
+    G, C = 4, 40
+    lens = (C - 1, C, 31, 33, 63, 64, 65, 129, 700, 1500)
+    w = _w("mq_tc_bs%d" % bs, G, 2, "bf16", "bf16", lens, bs=bs)
+    inst, batch = _filled(w)
+    tables, lens_t = batch.tables(), batch.seq_lens()
+    q = torch.randn(w.num_seqs, C, w.num_q_heads, w.head_dim, generator=torch.Generator().manual_seed(bs))
+    q = q.to(torch.bfloat16)
+    assert pk.multi_query_algo(batch.pool, C, w.num_q_heads) == "tc"
+    ref, _ = oracle_reference_mq(w, inst.k_scale, inst.v_scale, 0, q, tables, lens_t.tolist(), list(range(w.num_seqs)))
+    out = pk.paged_multi_query_attention(q.cuda(), batch.pool, 0, tables.cuda(), lens_t.cuda(),
+                                         int(lens_t.max()), w.scale, algo="tc")
+    torch.cuda.synchronize()
+    compare(out, ref, TOL["bf16"], w.name)
+    assert torch.all(out[0, 0] == 0)
+    assert batch.pool.errors() == 0
+
+
 def test_one_query_equals_decode():
     w = _w("mq_one", 4, 2, "bf16", "bf16", (5, 100, 700))
     inst, batch = _filled(w)
