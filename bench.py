@@ -12,7 +12,7 @@ sequences with lengths U[128, 4096], 32 query / 8 KV heads, head_dim 128,
 flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--algo auto|simt|mma] [--split S] [--impl ours|reference]
+                  [--algo auto|simt|mma|tc] [--split S] [--impl ours|reference]
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload (the only reference this method has).
@@ -220,8 +220,11 @@ def run_ours(args):
     algo = (pk.multi_query_algo(batch.pool, C, w.num_q_heads, split, args.algo) if C > 1
             else pk.decode_algo(batch.pool, w.num_q_heads, args.algo))
     fused = (not args.unfused) and C == 1 and algo == "mma" and w.group <= 8
-    schedule = ("one CTA per 128 query rows" if algo == "tc" else
-                "balanced" if (algo == "mma" and split == 0) else "fixed splits")
+    rows = C * (w.num_q_heads // w.num_kv_heads)  # query rows per KV head
+    # (the tcgen05 design balances tiles only when its grid would leave CTA slots idle)
+    tc_bal = rows <= 128 and w.num_seqs * w.num_kv_heads < 2 * torch.cuda.get_device_properties(dev).multi_processor_count
+    schedule = ("one CTA per 128 query rows" if algo == "tc" and not tc_bal else
+                "balanced" if (algo in ("mma", "tc") and split == 0) else "fixed splits")
     work = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -514,7 +517,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="llama")
-    ap.add_argument("--algo", default="auto", choices=["auto", "simt", "mma"])
+    ap.add_argument("--algo", default="auto", choices=["auto", "simt", "mma", "tc"])
     ap.add_argument("--split", type=int, default=None,
                     help="fixed split size in tokens; 0 = balanced schedule; default: the workload's recipe")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -67,6 +67,17 @@ int row_bound(int rows) {
 }
 constexpr int kMaxQueries = 1 << 20;
 constexpr int kTcMinRows = 32;  // query rows per KV head from which AUTO takes the tcgen05 design
+// Up to this many query rows per KV head (one 128-row tile) the tcgen05
+// design can run the balanced persistent schedule.
+constexpr int kTcBalMaxRows = 128;
+// The tcgen05 design takes the balanced schedule when one CTA per (sequence,
+// KV head) would leave CTA slots idle (a few long sequences).  With enough
+// units the grid keeps every SM busy, and whole units need no Q reload or
+// merge at segment ends, so the grid is as fast or faster.
+bool tc_balanced(int num_seqs, int num_kv_heads, int64_t rows) {
+    return rows <= kTcBalMaxRows && num_seqs <= kMaxBalancedSeqs &&
+           static_cast<int64_t>(num_seqs) * num_kv_heads < bal_ctas();
+}
 // Rows of one balanced-schedule partial slot: the template row bound of the
 // largest launch (a KV-head pair's 2 * gh rows for decode).
 int bal_rows(int gh, int C) {
@@ -306,7 +317,12 @@ pkv_status paged_multi_query_plan(const pkv_pool* p, int32_t num_seqs, int32_t n
     const int cq = mma_chunk(gh, num_queries);
     size_t body = fixed_bytes(num_seqs, cq * num_q_heads, p->d.head_dim, ns);
     if (split_tokens == 0 && num_seqs <= kMaxBalancedSeqs) {
-        const size_t bb = bal_bytes(bal_ctas(), bal_rows(gh, num_queries), p->d.head_dim);
+        size_t bb = bal_bytes(bal_ctas(), bal_rows(gh, num_queries), p->d.head_dim);
+        // the tcgen05 design's balanced schedule: one slot row per query row
+        if (static_cast<int64_t>(num_queries) * gh <= kTcBalMaxRows) {
+            const size_t bt = bal_bytes(bal_ctas(), num_queries * gh, p->d.head_dim);
+            if (bt > bb) bb = bt;
+        }
         if (bb > body) body = bb;
     }
     size_t ws = body > 0 ? counters_bytes(num_seqs, p->d.num_kv_heads) + body : 0;
@@ -404,7 +420,8 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
     pkv_status st =
         paged_multi_query_plan(p, num_seqs, num_queries, num_q_heads, max_seq_len, split_tokens, &S, &NS, &need);
     if (st != PKV_OK) return st;
-    if (!use_tc && need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+    const bool tc_bal = use_tc && split_tokens == 0 && tc_balanced(num_seqs, p->d.num_kv_heads, static_cast<int64_t>(num_queries) * gh);
+    if ((!use_tc || tc_bal) && need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
         return PKV_ERR_WORKSPACE;
 
     DecodeArgs a{};
@@ -445,11 +462,11 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
         uint8_t* w = static_cast<uint8_t*>(workspace);
         a.counters = reinterpret_cast<int32_t*>(w);
         uint8_t* body = w + counters_bytes(num_seqs, p->d.num_kv_heads);
-        if (balanced) {
+        if (balanced || tc_bal) {
             a.bal_max_ctas = bal_ctas();
             a.bal_o = reinterpret_cast<float*>(body);
-            a.bal_lse = reinterpret_cast<float*>(body + bal_o_bytes(a.bal_max_ctas, bal_rows(gh, num_queries),
-                                                                    p->d.head_dim));
+            const int rows = tc_bal ? num_queries * gh : bal_rows(gh, num_queries);
+            a.bal_lse = reinterpret_cast<float*>(body + bal_o_bytes(a.bal_max_ctas, rows, p->d.head_dim));
         } else if (NS > 1) {
             const size_t rows = static_cast<size_t>(num_seqs) * cq_mma * num_q_heads * NS;
             a.o_part = reinterpret_cast<float*>(body);
@@ -464,11 +481,12 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
     const void* tk = pair ? &p->tmap_k2 : &p->tmap_k;
     const void* tv = pair ? &p->tmap_v2 : &p->tmap_v;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (use_tc) {
+    if (use_tc) {  // the balanced schedule (bal_max_ctas > 0) or one CTA per row tile
         a.heads_per_cta = 1;
         a.q_first = 0;
         a.num_queries = num_queries;
         a.len_trim = 0;
+        if (!tc_bal) a.bal_max_ctas = 0;
         return cuda_status(launch_attention_tc(a, &p->tmap_kh, &p->tmap_vh, s));
     }
     // one launch (plus combine) per query chunk; a chunk reads only the tokens

@@ -35,6 +35,8 @@
 // TMEM and skips its output.
 #include <cuda.h>
 
+#include <climits>
+
 #include "device_common.cuh"
 
 namespace pkv {
@@ -51,17 +53,20 @@ constexpr int kQOff = 0;
 constexpr int kKVOff = 2 * kQHalf;
 constexpr int kStageBytes = 4 * kHalfBytes;  // K (16 KB) + V (16 KB)
 constexpr int kBarOff = kKVOff + 2 * kStageBytes;
-constexpr int kBarBytes = 192;
-constexpr int kAlignSlack = 1024;          // room to align the base to 1024 B
-constexpr int kSmem = kBarOff + kBarBytes + kAlignSlack;
+constexpr int kBarBytes = 256;
+constexpr int kRangeOff = kBarOff + kBarBytes;   // per warp: the balanced schedule's {g0, T, P}
+constexpr int kMergeOff = kRangeOff + 7 * 3 * 8;  // [kRows] M and [kRows] 1/z of a merge
+constexpr int kAlignSlack = 1024;               // room to align the base to 1024 B
+constexpr int kSmem = kMergeOff + 2 * kRows * 4 + kAlignSlack;
 static_assert(kSmem <= 115712, "two CTAs per SM");
 constexpr uint32_t kTmemCols = 256;        // per CTA: 2 CTAs per SM
+constexpr int kMC = 4;                     // 4-float chunks per merge round
 constexpr uint32_t kOCol = 2 * kTok;       // score buffers at columns 0 and kTok
 __device__ __forceinline__ uint32_t s_col(int s) { return s ? static_cast<uint32_t>(kTok) : 0u; }
 
 // mbarriers (8 bytes each) after the tiles
 enum Bar { kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1, kSFull0, kSFull1, kPFull0,
-           kPFull1, kPvDone, kQReady, kDone, kNumBars };
+           kPFull1, kPvDone0, kPvDone1, kQReady, kOFree, kGroup, kDone, kNumBars };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -184,6 +189,123 @@ __device__ __forceinline__ uint32_t tile_off(int r, int ch, int half_bytes) {
     return static_cast<uint32_t>((ch >> 3) * half_bytes + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+// 64-token tiles of sequence b (0 past the batch); with one row tile per
+// (sequence, KV head) the last query sees the whole visible length.
+__device__ __forceinline__ int seq_tiles(const DecodeArgs& a, int b) {
+    return b < a.num_seqs ? (visible_len(a, b, false) + kTok - 1) / kTok : 0;
+}
+
+// The tiles a CTA processes, in order.  A unit is the 128-row query tile of
+// one (sequence, KV head) -- for the balanced schedule, the only row tile --
+// and a segment is the run of a unit's tiles one CTA owns.
+//  * grid schedule: one unit per CTA, (row tile, KV head, sequence) =
+//    blockIdx, all of its tiles;
+//  * balanced schedule (query rows <= 128 per KV head): the tiles of all units,
+//    flattened in (sequence, KV head, tile) order, T in total, are cut into P
+//    equal ranges, CTA c taking [c T / P, (c + 1) T / P).  Units cut by a range
+//    boundary are finished by the CTA that publishes its piece last.
+template <bool kBal>
+struct Walk {
+    int b = 0, h = 0, rt_ = 0;      // unit: sequence, KV head, row tile
+    int L = 0, t_end_ = 0, nt = 0;  // visible length, tokens the unit reads, its tiles
+    int t = 0;                      // tile within the unit
+    int k = 0, ntiles = 0;          // tile within the CTA's range, the range's length
+
+    // (balanced schedule: one row tile, whose last query sees the whole length)
+    __device__ int rt() const { return kBal ? 0 : rt_; }
+    __device__ int t_end() const { return kBal ? L : t_end_; }
+
+    __device__ bool more() const { return k < ntiles; }
+    __device__ bool seg_first() const { return k == 0 || t == 0; }
+    __device__ bool seg_last() const { return k == ntiles - 1 || t == nt - 1; }
+    // the unit lies inside the CTA's range / starts at or before it
+    __device__ bool whole() const { return k >= t && k - t + nt <= ntiles; }
+    __device__ bool cta_first() const { return k <= t; }
+
+    // Warp-collective (the balanced schedule sums the lengths with shuffles).
+    // range: where the balanced schedule leaves {g0, T, P} for segment ends.
+    __device__ void init(const DecodeArgs& a, int lane, int gh, long long* range) {
+        if constexpr (!kBal) {
+            rt_ = blockIdx.x;
+            h = blockIdx.y;
+            b = blockIdx.z;
+            L = visible_len(a, b, false);
+            const int nq = a.num_queries * gh;
+            const int last_row = min(nq, (rt_ + 1) * kRows) - 1;
+            t_end_ = L - a.num_queries + last_row / gh + 1;
+            nt = t_end_ > 0 ? (t_end_ + kTok - 1) / kTok : 0;
+            ntiles = nt;
+        } else {
+            const int B = a.num_seqs, Hkv = a.num_kv_heads;
+            long long tot = 0;
+            for (int b0 = 0; b0 < B; b0 += 32) tot += warp_sum_ll(seq_tiles(a, b0 + lane));
+            const long long T = tot * Hkv;
+            const long long P = T < static_cast<long long>(gridDim.x) ? T : static_cast<long long>(gridDim.x);
+            const long long c = blockIdx.x;
+            const long long g0 = c < P ? c * T / P : T, g1 = c < P ? (c + 1) * T / P : T;
+            if (lane == 0) {
+                range[0] = g0;
+                range[1] = T;
+                range[2] = P;
+            }
+            ntiles = static_cast<int>(g1 - g0);  // about T / P: a few thousand at most
+            if (g0 >= g1) return;
+            // locate tile g0: sequence b, with cum = the tiles of the sequences before it
+            long long cum = 0;
+            for (int b0 = 0; b0 < B; b0 += 32) {
+                const long long u = static_cast<long long>(seq_tiles(a, b0 + lane)) * Hkv;
+                long long incl = u;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const long long x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                    if (lane >= o) incl += x;
+                }
+                const long long sum = __shfl_sync(0xFFFFFFFFu, incl, 31);
+                if (g0 < cum + sum) {
+                    const unsigned m = __ballot_sync(0xFFFFFFFFu, cum + incl > g0);
+                    const int l = __ffs(m) - 1;
+                    cum += __shfl_sync(0xFFFFFFFFu, incl - u, l);
+                    b = b0 + l;
+                    break;
+                }
+                cum += sum;
+            }
+            L = visible_len(a, b, false);
+            nt = (L + kTok - 1) / kTok;
+            const long long off = g0 - cum;
+            h = static_cast<int>(off / nt);
+            t = static_cast<int>(off % nt);
+        }
+    }
+    __device__ void next(const DecodeArgs& a) {
+        ++k;
+        if constexpr (kBal) {
+            if (++t < nt) return;
+            t = 0;
+            if (++h < a.num_kv_heads) return;
+            h = 0;
+            for (++b; b < a.num_seqs; ++b) {
+                L = visible_len(a, b, false);
+                if (L > 0) break;
+            }
+            if (b < a.num_seqs) nt = (L + kTok - 1) / kTok;
+        } else {
+            ++t;
+        }
+    }
+};
+
+template <bool kBal>
 __global__ void __launch_bounds__(kThreads, 2)
 attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                     const DecodeArgs a) {
@@ -194,38 +316,42 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     auto B = [&](int i) { return bars + 8u * i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 8 * kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 8 * kNumBars + 4);
-    static_assert(8 * kNumBars + 8 <= kBarBytes, "barrier area");
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 8 * kNumBars + 8);
+    float* merge_m = reinterpret_cast<float*>(smem + kMergeOff);  // [kRows] M, [kRows] 1/z
+    static_assert(8 * kNumBars + 12 <= kBarBytes, "barrier area");
     if (smem - smem_raw > kAlignSlack) {  // the base was not aligned enough for the layout
         if (threadIdx.x == 0 && a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
         return;
     }
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int gh = a.num_q_heads / a.num_kv_heads;
     const int C = a.num_queries, nq = C * gh;
-    const int row0 = rt * kRows;
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
-    // tokens this row tile may see: up to the last query's position
-    const int L = visible_len(a, b, rt == 0 && h == 0 && threadIdx.x == 0);
-    const int last_row = min(nq, row0 + kRows) - 1;
-    const int t_end = L - C + last_row / gh + 1;
-    if (t_end <= 0) {  // every query of the tile sits at a negative position: zero rows
-        for (int i = threadIdx.x; i < kRows * kDim; i += kThreads) {
-            const int n = row0 + i / kDim;
-            if (n >= nq) continue;
-            const size_t orow = (static_cast<size_t>(b) * a.q_total + a.q_first + n / gh) * a.num_q_heads +
-                                static_cast<size_t>(h) * gh + n % gh;
-            static_cast<__nv_bfloat16*>(a.out)[orow * kDim + i % kDim] = __float2bfloat16_rn(0.f);
+    auto out_row = [&](int ob, int oh, int n) -> __nv_bfloat16* {
+        return static_cast<__nv_bfloat16*>(a.out) +
+               ((static_cast<size_t>(ob) * a.q_total + a.q_first + n / gh) * a.num_q_heads +
+                static_cast<size_t>(oh) * gh + n % gh) *
+                   kDim;
+    };
+    if constexpr (!kBal) {
+        // every query of the tile at a negative position: zero rows
+        const int rt = blockIdx.x, h = blockIdx.y, b = blockIdx.z, row0 = rt * kRows;
+        const int L = visible_len(a, b, rt == 0 && h == 0 && threadIdx.x == 0);
+        if (L - C + (min(nq, row0 + kRows) - 1) / gh + 1 <= 0) {
+            for (int i = threadIdx.x; i < kRows * kDim; i += kThreads) {
+                const int n = row0 + i / kDim;
+                if (n < nq) out_row(b, h, n)[i % kDim] = __float2bfloat16_rn(0.f);
+            }
+            return;
         }
-        return;
     }
-    const int nt = (t_end + kTok - 1) / kTok;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
-            const uint32_t cnt = (i == kPFull0 || i == kPFull1 || i == kQReady) ? 4u : 1u;
+            const uint32_t cnt =
+                (i == kPFull0 || i == kPFull1 || i == kQReady || i == kOFree || i == kGroup) ? 4u : 1u;
             bar_init(B(i), cnt);
         }
         *abort_flag = 0;
@@ -245,6 +371,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         *abort_flag = 1;
         if (a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
     };
+    long long* range = reinterpret_cast<long long*>(smem + kRangeOff) + 3 * warp;  // this warp's {g0, T, P}
+    Walk<kBal> w;
+    w.init(a, lane, gh, range);
 
     if (warp == 4 || warp == 6) {
         // ---------------------------------------------- producers: K (warp 4), V (warp 6)
@@ -254,46 +383,52 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         const CUtensorMap* map = is_v ? &tmv : &tmk;
         const int full0 = is_v ? kVFull0 : kKFull0, empty0 = is_v ? kVEmpty0 : kKEmpty0;
         const int bs = a.block_size;
-        const int32_t* table = a.tables + static_cast<size_t>(b) * a.max_blocks;
         const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
-        int issued = 0;
-        for (int j = 0; j < nt && !*abort_flag; ++j) {
-            const int s = j & 1;
-            if (j >= 2 && !bar_wait(B(empty0 + s), ((j >> 1) - 1) & 1)) {
+        int k = 0;  // tiles issued
+        for (; w.more() && !*abort_flag; w.next(a), ++k) {
+            const int s = k & 1;
+            if (k >= 2 && !bar_wait(B(empty0 + s), ((k >> 1) - 1) & 1)) {
                 if (lane == 0) fail();
                 break;
             }
-            const int tok0 = j * kTok, n = min(kTok, t_end - tok0), nblk = (n + bs - 1) / bs;
+            const int32_t* table = a.tables + static_cast<size_t>(w.b) * a.max_blocks;
+            const int tok0 = w.t * kTok, n = min(kTok, w.t_end() - tok0), nblk = (n + bs - 1) / bs;
             const uint32_t dst0 = sbase + kKVOff + s * kStageBytes + (is_v ? 2 * kHalfBytes : 0);
             if (lane == 0) bar_expect_tx(B(full0 + s), static_cast<uint32_t>(nblk * bs * 128 * 2));
-            for (int k = 0; k < nblk; ++k) {
-                const int idx = tok0 / bs + k;
+            for (int kb = 0; kb < nblk; ++kb) {
+                const int idx = tok0 / bs + kb;
                 int blk = (lane == 0 && idx < a.max_blocks) ? table[idx] : 0;
                 if (lane == 0 && static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks)) {
                     if (a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
                     blk = 0;  // read an in-bounds block; the flag marks the output invalid
                 }
                 if (lane == 0) {
-                    const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + h) * bs);
-                    for (int hf = 0; hf < 2; ++hf) tma_3d(dst0 + hf * kHalfBytes + k * bs * 128, map, 0, y, hf, B(full0 + s));
+                    const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + w.h) * bs);
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_3d(dst0 + hf * kHalfBytes + kb * bs * 128, map, 0, y, hf, B(full0 + s));
                 }
             }
-            ++issued;
         }
         // drain: the copies in flight land before the CTA frees anything
         if (lane == 0)
-            for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
+            for (int j = k - 1; j >= 0 && j >= k - 2; --j)
                 if (!bar_wait(B(full0 + (j & 1)), (j >> 1) & 1)) fail();
     } else if (warp == 5) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            bool ok = bar_wait(B(kQReady), 0);
-            fence_after();
-            // S_j goes to buffer j & 1; the PV of tile j - 2, which read P from
-            // that buffer, was issued before it, and MMAs run in issue order
-            auto issue_s = [&](int j) -> bool {
-                const int s = j & 1;
-                if (!bar_wait(B(kKFull0 + s), (j >> 1) & 1)) return false;
+            bool ok = true;
+            // S_k goes to buffer k & 1; the PV of tile k - 2, which read P from
+            // that buffer, was issued before it, and MMAs run in issue order.
+            // The S cursor runs one tile ahead of the PV cursor w.
+            Walk<kBal> ws = w;
+            int seg_s = 0;  // segments whose Q tile the S cursor has waited for
+            auto issue_s = [&](int k) -> bool {
+                const int s = k & 1;
+                if (ws.seg_first()) {  // the softmax warps have stored this unit's Q tile
+                    if (!bar_wait(B(kQReady), seg_s & 1)) return false;
+                    ++seg_s;
+                }
+                if (!bar_wait(B(kKFull0 + s), (k >> 1) & 1)) return false;
                 fence_after();
                 const uint32_t kst = sbase + kKVOff + s * kStageBytes;
 #pragma unroll
@@ -306,26 +441,40 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                 mma_commit(B(kKEmpty0 + s));  // K of this stage no longer needed
                 return true;
             };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; j < nt && ok && !*abort_flag; ++j) {
-                if (j + 1 < nt && !issue_s(j + 1)) {
-                    ok = false;
-                    break;
+            if (ws.more()) {
+                ok = issue_s(0);
+                ws.next(a);
+            }
+            int seg = 0;  // segments whose first PV has been issued
+            for (int k = 0; w.more() && ok && !*abort_flag; w.next(a), ++k) {
+                if (ws.more()) {
+                    if (!issue_s(k + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    ws.next(a);
                 }
-                // one P barrier per score buffer: the signal of tile j + 1 cannot
+                const bool first = w.seg_first();
+                // one P barrier per score buffer: the signal of tile k + 1 cannot
                 // land on the phase awaited here
-                if (!bar_wait(B(kPFull0 + (j & 1)), (j >> 1) & 1) || !bar_wait(B(kVFull0 + (j & 1)), (j >> 1) & 1)) {
+                if (!bar_wait(B(kPFull0 + (k & 1)), (k >> 1) & 1) || !bar_wait(B(kVFull0 + (k & 1)), (k >> 1) & 1)) {
                     ok = false;
                     break;
                 }
+                // a new segment overwrites O: the softmax warps have read out the last one
+                if (first && seg > 0 && !bar_wait(B(kOFree), (seg - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (first) ++seg;
                 fence_after();
-                const uint32_t vst = sbase + kKVOff + (j & 1) * kStageBytes + 2 * kHalfBytes;
+                const uint32_t vst = sbase + kKVOff + (k & 1) * kStageBytes + 2 * kHalfBytes;
 #pragma unroll
                 for (int ks = 0; ks < kTok / 16; ++ks)  // K = tokens in 16-wide steps: 8 TMEM columns of P each
-                    mma_bf16_ta(tmem + kOCol, tmem + s_col(j & 1) + 8 * ks, sdesc(vst + ks * 16 * 128, kHalfBytes),
-                                idesc(kDim, 1), (j > 0 || ks > 0) ? 1u : 0u);
-                mma_commit(B(kPvDone));
-                mma_commit(B(kVEmpty0 + (j & 1)));
+                    mma_bf16_ta(tmem + kOCol, tmem + s_col(k & 1) + 8 * ks, sdesc(vst + ks * 16 * 128, kHalfBytes),
+                                idesc(kDim, 1), (!first || ks > 0) ? 1u : 0u);
+                mma_commit(B(kPvDone0 + (k & 1)));
+                mma_commit(B(kVEmpty0 + (k & 1)));
             }
             if (!ok) fail();
             mma_commit(B(kDone));  // completes once every MMA issued above has finished
@@ -336,101 +485,130 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         // ------------------------------------------------- softmax + epilogue
         const int m = threadIdx.x;  // query row of the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-        const int n = row0 + m;
+        const int n = w.rt() * kRows + m;
         const bool valid = n < nq;
+        const bool busy = w.rt() * kRows + 32 * warp < nq;  // the warp holds at least one query row
         const int qc = valid ? n / gh : 0;
-        // Q row -> shared memory (swizzled K-major layout); padding rows are zero
-        {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const __nv_bfloat16*>(a.q) +
-                ((static_cast<size_t>(b) * a.q_total + a.q_first + qc) * a.num_q_heads + static_cast<size_t>(h) * gh +
-                 (valid ? n % gh : 0)) *
-                    kDim);
-#pragma unroll 4
-            for (int ch = 0; ch < 16; ++ch) {
-                const uint4 v = valid ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(smem + kQOff + tile_off(m, ch, kQHalf)) = v;
-            }
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) bar_arrive(B(kQReady));
-
-        const int lim = valid ? L - C + qc + 1 : 0;  // tokens visible to this row
         const float qk = a.qk_scale_log2;
+        int grp = 0;  // group rendezvous completed
+        // the four softmax warps meet (bounded; memory ordered through the mbarrier)
+        auto group_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) bar_arrive(B(kGroup));
+            const bool r = bar_wait_warp(B(kGroup), grp & 1);
+            ++grp;
+            return r;
+        };
+        // Q rows of a unit -> shared memory (swizzled K-major layout); padding
+        // rows of busy warps are zero, those of idle warps are never read into
+        // an output (each output row depends only on its own S and P rows)
+        auto load_q = [&](int qb, int qh) {
+            if (busy) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(a.q) +
+                    ((static_cast<size_t>(qb) * a.q_total + a.q_first + qc) * a.num_q_heads +
+                     static_cast<size_t>(qh) * gh + (valid ? n % gh : 0)) *
+                        kDim);
+#pragma unroll 4
+                for (int ch = 0; ch < 16; ++ch) {
+                    const uint4 v = valid ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(smem + kQOff + tile_off(m, ch, kQHalf)) = v;
+                }
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) bar_arrive(B(kQReady));
+        };
+        if (w.more()) load_q(w.b, w.h);
+
         float m_used = -INFINITY, l = 0.f;
+        int lim = 0;
         bool ok = true;
-        for (int j = 0; j < nt; ++j) {
-            const int s = j & 1, tok0 = j * kTok;
-            if (!bar_wait_warp(B(kSFull0 + s), (j >> 1) & 1)) {
+        for (int k = 0; w.more(); w.next(a), ++k) {
+            const int s = k & 1, tok0 = w.t * kTok;
+            if (w.seg_first()) {
+                m_used = -INFINITY;
+                l = 0.f;
+                lim = valid ? w.L - C + qc + 1 : INT_MAX;  // tokens visible to this row
+            }
+            if (!bar_wait_warp(B(kSFull0 + s), (k >> 1) & 1)) {
                 ok = false;
                 break;
             }
             fence_after();
             const uint32_t sa = tmem + lane_off + s_col(s);
-            // the whole warp sees every token of the tile: no causal compares
-            const bool full = __all_sync(0xFFFFFFFFu, tok0 + kTok <= lim);
-            // the row's kTok scores into registers: one round trip to tensor memory
-            uint32_t v[kTok];
+            bool rescale = false;
+            float alpha = 1.f;
+            if (busy) {
+                // the whole warp sees every token of the tile: no causal compares
+                const bool full = __all_sync(0xFFFFFFFFu, tok0 + kTok <= lim);
+                // the row's kTok scores into registers: one round trip to tensor memory
+                uint32_t v[kTok];
 #pragma unroll
-            for (int c4 = 0; c4 < kTok / 32; ++c4) tmem_ld32_nowait(sa + 32 * c4, v + 32 * c4);
-            asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-            // the tile's row max over visible tokens (of the raw scores when
-            // the scale is positive, then scaled once)
-            float mx = -INFINITY;
-            if (full && qk > 0.f) {
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                for (int c4 = 0; c4 < kTok / 32; ++c4) tmem_ld32_nowait(sa + 32 * c4, v + 32 * c4);
+                asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+                // the tile's row max over visible tokens (of the raw scores when
+                // the scale is positive, then scaled once)
+                float mx = -INFINITY;
+                if (full && qk > 0.f) {
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int i = 0; i < kTok; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(v[i]));
-                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * qk;
-            } else {
+                    for (int i = 0; i < kTok; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(v[i]));
+                    mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * qk;
+                } else {
 #pragma unroll
-                for (int i = 0; i < kTok; ++i)
-                    if (tok0 + i < lim) mx = fmaxf(mx, __uint_as_float(v[i]) * qk);
-            }
-            // lazy base: move it (and rescale O and l) only when the max grew by > 8
-            const float m_new = fmaxf(m_used, mx);
-            const bool rescale = m_used != -INFINITY && m_new > m_used + 8.f;
-            const float base_new = m_used == -INFINITY || rescale ? m_new : m_used;
-            const float alpha = rescale ? ex2(m_used - m_new) : 1.f;
-            m_used = base_new;
-            const float base = m_used == -INFINITY ? 0.f : m_used;
-            // probabilities -> P as BF16 pairs over the first kTok/2 columns of
-            // this score buffer (P does not depend on O: this overlaps PV j-1)
-            uint32_t pk[kTok / 2];
-            float l2[2] = {0.f, 0.f};
-            if (full) {
-#pragma unroll
-                for (int i = 0; i < kTok / 2; ++i) {
-                    const float p0 = ex2(fmaf(__uint_as_float(v[2 * i]), qk, -base));
-                    const float p1 = ex2(fmaf(__uint_as_float(v[2 * i + 1]), qk, -base));
-                    l2[i & 1] += p0 + p1;
-                    pk[i] = bf16x2(p0, p1);
+                    for (int i = 0; i < kTok; ++i)
+                        if (tok0 + i < lim) mx = fmaxf(mx, __uint_as_float(v[i]) * qk);
                 }
-            } else {
+                // lazy base: move it (and rescale O and l) only when the max grew by > 8
+                const float m_new = fmaxf(m_used, mx);
+                rescale = m_used != -INFINITY && m_new > m_used + 8.f;
+                const float base_new = m_used == -INFINITY || rescale ? m_new : m_used;
+                alpha = rescale ? ex2(m_used - m_new) : 1.f;
+                m_used = base_new;
+                const float base = m_used == -INFINITY ? 0.f : m_used;
+                // probabilities -> P as BF16 pairs over the first kTok/2 columns of
+                // this score buffer (P does not depend on O: this overlaps PV k-1)
+                uint32_t pk[kTok / 2];
+                float lt = 0.f;
+                if (full) {
 #pragma unroll
-                for (int i = 0; i < kTok / 2; ++i) {
-                    const int t0 = tok0 + 2 * i;
-                    const float p0 = t0 < lim ? ex2(fmaf(__uint_as_float(v[2 * i]), qk, -base)) : 0.f;
-                    const float p1 = t0 + 1 < lim ? ex2(fmaf(__uint_as_float(v[2 * i + 1]), qk, -base)) : 0.f;
-                    l2[i & 1] += p0 + p1;
-                    pk[i] = bf16x2(p0, p1);
+                    for (int i = 0; i < kTok / 2; ++i) {
+                        const float p0 = ex2(fmaf(__uint_as_float(v[2 * i]), qk, -base));
+                        const float p1 = ex2(fmaf(__uint_as_float(v[2 * i + 1]), qk, -base));
+                        lt += p0 + p1;
+                        pk[i] = bf16x2(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kTok / 2; ++i) {
+                        const int t0 = tok0 + 2 * i;
+                        const float p0 = t0 < lim ? ex2(fmaf(__uint_as_float(v[2 * i]), qk, -base)) : 0.f;
+                        const float p1 = t0 + 1 < lim ? ex2(fmaf(__uint_as_float(v[2 * i + 1]), qk, -base)) : 0.f;
+                        lt += p0 + p1;
+                        pk[i] = bf16x2(p0, p1);
+                    }
                 }
+                l = l * alpha + lt;
+                tmem_st32(sa, pk);
             }
-            l = l * alpha + (l2[0] + l2[1]);
-            tmem_st32(sa, pk);
-            // Consume every PV phase in order (the PV of tile j - 1 here): a
-            // parity wait is only unambiguous when the barrier is at most one
-            // phase from the one awaited, and PV j cannot finish before this
-            // softmax signals P j.  O is stable from here on until then.
-            if (j > 0) {
-                if (!bar_wait_warp(B(kPvDone), (j - 1) & 1)) {
+            // PV completions, one barrier per tile parity.  A parity wait is only
+            // unambiguous when the barrier is at most one phase from the one
+            // awaited, so every phase is consumed: PV k - 2 here, which has
+            // finished already (S k, just read, was issued after it, and MMAs
+            // complete in order).  PV k cannot finish before this softmax
+            // signals P k.  So only a rescale of O waits for the PV before it.
+            if (k >= 2 && !bar_wait_warp(B(kPvDone0 + s), ((k - 2) >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            const bool any_rescale = busy && __any_sync(0xFFFFFFFFu, rescale);
+            if (any_rescale) {  // O is stable from PV k - 1 until P k is signalled
+                if (!bar_wait_warp(B(kPvDone0 + (s ^ 1)), ((k - 1) >> 1) & 1)) {
                     ok = false;
                     break;
                 }
                 fence_after();
-            }
-            if (__any_sync(0xFFFFFFFFu, rescale)) {
 #pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {  // tcgen05.ld/st are warp-wide
                     uint32_t o[32];
@@ -442,14 +620,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                 }
             }
             // V rows past the tile's tokens: zero (stale or unwritten rows could hold NaN)
-            const int nvalid = min(kTok, t_end - tok0);
+            const int nvalid = min(kTok, w.t_end() - tok0);
             if (nvalid < kTok) {
-                if (!bar_wait_warp(B(kVFull0 + s), (j >> 1) & 1)) {  // after the copy into this stage
+                if (!bar_wait_warp(B(kVFull0 + s), (k >> 1) & 1)) {  // after the copy into this stage
                     ok = false;
                     break;
                 }
                 uint8_t* vs = smem + kKVOff + s * kStageBytes + 2 * kHalfBytes;
-                for (int e = m; e < 2 * (kTok - nvalid) * 8; e += 128) {
+                for (int e = m; e < 2 * (kTok - nvalid) * 8; e += 128) {  // whole 128-byte rows: swizzle irrelevant
                     const int hf = e / ((kTok - nvalid) * 8), rem = e % ((kTok - nvalid) * 8);
                     const int r = nvalid + rem / 8, ch = rem % 8;
                     *reinterpret_cast<uint4*>(vs + hf * kHalfBytes + r * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -459,34 +637,149 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
             fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive(B(kPFull0 + s));
-        }
-        // epilogue: O / l -> BF16 output rows
-        if (ok && bar_wait_warp(B(kPvDone), (nt - 1) & 1)) {
+            if (!w.seg_last()) continue;
+
+            // ---- segment end.  Every S of this segment is done (S k was the
+            // last): the next unit's Q tile may replace this one now, so its
+            // first S overlaps this epilogue.
+            {
+                Walk<kBal> wn = w;
+                wn.next(a);
+                if (wn.more()) load_q(wn.b, wn.h);
+            }
+            if (!bar_wait_warp(B(kPvDone0 + s), (k >> 1) & 1)) {  // PV k
+                ok = false;
+                break;
+            }
             fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16* orow =
-                static_cast<__nv_bfloat16*>(a.out) +
-                ((static_cast<size_t>(b) * a.q_total + a.q_first + qc) * a.num_q_heads + static_cast<size_t>(h) * gh +
-                 (valid ? n % gh : 0)) *
-                    kDim;
+            const float inv = l > 0.f ? a.v_scale / l : 0.f;
+            const bool whole = w.whole();
+            const int slot = w.cta_first() ? 0 : 1;
+            const size_t prow = (static_cast<size_t>(blockIdx.x) * 2 + slot) * nq + (valid ? n : 0);
+            if (busy) {
+                __nv_bfloat16* orow = out_row(w.b, w.h, valid ? n : 0);
 #pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + kOCol + 32 * c4, v);
-                if (valid) {
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_off + kOCol + 32 * c4, v);
+                    if (!valid) continue;
+                    if (whole) {  // O / l -> BF16 output row
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 w;
-                        w.x = bf16x2(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
-                        w.y = bf16x2(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
-                        w.z = bf16x2(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
-                        w.w = bf16x2(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + 32 * c4 + 8 * q4) = w;
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 o;
+                            o.x = bf16x2(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
+                            o.y = bf16x2(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
+                            o.z = bf16x2(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
+                            o.w = bf16x2(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
+                            *reinterpret_cast<uint4*>(orow + 32 * c4 + 8 * q4) = o;
+                        }
+                    } else {  // this CTA's piece: O / l in fp32, and its log-sum-exp
+                        float4* dst = reinterpret_cast<float4*>(a.bal_o + prow * kDim + 32 * c4);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            dst[q4] = make_float4(__uint_as_float(v[4 * q4 + 0]) * inv, __uint_as_float(v[4 * q4 + 1]) * inv,
+                                                  __uint_as_float(v[4 * q4 + 2]) * inv, __uint_as_float(v[4 * q4 + 3]) * inv);
                     }
                 }
             }
-        } else if (lane == 0) {
-            fail();
+            // O is read: the next segment's first PV may overwrite it
+            fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(B(kOFree));
+            if (whole) continue;
+            if constexpr (kBal) {
+                if (valid) a.bal_lse[prow] = l > 0.f ? m_used + log2f(l) : -INFINITY;
+                // Publish: every thread's partial writes are fenced before the
+                // rendezvous, after which one GPU-scope acq_rel atomic counts the
+                // piece (and, for the last one, orders the others' writes before
+                // the reads below).
+                __threadfence();
+                if (!group_sync()) {
+                    ok = false;
+                    break;
+                }
+                // the CTAs c_first .. c_first + pieces - 1 own the unit's tiles
+                // [ps, ps + nt); CTA c owns [c T / P, (c + 1) T / P)
+                const long long T = range[1], P = range[2];
+                const long long ps = range[0] + w.k - w.t;
+                auto owner = [&](long long x) { return ((x + 1) * P - 1) / T; };
+                const long long cf = owner(ps);
+                const int pieces = static_cast<int>(owner(ps + w.nt - 1) - cf + 1);
+                const int s_first = (cf * T / P < ps) ? 1 : 0;
+                int* counter = a.counters + static_cast<size_t>(w.b) * a.num_kv_heads + w.h;
+                if (m == 0) *last_flag = atom_add_acq_rel(counter, 1) == pieces - 1 ? 1 : 0;
+                if (!group_sync()) {
+                    ok = false;
+                    break;
+                }
+                if (!*last_flag) continue;
+                __threadfence();
+                // pass 1: per row, the largest log-sum-exp M and 1/z, z = sum_j 2^(lse_j - M)
+                if (valid) {
+                    float M = -INFINITY, z = 0.f;
+                    for (int j = 0; j < pieces; ++j) {
+                        const float lj =
+                            __ldcg(a.bal_lse + (static_cast<size_t>(cf + j) * 2 + (j == 0 ? s_first : 0)) * nq + n);
+                        if (lj == -INFINITY) continue;  // a piece with no token for this query
+                        const float Mn = fmaxf(M, lj);
+                        z = z * exp2f(M - Mn) + exp2f(lj - Mn);
+                        M = Mn;
+                    }
+                    merge_m[m] = M;
+                    merge_m[kRows + m] = z > 0.f ? 1.f / z : 0.f;
+                }
+                if (!group_sync()) {
+                    ok = false;
+                    break;
+                }
+                // pass 2: thread m owns 4-float chunks m, m + 128, ... of the rows
+                // (32 per row), kMC at a time, with one round of independent loads per piece
+                const int nch = (nq * (kDim / 4) + 127) / 128;
+#pragma unroll 1
+                for (int c0 = 0; c0 < nch; c0 += kMC) {
+                    float4 acc[kMC];
+#pragma unroll
+                    for (int u = 0; u < kMC; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int j = 0; j < pieces; ++j) {
+                        const size_t pb = (static_cast<size_t>(cf + j) * 2 + (j == 0 ? s_first : 0)) * nq;
+#pragma unroll
+                        for (int u = 0; u < kMC; ++u) {
+                            const int idx = m + 128 * (c0 + u), r = idx >> 5, d4 = idx & 31;
+                            if (c0 + u >= nch || r >= nq) continue;
+                            const float lj = __ldcg(a.bal_lse + pb + r);
+                            const float4 o4 = __ldcg(reinterpret_cast<const float4*>(a.bal_o + (pb + r) * kDim) + d4);
+                            const float wt = lj == -INFINITY ? 0.f : exp2f(lj - merge_m[r]) * merge_m[kRows + r];
+                            acc[u].x = fmaf(wt, o4.x, acc[u].x);
+                            acc[u].y = fmaf(wt, o4.y, acc[u].y);
+                            acc[u].z = fmaf(wt, o4.z, acc[u].z);
+                            acc[u].w = fmaf(wt, o4.w, acc[u].w);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kMC; ++u) {
+                        const int idx = m + 128 * (c0 + u), r = idx >> 5, d4 = idx & 31;
+                        if (c0 + u >= nch || r >= nq) continue;
+                        uint2 pk;
+                        pk.x = bf16x2(acc[u].x, acc[u].y);
+                        pk.y = bf16x2(acc[u].z, acc[u].w);
+                        *reinterpret_cast<uint2*>(out_row(w.b, w.h, r) + 4 * d4) = pk;
+                    }
+                }
+                if (m == 0) *counter = 0;  // ready for the next call
+                // merge_m is rewritten only after two more rendezvous
+            }
+        }
+        if (!ok) {
+            if (lane == 0) fail();
+        } else if (kBal && !*abort_flag) {
+            // zero the rows of sequences with nothing visible (and report bad lengths once)
+            const size_t per_seq = static_cast<size_t>(C) * a.num_q_heads * kDim;
+            for (int b = blockIdx.x; b < a.num_seqs; b += gridDim.x) {
+                if (visible_len(a, b, m == 0) != 0) continue;
+                uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                                    (static_cast<size_t>(b) * a.q_total + a.q_first) * a.num_q_heads * kDim);
+                for (size_t i = m; i < per_seq / 8; i += 128) o[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
     }
     // teardown: every role has finished its waits (all bounded); free TMEM
@@ -497,6 +790,27 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
+template <bool kBal>
+cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap* tk, const CUtensorMap* tv, dim3 grid,
+                      cudaStream_t stream) {
+    static int configured_mask = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 31) return cudaErrorNotSupported;
+    if (!(configured_mask & (1 << dev))) {
+        cudaError_t e =
+            cudaFuncSetAttribute(attention_tc_kernel<kBal>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e == cudaSuccess)  // the largest carveout, so that two CTAs fit per SM
+            e = cudaFuncSetAttribute(attention_tc_kernel<kBal>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        configured_mask |= 1 << dev;
+    }
+    // (2 CTAs per SM by shared memory; each allocates half of the tensor memory)
+    attention_tc_kernel<kBal><<<grid, kThreads, kSmem, stream>>>(*tk, *tv, a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool attention_tc_supported(pkv_dtype kv, int head_dim, int block_size) {
@@ -504,24 +818,15 @@ bool attention_tc_supported(pkv_dtype kv, int head_dim, int block_size) {
 }
 
 cudaError_t launch_attention_tc(const DecodeArgs& a, const void* tmap_k, const void* tmap_v, cudaStream_t stream) {
-    static int configured_mask = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 31) return cudaErrorNotSupported;
-    if (!(configured_mask & (1 << dev))) {
-        cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e == cudaSuccess)  // the largest carveout, so that two CTAs fit per SM
-            e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        configured_mask |= 1 << dev;
+    const CUtensorMap* tk = static_cast<const CUtensorMap*>(tmap_k);
+    const CUtensorMap* tv = static_cast<const CUtensorMap*>(tmap_v);
+    if (a.bal_max_ctas > 0) {
+        if (a.num_queries * (a.num_q_heads / a.num_kv_heads) > kRows || !a.bal_o || !a.bal_lse || !a.counters)
+            return cudaErrorInvalidValue;
+        return launch_tc<true>(a, tk, tv, dim3(a.bal_max_ctas), stream);
     }
     const int nq = a.num_queries * (a.num_q_heads / a.num_kv_heads);
-    dim3 grid((nq + kRows - 1) / kRows, a.num_kv_heads, a.num_seqs);
-    // (2 CTAs per SM by shared memory; each allocates half of the tensor memory)
-    attention_tc_kernel<<<grid, kThreads, kSmem, stream>>>(*static_cast<const CUtensorMap*>(tmap_k),
-                                                           *static_cast<const CUtensorMap*>(tmap_v), a);
-    return cudaGetLastError();
+    return launch_tc<false>(a, tk, tv, dim3((nq + kRows - 1) / kRows, a.num_kv_heads, a.num_seqs), stream);
 }
 
 }  // namespace pkv

@@ -106,8 +106,10 @@ def test_one_query_equals_decode():
         assert torch.equal(a[:, 0], b)
 
 
-@pytest.mark.parametrize("name,sample", [("specverify", (0, 1, 17, 33, 63)), ("prefill", (0, 9))])
-def test_multi_query_workload_full_size(name, sample, record_property):
+@pytest.mark.parametrize("name,sample,algo", [("specverify", (0, 1, 17, 33, 63), "auto"),
+                                              ("specverify", (0, 2, 40, 63), "tc"),  # 512 units: a CTA per unit
+                                              ("prefill", (0, 9), "auto")])
+def test_multi_query_workload_full_size(name, sample, algo, record_property):
     """The benchmark's multi-query step at full size (append the last C
     positions, then attend), checked on sampled sequences against the oracle."""
     w = wl.WORKLOADS[name]
@@ -119,13 +121,36 @@ def test_multi_query_workload_full_size(name, sample, record_property):
     tables, lens = batch.tables(), batch.seq_lens()
     assert torch.equal(lens, inst.lens)
     out = pk.paged_multi_query_attention(q.cuda(), batch.pool, 0, tables.cuda(), lens.cuda(), int(lens.max()),
-                                         w.scale)
+                                         w.scale, algo=algo)
     torch.cuda.synchronize()
     ref, _ = oracle_reference_mq(w, inst.k_scale, inst.v_scale, 0, q, tables, lens.tolist(), list(sample))
     max_abs, max_rel = compare(out[list(sample)], ref, TOL[w.kv_dtype], name)
     record_property("max_abs_err", max_abs)
     record_property("max_rel_err", max_rel)
     assert batch.pool.errors() == 0
+
+
+@pytest.mark.parametrize("C,lens", [(8, (20000, 9000, 4097, 0, 5)), (1, (30000, 64, 65)), (32, (12345, 31, 2))])
+def test_tc_balanced_few_long_sequences(C, lens):
+    """A few long sequences: fewer (sequence, KV head) units than CTA slots, so
+    the tcgen05 design shares every unit's tiles among many persistent CTAs and
+    the last CTA to finish a unit merges its pieces (dozens of them here)."""
+    G = 4
+    w = _w("mq_tc_long_c%d" % C, G, 2, "bf16", "bf16", lens, bs=32)
+    inst, batch = _filled(w)
+    tables, lens_t = batch.tables(), batch.seq_lens()
+    q = torch.randn(w.num_seqs, C, w.num_q_heads, w.head_dim, generator=torch.Generator().manual_seed(C + 5))
+    q = q.to(torch.bfloat16)
+    ref, _ = oracle_reference_mq(w, inst.k_scale, inst.v_scale, 0, q, tables, lens_t.tolist(), list(range(w.num_seqs)))
+    _, _, wsb = pk.multi_query_plan(batch.pool, w.num_seqs, C, w.num_q_heads, int(lens_t.max()), 0)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    for rep in range(2):  # the merge counters are back at zero for the second call
+        out = pk.paged_multi_query_attention(q.cuda(), batch.pool, 0, tables.cuda(), lens_t.cuda(),
+                                             int(lens_t.max()), w.scale, algo="tc", workspace=ws)
+        torch.cuda.synchronize()
+        compare(out, ref, TOL["bf16"], "%s rep %d" % (w.name, rep))
+        assert batch.pool.errors() == 0
+    assert torch.count_nonzero(ws[: 4 * w.num_seqs * w.num_kv_heads]) == 0
 
 
 @pytest.mark.parametrize("C", [16, 64])
