@@ -8,7 +8,13 @@
 // kernels": the scores stay on chip.  Query c of the C queries of a sequence
 // sits at position L - C + c of its visible length L and attends causally.
 //
-// One CTA per (128 query rows, KV head, sequence); 6 warps:
+// Two schedules.  Grid: one CTA per (128 query rows, KV head, sequence), all
+// of its tiles.  Balanced (at most 128 query rows per KV head, and fewer
+// (sequence, KV head) units than CTA slots, i.e. a few long sequences): 2
+// persistent CTAs per SM share out the 64-token tiles of all units equally;
+// a CTA reloads Q at each unit it starts, and a unit cut between CTAs is
+// merged from their pieces (O / l and log-sum-exp) by the last to finish.
+// 7 warps:
 //  * warps 4 and 6, TMA producers for K and for V: per 64-token tile, one box
 //    {64 columns, bs rows, 1 half} per KV block and half, so a stage holds each of
 //    K and V as [half: head_dim 0-63 | 64-127][64 token rows][128 B], 128-byte
@@ -18,15 +24,17 @@
 //    then O += P_j V_j (M 128 rows, N 128 head dims, K 64 tokens) into the
 //    TMEM output accumulator.  tcgen05.commit signals mbarriers.
 //  * warps 0-3, softmax and epilogue: thread m owns query row m (TMEM lane m).
-//    It reads its 64 scores with tcgen05.ld (twice: max, then
-//    probabilities), masks causally, and overwrites the score buffer with P
-//    as BF16 pairs, which the PV MMA reads as its A operand from tensor
-//    memory; no shared-memory P, so a softmax never waits for the previous
-//    PV except to rescale O.  The running max is updated lazily: O (in
+//    It reads its 64 scores with tcgen05.ld in one round trip, masks
+//    causally (only on tiles its warp does not fully see), and overwrites
+//    the score buffer with P as BF16 pairs, which the PV MMA reads as its A
+//    operand from tensor memory; no shared-memory P, so a softmax never
+//    waits for the previous PV except to rescale O.  Warps without a query
+//    row only keep pace with the barriers.  The running max is updated lazily: O (in
 //    TMEM) and the running sum are rescaled only when the row max grows by
 //    more than 8 in log2 units, so probabilities stay below 2^8 and fp32 keeps
 //    full precision; the final division by the sum uses the same base.
-//  * Epilogue: O / l, rounded to BF16, written to the output rows.
+//  * Epilogue: O / l, rounded to BF16, written to the output rows (or, for a
+//    piece of a shared unit, to the workspace, then merged).
 // Shared memory: Q 32 KB, 2 stages x (K 16 KB + V 16 KB) for 64-token
 // tiles; TMEM: two 64-column score buffers and a 128-column output
 // accumulator (256 allocated); 2 CTAs per SM, so that two softmax warpgroups
@@ -384,20 +392,29 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         const int full0 = is_v ? kVFull0 : kKFull0, empty0 = is_v ? kVEmpty0 : kKEmpty0;
         const int bs = a.block_size;
         const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
+        // Block-table entries cache_base .. cache_base + 31 of sequence cache_b,
+        // one per lane: one coalesced load per 32 blocks instead of a
+        // dependent load per block ahead of each copy.
+        int cache = 0, cache_base = 0, cache_b = -1;
         int k = 0;  // tiles issued
         for (; w.more() && !*abort_flag; w.next(a), ++k) {
             const int s = k & 1;
+            const int tok0 = w.t * kTok, n = min(kTok, w.t_end() - tok0), nblk = (n + bs - 1) / bs;
+            const int idx0 = tok0 / bs;
+            if (w.b != cache_b || idx0 < cache_base || idx0 + nblk > cache_base + 32) {  // (before the wait)
+                cache_b = w.b;
+                cache_base = idx0;
+                const int idx = idx0 + lane;
+                cache = idx < a.max_blocks ? __ldg(a.tables + static_cast<size_t>(w.b) * a.max_blocks + idx) : 0;
+            }
             if (k >= 2 && !bar_wait(B(empty0 + s), ((k >> 1) - 1) & 1)) {
                 if (lane == 0) fail();
                 break;
             }
-            const int32_t* table = a.tables + static_cast<size_t>(w.b) * a.max_blocks;
-            const int tok0 = w.t * kTok, n = min(kTok, w.t_end() - tok0), nblk = (n + bs - 1) / bs;
             const uint32_t dst0 = sbase + kKVOff + s * kStageBytes + (is_v ? 2 * kHalfBytes : 0);
             if (lane == 0) bar_expect_tx(B(full0 + s), static_cast<uint32_t>(nblk * bs * 128 * 2));
             for (int kb = 0; kb < nblk; ++kb) {
-                const int idx = tok0 / bs + kb;
-                int blk = (lane == 0 && idx < a.max_blocks) ? table[idx] : 0;
+                int blk = __shfl_sync(0xFFFFFFFFu, cache, idx0 + kb - cache_base);
                 if (lane == 0 && static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks)) {
                     if (a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
                     blk = 0;  // read an in-bounds block; the flag marks the output invalid
