@@ -355,9 +355,10 @@ def run_ours(args):
             "peak": tpeak if tensor_bound else peak, "unit": "TFLOP/s" if tensor_bound else "GB/s",
             "frac": round((tflops / tpeak) if tensor_bound else (achieved / peak), 4),
             "traffic": traffic,
-            "kernel": "%s call (decode_%s_kernel%s)" % ("paged_decode_append_attention" if fused else
-                                                        "paged_decode_attention", algo,
-                                                        " + combine" if combine else ""),
+            "kernel": "%s call (%s%s)" % ("paged_decode_append_attention" if fused else
+                                          "paged_multi_query_attention" if C > 1 else "paged_decode_attention",
+                                          "attention_tc_kernel" if algo == "tc" else "decode_%s_kernel" % algo,
+                                          " + combine" if combine else ""),
             "ms_per_launch": round(att_ms, 5), "bytes_per_launch": att_bytes, "flops_per_launch": att_flops,
             "hbm_gbs": round(achieved, 1), "hbm_frac": round(achieved / peak, 4), "tflops": round(tflops, 2),
             "kernel_launches_per_call": chunks * (2 if combine else 1),

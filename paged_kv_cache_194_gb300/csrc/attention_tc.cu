@@ -60,21 +60,41 @@ constexpr int kHalfBytes = kTok * 128;     // one 64-column half of a K or V til
 constexpr int kQOff = 0;
 constexpr int kKVOff = 2 * kQHalf;
 constexpr int kStageBytes = 4 * kHalfBytes;  // K (16 KB) + V (16 KB)
-constexpr int kBarOff = kKVOff + 2 * kStageBytes;
-constexpr int kBarBytes = 256;
-constexpr int kRangeOff = kBarOff + kBarBytes;   // per warp: the balanced schedule's {g0, T, P}
-constexpr int kMergeOff = kRangeOff + 7 * 3 * 8;  // [kRows] M and [kRows] 1/z of a merge
-constexpr int kAlignSlack = 1024;               // room to align the base to 1024 B
-constexpr int kSmem = kMergeOff + 2 * kRows * 4 + kAlignSlack;
-static_assert(kSmem <= 115712, "two CTAs per SM");
-constexpr uint32_t kTmemCols = 256;        // per CTA: 2 CTAs per SM
+constexpr int kAlignSlack = 1024;             // room to align the base to 1024 B
 constexpr int kMC = 4;                     // 4-float chunks per merge round
-constexpr uint32_t kOCol = 2 * kTok;       // score buffers at columns 0 and kTok
-__device__ __forceinline__ uint32_t s_col(int s) { return s ? static_cast<uint32_t>(kTok) : 0u; }
 
-// mbarriers (8 bytes each) after the tiles
-enum Bar { kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1, kSFull0, kSFull1, kPFull0,
-           kPFull1, kPvDone0, kPvDone1, kQReady, kOFree, kGroup, kDone, kNumBars };
+// mbarriers (8 bytes each) after the tiles: these, then the full and empty
+// barriers of the K and V rings
+enum Bar { kQReady, kOFree, kGroup, kDone, kFixedBars };
+
+// One configuration: kNS stages in each of the K and V rings.  Two stages
+// leave room for 2 CTAs per SM, each with 256 TMEM columns: 2 score buffers
+// (kNSB) of 64 columns and the 128-column output accumulator.  With more
+// stages a CTA is alone on its SM and takes all 512 columns, i.e. 4 score
+// buffers, so S can run up to three tiles ahead of the softmax.  That
+// configuration computes the same results but ran slower in every case
+// measured (4 to 1024 query rows per KV head): one CTA's producers and MMA
+// issuer, not the bytes in flight, set the pace, and two CTAs per SM double
+// them.  So the launcher uses two stages.
+template <int kNS>
+struct Cfg {
+    static constexpr int kCtasPerSm = kNS == 2 ? 2 : 1;
+    static constexpr int kNSB = kCtasPerSm == 2 ? 2 : 4;
+    static constexpr uint32_t kTmemCols = kCtasPerSm == 2 ? 256 : 512;
+    static constexpr uint32_t kOCol = kNSB * kTok;
+    // per score buffer: S written, P written, PV that read P done
+    static constexpr int kSFull = kFixedBars, kPFull = kSFull + kNSB, kPvDone = kPFull + kNSB;
+    static constexpr int kKFull = kPvDone + kNSB, kKEmpty = kKFull + kNS;
+    static constexpr int kVFull = kKEmpty + kNS, kVEmpty = kVFull + kNS;
+    static constexpr int kNumBars = kVEmpty + kNS;
+    static_assert(kOCol + kDim <= kTmemCols, "tensor memory");
+    static constexpr int kBarOff = kKVOff + kNS * kStageBytes;
+    static constexpr int kBarBytes = (8 * kNumBars + 12 + 63) / 64 * 64;  // + TMEM address, abort and merge flags
+    static constexpr int kRangeOff = kBarOff + kBarBytes;   // per warp: the balanced schedule's {g0, T, P}
+    static constexpr int kMergeOff = kRangeOff + 7 * 3 * 8;  // [kRows] M and [kRows] 1/z of a merge
+    static constexpr int kSmem = kMergeOff + 2 * kRows * 4 + kAlignSlack;
+    static_assert(kCtasPerSm == 2 ? kSmem <= 115712 : kSmem <= 232448, "shared memory per CTA");
+};
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -98,6 +118,16 @@ __device__ __forceinline__ bool bar_wait(uint32_t b, uint32_t parity) {
         if (ok) return true;
     }
     return false;
+}
+// One look at the barrier, without waiting: has the phase of this parity completed?
+__device__ __forceinline__ bool bar_test(uint32_t b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(b), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 // The same wait by every lane of a warp, with one verdict for all of them
 // (tcgen05.ld/st that follow are warp-wide).
@@ -313,20 +343,20 @@ struct Walk {
     }
 };
 
-template <bool kBal>
-__global__ void __launch_bounds__(kThreads, 2)
+template <bool kBal, int kNS>
+__global__ void __launch_bounds__(kThreads, Cfg<kNS>::kCtasPerSm)
 attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                     const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = su32(smem);
-    const uint32_t bars = sbase + kBarOff;
+    using Lt = Cfg<kNS>;
+    const uint32_t bars = sbase + Lt::kBarOff;
     auto B = [&](int i) { return bars + 8u * i; };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 8 * kNumBars);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 8 * kNumBars + 4);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 8 * kNumBars + 8);
-    float* merge_m = reinterpret_cast<float*>(smem + kMergeOff);  // [kRows] M, [kRows] 1/z
-    static_assert(8 * kNumBars + 12 <= kBarBytes, "barrier area");
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lt::kBarOff + 8 * Lt::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lt::kBarOff + 8 * Lt::kNumBars + 4);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + Lt::kBarOff + 8 * Lt::kNumBars + 8);
+    float* merge_m = reinterpret_cast<float*>(smem + Lt::kMergeOff);  // [kRows] M, [kRows] 1/z
     if (smem - smem_raw > kAlignSlack) {  // the base was not aligned enough for the layout
         if (threadIdx.x == 0 && a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
         return;
@@ -357,9 +387,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     }
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNumBars; ++i) {
+        for (int i = 0; i < Lt::kNumBars; ++i) {
             const uint32_t cnt =
-                (i == kPFull0 || i == kPFull1 || i == kQReady || i == kOFree || i == kGroup) ? 4u : 1u;
+                ((i >= Lt::kPFull && i < Lt::kPFull + Lt::kNSB) || i == kQReady || i == kOFree || i == kGroup) ? 4u
+                                                                                                             : 1u;
             bar_init(B(i), cnt);
         }
         *abort_flag = 0;
@@ -367,7 +398,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(tmem_slot)),
-                     "r"(kTmemCols)
+                     "r"(Lt::kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
@@ -379,7 +410,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         *abort_flag = 1;
         if (a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
     };
-    long long* range = reinterpret_cast<long long*>(smem + kRangeOff) + 3 * warp;  // this warp's {g0, T, P}
+    long long* range = reinterpret_cast<long long*>(smem + Lt::kRangeOff) + 3 * warp;  // this warp's {g0, T, P}
     Walk<kBal> w;
     w.init(a, lane, gh, range);
 
@@ -389,7 +420,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         // so K loads run a tile ahead of V loads.
         const bool is_v = warp == 6;
         const CUtensorMap* map = is_v ? &tmv : &tmk;
-        const int full0 = is_v ? kVFull0 : kKFull0, empty0 = is_v ? kVEmpty0 : kKEmpty0;
+        const int full0 = is_v ? Lt::kVFull : Lt::kKFull, empty0 = is_v ? Lt::kVEmpty : Lt::kKEmpty;
         const int bs = a.block_size;
         const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
         // Block-table entries cache_base .. cache_base + 31 of sequence cache_b,
@@ -398,7 +429,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         int cache = 0, cache_base = 0, cache_b = -1;
         int k = 0;  // tiles issued
         for (; w.more() && !*abort_flag; w.next(a), ++k) {
-            const int s = k & 1;
+            const int s = k % kNS;
             const int tok0 = w.t * kTok, n = min(kTok, w.t_end() - tok0), nblk = (n + bs - 1) / bs;
             const int idx0 = tok0 / bs;
             if (w.b != cache_b || idx0 < cache_base || idx0 + nblk > cache_base + 32) {  // (before the wait)
@@ -407,7 +438,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                 const int idx = idx0 + lane;
                 cache = idx < a.max_blocks ? __ldg(a.tables + static_cast<size_t>(w.b) * a.max_blocks + idx) : 0;
             }
-            if (k >= 2 && !bar_wait(B(empty0 + s), ((k >> 1) - 1) & 1)) {
+            if (k >= kNS && !bar_wait(B(empty0 + s), ((k / kNS) - 1) & 1)) {
                 if (lane == 0) fail();
                 break;
             }
@@ -428,53 +459,61 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         }
         // drain: the copies in flight land before the CTA frees anything
         if (lane == 0)
-            for (int j = k - 1; j >= 0 && j >= k - 2; --j)
-                if (!bar_wait(B(full0 + (j & 1)), (j >> 1) & 1)) fail();
+            for (int j = k - 1; j >= 0 && j >= k - kNS; --j)
+                if (!bar_wait(B(full0 + j % kNS), (j / kNS) & 1)) fail();
     } else if (warp == 5) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             bool ok = true;
-            // S_k goes to buffer k & 1; the PV of tile k - 2, which read P from
-            // that buffer, was issued before it, and MMAs run in issue order.
-            // The S cursor runs one tile ahead of the PV cursor w.
+            constexpr int NSB = Lt::kNSB;
+            // S_j goes to score buffer j % NSB once the PV of tile j - NSB, which
+            // read P from it, has been issued (MMAs run in issue order).  The S
+            // cursor ws runs up to NSB - 1 tiles ahead of the PV cursor w.  The
+            // S of tiles k and k + 1 may block: the softmax of tile k needs only
+            // work issued already (S k, PV k - 1) to signal P k and, at a unit's
+            // end, to store the next unit's Q.  An S further ahead that would
+            // wait (for K, or for a Q the softmax stores only after scores not
+            // yet issued) is left for later, so the PVs the softmax may be
+            // waiting on still get issued.
             Walk<kBal> ws = w;
-            int seg_s = 0;  // segments whose Q tile the S cursor has waited for
-            auto issue_s = [&](int k) -> bool {
-                const int s = k & 1;
-                if (ws.seg_first()) {  // the softmax warps have stored this unit's Q tile
-                    if (!bar_wait(B(kQReady), seg_s & 1)) return false;
-                    ++seg_s;
-                }
-                if (!bar_wait(B(kKFull0 + s), (k >> 1) & 1)) return false;
-                fence_after();
-                const uint32_t kst = sbase + kKVOff + s * kStageBytes;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {  // K = head_dim in 16-wide steps
-                    const uint32_t kin = (ks & 3) * 32;
-                    mma_bf16(tmem + s_col(s), sdesc(sbase + kQOff + (ks >> 2) * kQHalf + kin, 16),
-                             sdesc(kst + (ks >> 2) * kHalfBytes + kin, 16), idesc(kTok, 0), ks > 0 ? 1u : 0u);
-                }
-                mma_commit(B(kSFull0 + s));
-                mma_commit(B(kKEmpty0 + s));  // K of this stage no longer needed
-                return true;
-            };
-            if (ws.more()) {
-                ok = issue_s(0);
-                ws.next(a);
-            }
-            int seg = 0;  // segments whose first PV has been issued
+            int ns = 0;     // S issued
+            int seg_s = 0;  // segments whose Q tile the S cursor has taken
+            int seg = 0;    // segments whose first PV has been issued
             for (int k = 0; w.more() && ok && !*abort_flag; w.next(a), ++k) {
-                if (ws.more()) {
-                    if (!issue_s(k + 1)) {
-                        ok = false;
+                while (ws.more() && ns < k + NSB) {
+                    const bool must = ns <= k + 1;
+                    const int st = ns % kNS;
+                    const bool q_new = ws.seg_first();
+                    if (q_new && !(must ? bar_wait(B(kQReady), seg_s & 1) : bar_test(B(kQReady), seg_s & 1))) {
+                        ok = !must;
                         break;
                     }
+                    if (!(must ? bar_wait(B(Lt::kKFull + st), (ns / kNS) & 1)
+                               : bar_test(B(Lt::kKFull + st), (ns / kNS) & 1))) {
+                        ok = !must;
+                        break;
+                    }
+                    if (q_new) ++seg_s;
+                    fence_after();
+                    const uint32_t kst = sbase + kKVOff + st * kStageBytes;
+                    const uint32_t sb = tmem + static_cast<uint32_t>((ns % NSB) * kTok);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {  // K = head_dim in 16-wide steps
+                        const uint32_t kin = (ks & 3) * 32;
+                        mma_bf16(sb, sdesc(sbase + kQOff + (ks >> 2) * kQHalf + kin, 16),
+                                 sdesc(kst + (ks >> 2) * kHalfBytes + kin, 16), idesc(kTok, 0), ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(B(Lt::kSFull + ns % NSB));
+                    mma_commit(B(Lt::kKEmpty + st));  // K of this stage no longer needed
                     ws.next(a);
+                    ++ns;
                 }
+                if (!ok) break;
                 const bool first = w.seg_first();
-                // one P barrier per score buffer: the signal of tile k + 1 cannot
-                // land on the phase awaited here
-                if (!bar_wait(B(kPFull0 + (k & 1)), (k >> 1) & 1) || !bar_wait(B(kVFull0 + (k & 1)), (k >> 1) & 1)) {
+                // one P barrier per score buffer: the signal of tile k + NSB
+                // cannot land on the phase awaited here
+                if (!bar_wait(B(Lt::kPFull + k % NSB), (k / NSB) & 1) ||
+                    !bar_wait(B(Lt::kVFull + k % kNS), (k / kNS) & 1)) {
                     ok = false;
                     break;
                 }
@@ -485,13 +524,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                 }
                 if (first) ++seg;
                 fence_after();
-                const uint32_t vst = sbase + kKVOff + (k & 1) * kStageBytes + 2 * kHalfBytes;
+                const uint32_t vst = sbase + kKVOff + (k % kNS) * kStageBytes + 2 * kHalfBytes;
+                const uint32_t pb = tmem + static_cast<uint32_t>((k % NSB) * kTok);
 #pragma unroll
                 for (int ks = 0; ks < kTok / 16; ++ks)  // K = tokens in 16-wide steps: 8 TMEM columns of P each
-                    mma_bf16_ta(tmem + kOCol, tmem + s_col(k & 1) + 8 * ks, sdesc(vst + ks * 16 * 128, kHalfBytes),
-                                idesc(kDim, 1), (!first || ks > 0) ? 1u : 0u);
-                mma_commit(B(kPvDone0 + (k & 1)));
-                mma_commit(B(kVEmpty0 + (k & 1)));
+                    mma_bf16_ta(tmem + Lt::kOCol, pb + 8 * ks, sdesc(vst + ks * 16 * 128, kHalfBytes), idesc(kDim, 1),
+                                (!first || ks > 0) ? 1u : 0u);
+                mma_commit(B(Lt::kPvDone + k % NSB));
+                mma_commit(B(Lt::kVEmpty + k % kNS));
             }
             if (!ok) fail();
             mma_commit(B(kDone));  // completes once every MMA issued above has finished
@@ -542,18 +582,18 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         int lim = 0;
         bool ok = true;
         for (int k = 0; w.more(); w.next(a), ++k) {
-            const int s = k & 1, tok0 = w.t * kTok;
+            const int s = k % Lt::kNSB, tok0 = w.t * kTok;  // score buffer
             if (w.seg_first()) {
                 m_used = -INFINITY;
                 l = 0.f;
                 lim = valid ? w.L - C + qc + 1 : INT_MAX;  // tokens visible to this row
             }
-            if (!bar_wait_warp(B(kSFull0 + s), (k >> 1) & 1)) {
+            if (!bar_wait_warp(B(Lt::kSFull + s), (k / Lt::kNSB) & 1)) {
                 ok = false;
                 break;
             }
             fence_after();
-            const uint32_t sa = tmem + lane_off + s_col(s);
+            const uint32_t sa = tmem + lane_off + static_cast<uint32_t>(s * kTok);
             bool rescale = false;
             float alpha = 1.f;
             if (busy) {
@@ -609,19 +649,19 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                 l = l * alpha + lt;
                 tmem_st32(sa, pk);
             }
-            // PV completions, one barrier per tile parity.  A parity wait is only
+            // PV completions, one barrier per score buffer.  A parity wait is only
             // unambiguous when the barrier is at most one phase from the one
-            // awaited, so every phase is consumed: PV k - 2 here, which has
+            // awaited, so every phase is consumed: PV k - NSB here, which has
             // finished already (S k, just read, was issued after it, and MMAs
             // complete in order).  PV k cannot finish before this softmax
             // signals P k.  So only a rescale of O waits for the PV before it.
-            if (k >= 2 && !bar_wait_warp(B(kPvDone0 + s), ((k - 2) >> 1) & 1)) {
+            if (k >= Lt::kNSB && !bar_wait_warp(B(Lt::kPvDone + s), ((k / Lt::kNSB) - 1) & 1)) {
                 ok = false;
                 break;
             }
             const bool any_rescale = busy && __any_sync(0xFFFFFFFFu, rescale);
             if (any_rescale) {  // O is stable from PV k - 1 until P k is signalled
-                if (!bar_wait_warp(B(kPvDone0 + (s ^ 1)), ((k - 1) >> 1) & 1)) {
+                if (!bar_wait_warp(B(Lt::kPvDone + (k - 1) % Lt::kNSB), ((k - 1) / Lt::kNSB) & 1)) {
                     ok = false;
                     break;
                 }
@@ -629,7 +669,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
 #pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {  // tcgen05.ld/st are warp-wide
                     uint32_t o[32];
-                    const uint32_t oa = tmem + lane_off + kOCol + 32 * c4;
+                    const uint32_t oa = tmem + lane_off + Lt::kOCol + 32 * c4;
                     tmem_ld32(oa, o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
@@ -639,11 +679,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
             // V rows past the tile's tokens: zero (stale or unwritten rows could hold NaN)
             const int nvalid = min(kTok, w.t_end() - tok0);
             if (nvalid < kTok) {
-                if (!bar_wait_warp(B(kVFull0 + s), (k >> 1) & 1)) {  // after the copy into this stage
+                if (!bar_wait_warp(B(Lt::kVFull + k % kNS), (k / kNS) & 1)) {  // after the copy into this stage
                     ok = false;
                     break;
                 }
-                uint8_t* vs = smem + kKVOff + s * kStageBytes + 2 * kHalfBytes;
+                uint8_t* vs = smem + kKVOff + (k % kNS) * kStageBytes + 2 * kHalfBytes;
                 for (int e = m; e < 2 * (kTok - nvalid) * 8; e += 128) {  // whole 128-byte rows: swizzle irrelevant
                     const int hf = e / ((kTok - nvalid) * 8), rem = e % ((kTok - nvalid) * 8);
                     const int r = nvalid + rem / 8, ch = rem % 8;
@@ -653,7 +693,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
             }
             fence_before();
             __syncwarp();
-            if (lane == 0) bar_arrive(B(kPFull0 + s));
+            if (lane == 0) bar_arrive(B(Lt::kPFull + s));
             if (!w.seg_last()) continue;
 
             // ---- segment end.  Every S of this segment is done (S k was the
@@ -664,7 +704,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                 wn.next(a);
                 if (wn.more()) load_q(wn.b, wn.h);
             }
-            if (!bar_wait_warp(B(kPvDone0 + s), (k >> 1) & 1)) {  // PV k
+            if (!bar_wait_warp(B(Lt::kPvDone + s), (k / Lt::kNSB) & 1)) {  // PV k
                 ok = false;
                 break;
             }
@@ -678,7 +718,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
 #pragma unroll 1
                 for (int c4 = 0; c4 < 4; ++c4) {
                     uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + kOCol + 32 * c4, v);
+                    tmem_ld32(tmem + lane_off + Lt::kOCol + 32 * c4, v);
                     if (!valid) continue;
                     if (whole) {  // O / l -> BF16 output row
 #pragma unroll
@@ -804,27 +844,29 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     __syncthreads();
     fence_after();
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(Lt::kTmemCols)
+                     : "memory");
 }
 
-template <bool kBal>
+template <bool kBal, int kNS>
 cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap* tk, const CUtensorMap* tv, dim3 grid,
                       cudaStream_t stream) {
+    constexpr int kSmem = Cfg<kNS>::kSmem;
     static int configured_mask = 0;
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 31) return cudaErrorNotSupported;
     if (!(configured_mask & (1 << dev))) {
         cudaError_t e =
-            cudaFuncSetAttribute(attention_tc_kernel<kBal>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+            cudaFuncSetAttribute(attention_tc_kernel<kBal, kNS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e == cudaSuccess)  // the largest carveout, so that two CTAs fit per SM
-            e = cudaFuncSetAttribute(attention_tc_kernel<kBal>, cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(attention_tc_kernel<kBal, kNS>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         configured_mask |= 1 << dev;
     }
-    // (2 CTAs per SM by shared memory; each allocates half of the tensor memory)
-    attention_tc_kernel<kBal><<<grid, kThreads, kSmem, stream>>>(*tk, *tv, a);
+    // (Cfg<kNS>::kCtasPerSm CTAs per SM by shared memory; each allocates 256 TMEM columns)
+    attention_tc_kernel<kBal, kNS><<<grid, kThreads, kSmem, stream>>>(*tk, *tv, a);
     return cudaGetLastError();
 }
 
@@ -837,13 +879,12 @@ bool attention_tc_supported(pkv_dtype kv, int head_dim, int block_size) {
 cudaError_t launch_attention_tc(const DecodeArgs& a, const void* tmap_k, const void* tmap_v, cudaStream_t stream) {
     const CUtensorMap* tk = static_cast<const CUtensorMap*>(tmap_k);
     const CUtensorMap* tv = static_cast<const CUtensorMap*>(tmap_v);
-    if (a.bal_max_ctas > 0) {
-        if (a.num_queries * (a.num_q_heads / a.num_kv_heads) > kRows || !a.bal_o || !a.bal_lse || !a.counters)
-            return cudaErrorInvalidValue;
-        return launch_tc<true>(a, tk, tv, dim3(a.bal_max_ctas), stream);
-    }
     const int nq = a.num_queries * (a.num_q_heads / a.num_kv_heads);
-    return launch_tc<false>(a, tk, tv, dim3((nq + kRows - 1) / kRows, a.num_kv_heads, a.num_seqs), stream);
+    if (a.bal_max_ctas > 0) {
+        if (nq > kRows || !a.bal_o || !a.bal_lse || !a.counters) return cudaErrorInvalidValue;
+        return launch_tc<true, 2>(a, tk, tv, dim3(a.bal_max_ctas), stream);
+    }
+    return launch_tc<false, 2>(a, tk, tv, dim3((nq + kRows - 1) / kRows, a.num_kv_heads, a.num_seqs), stream);
 }
 
 }  // namespace pkv
