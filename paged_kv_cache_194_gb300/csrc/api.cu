@@ -407,10 +407,7 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PKV_ERR_INVALID_ARG;
     const int gh = num_q_heads / p->d.num_kv_heads;  // query heads per KV head
-    const int cq_mma = mma_chunk(gh, num_queries), cq_simt = simt_chunk(p, gh, num_queries);
-
-    (void)cq_mma;
-    (void)cq_simt;
+    const int cq_mma = mma_chunk(gh, num_queries);  // the largest chunk: sizes the fixed-split partials
     const int design = design_for(p, num_queries, gh, split_tokens, algo, new_k != nullptr);
     if (design < 0) return PKV_ERR_UNSUPPORTED;
     const bool use_tc = design == PKV_ALGO_TC, use_mma = design == PKV_ALGO_MMA;

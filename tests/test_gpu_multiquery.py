@@ -153,6 +153,22 @@ def test_tc_balanced_few_long_sequences(C, lens):
     assert torch.count_nonzero(ws[: 4 * w.num_seqs * w.num_kv_heads]) == 0
 
 
+@pytest.mark.parametrize("algo", ["tc", "mma"])
+def test_all_sequences_empty(algo):
+    """No sequence has a visible token: no tiles at all, every output row is zero."""
+    w = _w("mq_empty_%s" % algo, 4, 2, "bf16", "bf16", (0, 0, 0), bs=32)
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    tables, lens_t = batch.tables(), batch.seq_lens()
+    q = torch.randn(w.num_seqs, 8, w.num_q_heads, w.head_dim, generator=torch.Generator().manual_seed(9))
+    out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    pk.paged_multi_query_attention(q.to(torch.bfloat16).cuda(), batch.pool, 0, tables.cuda(), lens_t.cuda(), 0,
+                                   w.scale, out=out, algo=algo)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+    assert batch.pool.errors() == 0
+
+
 @pytest.mark.parametrize("C", [16, 64])
 def test_tc_back_to_back_launches(C):
     """Many tcgen05 launches in a row, with nothing between them: no error
