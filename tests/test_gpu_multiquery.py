@@ -156,10 +156,11 @@ def test_tc_balanced_few_long_sequences(C, lens):
 @pytest.mark.parametrize("algo", ["tc", "mma"])
 def test_all_sequences_empty(algo):
     """No sequence has a visible token: no tiles at all, every output row is zero."""
-    w = _w("mq_empty_%s" % algo, 4, 2, "bf16", "bf16", (0, 0, 0), bs=32)
+    w = _w("mq_empty_%s" % algo, 4, 2, "bf16", "bf16", (40, 7, 100), bs=32)  # (a pool needs blocks)
     inst = wl.instance(w)
     batch = DecodeBatch(inst)
-    tables, lens_t = batch.tables(), batch.seq_lens()
+    tables = batch.tables()
+    lens_t = torch.zeros(w.num_seqs, dtype=torch.int32)
     q = torch.randn(w.num_seqs, 8, w.num_q_heads, w.head_dim, generator=torch.Generator().manual_seed(9))
     out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
     pk.paged_multi_query_attention(q.to(torch.bfloat16).cuda(), batch.pool, 0, tables.cuda(), lens_t.cuda(), 0,
