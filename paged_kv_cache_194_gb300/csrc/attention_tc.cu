@@ -62,6 +62,7 @@ constexpr int kKVOff = 2 * kQHalf;
 constexpr int kStageBytes = 4 * kHalfBytes;  // K (16 KB) + V (16 KB)
 constexpr int kAlignSlack = 1024;             // room to align the base to 1024 B
 constexpr int kMC = 4;                     // 4-float chunks per merge round
+constexpr int kRankMaxSeqs = 128;          // the grid schedule orders units by length up to this many sequences
 
 // mbarriers (8 bytes each) after the tiles: these, then the full and empty
 // barriers of the K and V rings
@@ -271,12 +272,13 @@ struct Walk {
     __device__ bool cta_first() const { return k <= t; }
 
     // Warp-collective (the balanced schedule sums the lengths with shuffles).
-    // range: where the balanced schedule leaves {g0, T, P} for segment ends.
-    __device__ void init(const DecodeArgs& a, int lane, int gh, long long* range) {
+    // range: where the balanced schedule leaves {g0, T, P} for segment ends;
+    // (ub, uh, urt): the grid schedule's unit.
+    __device__ void init(const DecodeArgs& a, int lane, int gh, long long* range, int ub, int uh, int urt) {
         if constexpr (!kBal) {
-            rt_ = blockIdx.x;
-            h = blockIdx.y;
-            b = blockIdx.z;
+            rt_ = urt;
+            h = uh;
+            b = ub;
             L = visible_len(a, b, false);
             const int nq = a.num_queries * gh;
             const int last_row = min(nq, (rt_ + 1) * kRows) - 1;
@@ -373,9 +375,36 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                 static_cast<size_t>(oh) * gh + n % gh) *
                    kDim;
     };
+    // Grid schedule: blocks start in linear order, so hand out the longest
+    // units first (sequences by visible length, longest first; within one,
+    // the later row tiles, which see more tokens, first): the last wave is
+    // then made of short units.  For batches of up to kRankMaxSeqs sequences;
+    // beyond that, blockIdx order.
+    int ub = blockIdx.z, uh = blockIdx.y, urt = blockIdx.x;
+    if constexpr (!kBal) {
+        if (a.num_seqs <= kRankMaxSeqs) {
+            const int R = gridDim.x, Hkv = gridDim.y;
+            const int i = blockIdx.x + R * (blockIdx.y + Hkv * blockIdx.z);
+            const int rank = i / (R * Hkv), rem = i % (R * Hkv);
+            urt = R - 1 - rem / Hkv;
+            uh = rem % Hkv;
+            int* pick = reinterpret_cast<int*>(merge_m);
+            for (int c = threadIdx.x; c < a.num_seqs; c += kThreads) {  // the rank of sequence c
+                const int Lc = visible_len(a, c, false);
+                int r = 0;
+                for (int o = 0; o < a.num_seqs; ++o) {
+                    const int Lo = visible_len(a, o, false);
+                    r += (Lo > Lc || (Lo == Lc && o < c)) ? 1 : 0;
+                }
+                if (r == rank) *pick = c;
+            }
+            __syncthreads();
+            ub = *pick;
+        }
+    }
     if constexpr (!kBal) {
         // every query of the tile at a negative position: zero rows
-        const int rt = blockIdx.x, h = blockIdx.y, b = blockIdx.z, row0 = rt * kRows;
+        const int rt = urt, h = uh, b = ub, row0 = rt * kRows;
         const int L = visible_len(a, b, rt == 0 && h == 0 && threadIdx.x == 0);
         if (L - C + (min(nq, row0 + kRows) - 1) / gh + 1 <= 0) {
             for (int i = threadIdx.x; i < kRows * kDim; i += kThreads) {
@@ -412,7 +441,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     };
     long long* range = reinterpret_cast<long long*>(smem + Lt::kRangeOff) + 3 * warp;  // this warp's {g0, T, P}
     Walk<kBal> w;
-    w.init(a, lane, gh, range);
+    w.init(a, lane, gh, range, ub, uh, urt);
 
     if (warp == 4 || warp == 6) {
         // ---------------------------------------------- producers: K (warp 4), V (warp 6)
