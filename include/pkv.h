@@ -67,7 +67,7 @@ typedef enum pkv_algo {
     PKV_ALGO_MMA = 2,  /* tensor-core QK^T and PV with warp-level mma (BF16 / FP8 pools) */
     PKV_ALGO_TC = 3    /* multi-query only: tcgen05 MMAs with TMEM accumulators, 128 query
                           rows per CTA (BF16 pools, head_dim 128, fixed splits not used);
-                          AUTO picks it from 32 query rows per KV head */
+                          AUTO picks it from 8 query rows per KV head (2 or more queries) */
 } pkv_algo;
 
 /*

@@ -66,7 +66,7 @@ int row_bound(int rows) {
     return p;
 }
 constexpr int kMaxQueries = 1 << 20;
-constexpr int kTcMinRows = 32;  // query rows per KV head from which AUTO takes the tcgen05 design
+constexpr int kTcMinRows = 8;  // query rows per KV head from which AUTO takes the tcgen05 design
 // Up to this many query rows per KV head (one 128-row tile) the tcgen05
 // design can run the balanced persistent schedule.
 constexpr int kTcBalMaxRows = 128;
