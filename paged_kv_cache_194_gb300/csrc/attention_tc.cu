@@ -383,11 +383,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     int ub = blockIdx.z, uh = blockIdx.y, urt = blockIdx.x;
     if constexpr (!kBal) {
         if (a.num_seqs <= kRankMaxSeqs) {
-            const int R = gridDim.x, Hkv = gridDim.y;
-            const int i = blockIdx.x + R * (blockIdx.y + Hkv * blockIdx.z);
-            const int rank = i / (R * Hkv), rem = i % (R * Hkv);
-            urt = R - 1 - rem / Hkv;
-            uh = rem % Hkv;
+            const long long R = gridDim.x, Hkv = gridDim.y, per_seq = R * Hkv;
+            const long long i = blockIdx.x + R * (blockIdx.y + Hkv * static_cast<long long>(blockIdx.z));
+            const int rank = static_cast<int>(i / per_seq);  // < num_seqs: each rank is one sequence's
+            const long long rem = i % per_seq;
+            urt = static_cast<int>(R - 1 - rem / Hkv);
+            uh = static_cast<int>(rem % Hkv);
             int* pick = reinterpret_cast<int*>(merge_m);
             for (int c = threadIdx.x; c < a.num_seqs; c += kThreads) {  // the rank of sequence c
                 const int Lc = visible_len(a, c, false);
