@@ -153,6 +153,25 @@ def test_tc_balanced_few_long_sequences(C, lens):
     assert torch.count_nonzero(ws[: 4 * w.num_seqs * w.num_kv_heads]) == 0
 
 
+def test_tc_grid_many_sequences():
+    """More sequences than the grid schedule ranks by length (128) and more
+    (sequence, KV head) units than CTA slots: one CTA per unit in blockIdx
+    order, every element checked."""
+    G, C, B = 4, 8, 160
+    lens = tuple(1 + (37 * b) % 600 for b in range(B))
+    w = _w("mq_tc_many", G, 2, "bf16", "bf16", lens, bs=16)
+    inst, batch = _filled(w)
+    tables, lens_t = batch.tables(), batch.seq_lens()
+    q = torch.randn(w.num_seqs, C, w.num_q_heads, w.head_dim, generator=torch.Generator().manual_seed(11))
+    q = q.to(torch.bfloat16)
+    ref, _ = oracle_reference_mq(w, inst.k_scale, inst.v_scale, 0, q, tables, lens_t.tolist(), list(range(w.num_seqs)))
+    out = pk.paged_multi_query_attention(q.cuda(), batch.pool, 0, tables.cuda(), lens_t.cuda(),
+                                         int(lens_t.max()), w.scale, algo="tc")
+    torch.cuda.synchronize()
+    compare(out, ref, TOL["bf16"], w.name)
+    assert batch.pool.errors() == 0
+
+
 @pytest.mark.parametrize("algo", ["tc", "mma"])
 def test_all_sequences_empty(algo):
     """No sequence has a visible token: no tiles at all, every output row is zero."""
