@@ -316,6 +316,32 @@ def test_multi_query_matches_causal_bruteforce(C, G):
                 assert abs(lse[b, c, hq] - float(torch.logsumexp(s, 0))) < 1e-12
 
 
+def test_multi_query_negative_positions_give_zero_rows():
+    """A sequence shorter than C: queries whose position L - C + c is negative
+    see no token (a zero row, log-sum-exp -inf); the others see tokens 0 .. L - C + c."""
+    C, G = 6, 2
+    w = _small("mq_short", G=G, Hkv=2, kv="bf16", lens=(1, 2, 5, 6))
+    inst = wl.instance(w)
+    pool, rows = _fill_oracle(inst)
+    q = torch.randn(w.num_seqs, C, w.num_q_heads, w.head_dim,
+                    generator=torch.Generator().manual_seed(12)).to(torch.bfloat16)
+    out, lse = oracle.paged_attention_mq(q, "bf16", pool, 0, inst.tables, inst.lens, w.scale)
+    sc = float(np.float32(w.scale))
+    for b in range(w.num_seqs):
+        L = int(inst.lens[b])
+        for c in range(C):
+            qpos = L - C + c
+            for hq in range(w.num_q_heads):
+                if qpos < 0:
+                    assert np.all(out[b, c, hq] == 0) and lse[b, c, hq] == -math.inf
+                    continue
+                h = hq // G
+                K = rows[b][0].to(torch.float64)[: qpos + 1, h, :]
+                V = rows[b][1].to(torch.float64)[: qpos + 1, h, :]
+                s = (K @ q[b, c, hq].to(torch.float64)) * sc
+                np.testing.assert_allclose(out[b, c, hq], (torch.softmax(s, 0) @ V).numpy(), rtol=1e-12, atol=1e-12)
+
+
 def test_multi_query_rows_equal_decode_on_prefixes():
     """Query c is exactly decode attention over the first L - C + c + 1 tokens,
     and C = 1 is plain decode."""
