@@ -197,10 +197,12 @@ pkv_status paged_decode_attention(const void* q, pkv_dtype q_dtype, const pkv_po
  *   out  device [num_seqs][C][num_q_heads][head_dim];
  * other arguments as paged_decode_attention (which is the C = 1 case);
  * 1 <= C <= 2^20.  The tcgen05 design (PKV_ALGO_TC) serves every query in
- * one launch: up to 128 query rows per KV head with the balanced schedule
- * (persistent CTAs share out the 64-token tiles of all (sequence, KV head)
- * pairs equally and merge the pairs they split; needs the workspace), beyond
- * that one CTA per 128 query rows of a KV head.  With the other designs
+ * one launch.  Normally that is one CTA per 128 query rows of a (sequence,
+ * KV head), the longest sequences' CTAs first.  With at most 128 query rows
+ * per KV head and fewer (sequence, KV head) pairs than CTA slots (a few long
+ * sequences) it uses the balanced schedule instead: persistent CTAs share out
+ * the 64-token tiles of all pairs equally and merge the pairs they split,
+ * which needs the workspace.  With the other designs
  * one launch serves a chunk of consecutive queries: up to 64 query rows per KV
  * head (chunk x num_q_heads / num_kv_heads) for the warp-level tensor-core
  * design, a power of two up to 16 (fewer for FP8 and BF16 pools with large
