@@ -269,9 +269,14 @@ pkv_status paged_decode_append_attention(const void* q, pkv_dtype q_dtype, const
  * on a device looks up the array's device address with that device current;
  * make that first call before any stream capture.  A call whose plan needs
  * more than PKV_STATIC_SCRATCH_BYTES (see paged_decode_plan) returns
- * PKV_ERR_WORKSPACE before enqueuing anything.  All calls share the one
- * array: calls that overlap on the GPU race and must be ordered by the
- * caller.  No contents need clearing between calls.
+ * PKV_ERR_WORKSPACE, and a call any other check rejects returns its status,
+ * before enqueuing anything.  All calls share the one array, which keeps what
+ * the previous call left: calls that overlap on the GPU race and must be
+ * ordered by the caller.  Each call that uses the array first clears its own
+ * per-(sequence, KV head) counters there, in stream order (a memset on
+ * `stream` of 4 * num_seqs * num_kv_heads bytes rounded up to 256), so calls
+ * of different shapes, and a call after one that reported
+ * PKV_ERRBIT_TIMEOUT, need no clearing by the caller.
  */
 #define PKV_STATIC_SCRATCH_BYTES (16 * 1024 * 1024)
 pkv_status paged_decode_attention_static_ws(const void* q, pkv_dtype q_dtype, const pkv_pool* pool,
@@ -343,6 +348,28 @@ int32_t kv_bm_free_list(const pkv_block_manager* bm, int32_t* out, int32_t cap);
 int32_t kv_bm_block_ref(const pkv_block_manager* bm, int32_t block);
 /* Verify every invariant; PKV_ERR_INCONSISTENT if one fails. */
 pkv_status kv_bm_check(const pkv_block_manager* bm);
+
+/*
+ * Test hook for the failure path of the bounded pipeline waits.  The pages
+ * name no interface for it; "TensorRT-LLM, in depth", section "In-flight
+ * batching and the scheduler", has a request that cannot go on paused rather
+ * than failed, and its "Failure modes" heading lists failure handling.  Every
+ * wait of the tensor-core decode design (PKV_ALGO_MMA: decode, fused decode,
+ * multi-query) is bounded; an expired one sets PKV_ERRBIT_TIMEOUT, stops the
+ * CTA's pipeline, waits with the full bound for the copies the CTA has in
+ * flight, skips the CTA's output and returns.  This makes such an expiry
+ * happen on demand, without a fault or a hang:
+ *   polls >= 0  later launches of that design made from the calling host
+ *               thread give up the consumer warps' first wait for a loaded
+ *               stage after `polls` polls (0: without looking), in the CTA
+ *               whose linear block index is `cta` (every CTA when cta < 0);
+ *   polls < 0   normal bounds again (the default).
+ * Only that first wait is shortened; the waits that guard copies in flight
+ * keep their bound.  After a call that reported PKV_ERRBIT_TIMEOUT, the
+ * workspace's counters may be non-zero (clear them before reusing it), and
+ * the output rows of the units the stopped CTAs took part in are unwritten.
+ */
+void pkv_set_first_wait_limit_for_testing(int32_t polls, int32_t cta);
 
 /* Human-readable name of a status. */
 const char* pkv_status_string(pkv_status status);

@@ -27,7 +27,8 @@ EXPORTS = ("kv_pool_create", "kv_pool_destroy", "kv_pool_tensor_bytes", "kv_byte
            "kv_append", "paged_decode_plan", "paged_decode_algo", "paged_decode_attention",
            "paged_multi_query_plan", "paged_multi_query_algo", "paged_multi_query_attention",
            "paged_decode_append_attention",
-           "paged_decode_attention_static_ws", "pkv_status_string", "pkv_last_cuda_error",
+           "paged_decode_attention_static_ws", "pkv_set_first_wait_limit_for_testing", "pkv_status_string",
+           "pkv_last_cuda_error",
            "kv_block_manager_create", "kv_block_manager_destroy", "kv_bm_num_free", "kv_bm_add_sequence",
            "kv_bm_free_sequence", "kv_bm_grow", "kv_bm_decode_slots", "kv_bm_match_prefix", "kv_bm_seq_len",
            "kv_bm_block_tables", "kv_bm_free_list", "kv_bm_block_ref", "kv_bm_check")
@@ -100,6 +101,8 @@ def lib() -> ctypes.CDLL:
                                                    c.c_int32, c.c_int32, c.c_float, c.c_int32, c.c_int, P, P]
     L.paged_decode_algo.restype = c.c_int32
     L.paged_decode_algo.argtypes = [P, c.c_int32, c.c_int]
+    L.pkv_set_first_wait_limit_for_testing.restype = None
+    L.pkv_set_first_wait_limit_for_testing.argtypes = [c.c_int32, c.c_int32]
     L.pkv_status_string.restype = c.c_char_p
     L.pkv_status_string.argtypes = [c.c_int]
     L.pkv_last_cuda_error.restype = c.c_char_p
@@ -299,6 +302,13 @@ def paged_decode_attention_static_ws(q: torch.Tensor, pool: KVPool, layer: int, 
         split_tokens, ALGOS[algo], _dev(out, "out", q.dtype), _stream_ptr(stream))
     _check(rc, "paged_decode_attention_static_ws")
     return out
+
+
+def set_first_wait_limit_for_testing(polls: int, cta: int = -1) -> None:
+    """Make the tensor-core decode design's first stage wait give up after
+    `polls` polls in CTA `cta` (every CTA when negative) for later calls from
+    this thread; polls < 0 restores the normal bound (test hook)."""
+    lib().pkv_set_first_wait_limit_for_testing(int(polls), int(cta))
 
 
 def multi_query_plan(pool: KVPool, num_seqs: int, num_queries: int, num_q_heads: int, max_seq_len: int,

@@ -12,6 +12,9 @@ namespace pkv {
 
 namespace {
 thread_local char g_last_cuda_error[256] = "";
+// pkv_set_first_wait_limit_for_testing: polls (< 0: off) and the CTA it targets
+thread_local int32_t g_test_wait_polls = -1;
+thread_local int32_t g_test_wait_cta = -1;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -198,6 +201,8 @@ int dtype_bytes(pkv_dtype t) {
     return 0;
 }
 
+size_t workspace_counter_bytes(int num_seqs, int num_kv_heads) { return counters_bytes(num_seqs, num_kv_heads); }
+
 int num_sms() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
@@ -229,6 +234,11 @@ const char* pkv_status_string(pkv_status s) {
 }
 
 const char* pkv_last_cuda_error(void) { return g_last_cuda_error; }
+
+void pkv_set_first_wait_limit_for_testing(int32_t polls, int32_t cta) {
+    g_test_wait_polls = polls < 0 ? -1 : polls;
+    g_test_wait_cta = cta < 0 ? -1 : cta;
+}
 
 int64_t kv_bytes_per_token(int32_t num_layers, int32_t num_kv_heads, int32_t head_dim, pkv_dtype dtype) {
     return 2LL * num_layers * num_kv_heads * head_dim * dtype_bytes(dtype);
@@ -389,7 +399,8 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
                           const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                           int32_t num_seqs, int32_t num_queries, int32_t num_q_heads, int32_t max_seq_len,
                           float scale, int32_t split_tokens, pkv_algo algo, void* workspace, size_t workspace_bytes,
-                          void* out, void* stream, const void* new_k, const void* new_v, pkv_dtype new_dtype) {
+                          void* out, void* stream, const void* new_k, const void* new_v, pkv_dtype new_dtype,
+                          bool dry_run = false) {
     if (!p || layer < 0 || layer >= p->d.num_layers) return PKV_ERR_INVALID_ARG;
     if (num_queries < 1 || num_queries > kMaxQueries) return PKV_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_q_heads < 1 || max_blocks_per_seq < 1 || max_seq_len < 0) return PKV_ERR_INVALID_ARG;
@@ -420,6 +431,7 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
     const bool tc_bal = use_tc && split_tokens == 0 && tc_balanced(num_seqs, p->d.num_kv_heads, static_cast<int64_t>(num_queries) * gh);
     if ((!use_tc || tc_bal) && need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
         return PKV_ERR_WORKSPACE;
+    if (dry_run) return PKV_OK;  // every host-side check passed; nothing enqueued
 
     DecodeArgs a{};
     a.q = q;
@@ -446,6 +458,11 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
     const float log2e = 1.4426950408889634f;
     a.qk_scale_log2 = scale * p->d.k_scale * log2e;
     a.v_scale = p->d.v_scale;
+    if (g_test_wait_polls >= 0) {
+        a.test_wait_on = 1;
+        a.test_wait_polls = static_cast<uint32_t>(g_test_wait_polls);
+        a.test_wait_cta = g_test_wait_cta;
+    }
     if (new_k) {
         a.new_k = static_cast<const uint8_t*>(new_k);
         a.new_v = static_cast<const uint8_t*>(new_v);
@@ -504,6 +521,16 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
     return PKV_OK;
 }
 }  // namespace
+
+pkv_status decode_attention_check(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                  int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len, float scale,
+                                  int32_t split_tokens, pkv_algo algo, void* workspace, size_t workspace_bytes,
+                                  void* out) {
+    return attention_call(q, q_dtype, p, layer, block_tables, max_blocks_per_seq, seq_lens, num_seqs, 1, num_q_heads,
+                          max_seq_len, scale, split_tokens, algo, workspace, workspace_bytes, out, nullptr, nullptr,
+                          nullptr, PKV_BF16, true);
+}
 }  // namespace pkv
 
 extern "C" {

@@ -181,9 +181,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+// Bounded wait for the phase with the given parity to complete: at most
+// `polls` polls (0: give up without looking).  A pipeline wait passes the
+// CTA's abort word: it also gives up once another warp has raised it, so one
+// expired wait ends the whole CTA's pipeline promptly.  The drain waits that
+// guard copies still in flight pass none and keep their full bound.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t polls = kSpinLimit,
+                                          const volatile int* abort = nullptr) {
+    for (uint32_t i = 0; i < polls; ++i) {
         uint32_t ok;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -192,6 +197,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
             : "r"(bar), "r"(parity)
             : "memory");
         if (ok) return true;
+        if (abort && (i & 255u) == 255u && *abort) return false;
     }
     return false;
 }
@@ -216,6 +222,9 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
     int old;
     asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
+}
+__device__ __forceinline__ int cta_linear() {
+    return static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
@@ -306,13 +315,30 @@ struct Acc {
     float l[NT][2];        // lane-partial running sums
     float o[8][NT][4];     // O^T accumulator fragments (8 m-tiles of head_dim)
     uint32_t bq[8][NT][2]; // Q^T as the mma B operand, per 16-wide k-step
+    float qk[NT][2];       // score scale (log2 domain) of this lane's two columns
 };
+
+// FP8 pools: the query enters the f16 MMA scaled by a power of two, 2^-e per
+// query row, chosen so that the row's largest |q| lands in [2^14, 2^15): a
+// BF16 query of any magnitude then converts to f16 exactly (neither
+// overflowing past 65504 nor losing bits to subnormals, except terms below
+// 2^-29 of the row's largest, which stay within f16's subnormal precision),
+// and 2^e is folded back into that row's score scale.
+__device__ __forceinline__ int q_row_exponent(float amax) {
+    if (!(amax > 0.f)) return 0;  // zero (or NaN) row
+    const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127;  // floor(log2) for normal amax
+    const int e = ex - 14;
+    return e < -110 ? -110 : (e > 110 ? 110 : e);  // keeps 2^e and 2^-e normal binary32
+}
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
 
 // Start a segment: clear the state and build the Q^T fragments of columns
 // [col0, col0 + 8*NT) from the stage's query rows qs[NQ][128] (BF16, shared
-// memory); columns >= col_end are zero padding.
+// memory); columns >= col_end are zero padding.  qk: the score scale
+// (scale * k_scale * log2 e).
 template <int DT, int NT>
-__device__ __forceinline__ void acc_begin(Acc<NT>& s, const __nv_bfloat16* qs, int lane, int col0, int col_end) {
+__device__ __forceinline__ void acc_begin(Acc<NT>& s, const __nv_bfloat16* qs, int lane, int col0, int col_end,
+                                          float qk) {
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         s.m[j][0] = s.m[j][1] = -INFINITY;
@@ -324,21 +350,47 @@ __device__ __forceinline__ void acc_begin(Acc<NT>& s, const __nv_bfloat16* qs, i
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         const int n = col0 + 8 * j + r;
+        if constexpr (DT == PKV_BF16) {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            if (n >= col_end) {
-                s.bq[ks][j][0] = s.bq[ks][j][1] = 0u;
-                continue;
-            }
-            if constexpr (DT == PKV_BF16) {
+            for (int ks = 0; ks < 8; ++ks) {
+                if (n >= col_end) {
+                    s.bq[ks][j][0] = s.bq[ks][j][1] = 0u;
+                    continue;
+                }
                 const uint32_t* w = reinterpret_cast<const uint32_t*>(qs + n * kD + ks * 16 + 2 * q);
                 s.bq[ks][j][0] = w[0];
                 s.bq[ks][j][1] = w[4];  // +8 elements
-            } else {  // head_dim order permuted like K's: chunk ks, bytes 4q..4q+3
-                const __nv_bfloat16* p = qs + n * kD + ks * 16 + 4 * q;
-                s.bq[ks][j][0] = pack2<DT>(__bfloat162float(p[0]), __bfloat162float(p[1]));
-                s.bq[ks][j][1] = pack2<DT>(__bfloat162float(p[2]), __bfloat162float(p[3]));
             }
+            s.qk[j][0] = s.qk[j][1] = qk;
+        } else {  // head_dim order permuted like K's: chunk ks, bytes 4q..4q+3
+            // the row's largest |q|: this lane's 32 values, then the row's 4 lanes
+            float amax = 0.f;
+            if (n < col_end) {
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const __nv_bfloat16* p = qs + n * kD + ks * 16 + 4 * q;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(__bfloat162float(p[i])));
+                }
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+            const int e = q_row_exponent(amax);
+            const float f = pow2f(-e);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                if (n >= col_end) {
+                    s.bq[ks][j][0] = s.bq[ks][j][1] = 0u;
+                    continue;
+                }
+                const __nv_bfloat16* p = qs + n * kD + ks * 16 + 4 * q;
+                s.bq[ks][j][0] = pack2<DT>(__bfloat162float(p[0]) * f, __bfloat162float(p[1]) * f);
+                s.bq[ks][j][1] = pack2<DT>(__bfloat162float(p[2]) * f, __bfloat162float(p[3]) * f);
+            }
+            // this lane's columns 2q, 2q+1 are the rows held by lanes 8q and 8q+4
+            const float qrow = qk * pow2f(e);
+            s.qk[j][0] = __shfl_sync(0xFFFFFFFFu, qrow, 8 * q);
+            s.qk[j][1] = __shfl_sync(0xFFFFFFFFu, qrow, 8 * q + 4);
         }
     }
 }
@@ -383,7 +435,7 @@ __device__ __forceinline__ LaneOffsets lane_offsets(int lane) {
 // lane's two columns of n-tile j (all <= n; equal to n for decode).
 template <int DT, int MT, int NT>
 __device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* vst, int n, int row0, int lane,
-                                             const uint32_t (&wb)[MT], uint32_t half_stride, float qk,
+                                             const uint32_t (&wb)[MT], uint32_t half_stride,
                                              const LaneOffsets& lo, const int (&lim)[NT][2]) {
     constexpr int kHalves = MmaCfg<DT>::kHalves;
     if (row0 >= n) return;
@@ -455,10 +507,10 @@ __device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* 
         const int ra = row0 + 16 * i + r, rb = ra + 8;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-            sv[i][j][0] = ra < lim[j][0] ? sc[i][j][0] * qk : -INFINITY;
-            sv[i][j][1] = ra < lim[j][1] ? sc[i][j][1] * qk : -INFINITY;
-            sv[i][j][2] = rb < lim[j][0] ? sc[i][j][2] * qk : -INFINITY;
-            sv[i][j][3] = rb < lim[j][1] ? sc[i][j][3] * qk : -INFINITY;
+            sv[i][j][0] = ra < lim[j][0] ? sc[i][j][0] * s.qk[j][0] : -INFINITY;
+            sv[i][j][1] = ra < lim[j][1] ? sc[i][j][1] * s.qk[j][1] : -INFINITY;
+            sv[i][j][2] = rb < lim[j][0] ? sc[i][j][2] * s.qk[j][0] : -INFINITY;
+            sv[i][j][3] = rb < lim[j][1] ? sc[i][j][3] * s.qk[j][1] : -INFINITY;
             x[j][0] = fmaxf(x[j][0], fmaxf(sv[i][j][0], sv[i][j][2]));
             x[j][1] = fmaxf(x[j][1], fmaxf(sv[i][j][1], sv[i][j][3]));
         }
@@ -860,7 +912,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         bool ok = true;
         auto acquire = [&](long long kk) -> int {  // stage for the kk-th issue, after it is free
             const int s = static_cast<int>(kk % kStages);
-            if (kk >= kStages && ok) ok = mbar_wait(smem_u32(&empty[s]), static_cast<uint32_t>(((kk / kStages) - 1) & 1));
+            if (kk >= kStages && ok)
+                ok = mbar_wait(smem_u32(&empty[s]), static_cast<uint32_t>(((kk / kStages) - 1) & 1), kSpinLimit,
+                               abort_flag);
             if (*abort_flag) ok = false;
             return s;
         };
@@ -1038,7 +1092,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     auto csync = [&]() -> bool {
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(csync_bar));
-        const bool okw = mbar_wait(smem_u32(csync_bar), cphase);
+        const bool okw = mbar_wait(smem_u32(csync_bar), cphase, kSpinLimit, abort_flag);
         cphase ^= 1u;
         __syncwarp();
         if (!okw) {
@@ -1056,9 +1110,12 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     };
 
+    // test hook: this CTA's first stage wait may be cut short (an expired wait on demand)
+    const bool short_first = a.test_wait_on != 0 && (a.test_wait_cta < 0 || a.test_wait_cta == cta_linear());
     for (long long k = 0;; ++k) {
         const int s = static_cast<int>(k % kStages);
-        if (!mbar_wait(smem_u32(&full[s]), static_cast<uint32_t>((k / kStages) & 1))) {
+        const uint32_t polls = (k == 0 && short_first) ? a.test_wait_polls : kSpinLimit;
+        if (!mbar_wait(smem_u32(&full[s]), static_cast<uint32_t>((k / kStages) & 1), polls, abort_flag)) {
             aborted = true;
             if (lane == 0) {
                 *abort_flag = 1;
@@ -1071,7 +1128,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         uint8_t* kst = smem + s * Lt::kStageBytes;
         if (ti.flags & kSegFirst)
             acc_begin<DT, kNT>(acc, reinterpret_cast<const __nv_bfloat16*>(smem + Lt::kQOff + s * Lt::kQBytes), lane,
-                               col0, col_end);
+                               col0, col_end, qk);
         int lim[kNT][2];
 #pragma unroll
         for (int j = 0; j < kNT; ++j) {
@@ -1081,7 +1138,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 #pragma unroll
         for (int st = 0; st < kCalls; ++st)
             consume_tile<DT, kCallMT, kNT>(acc, kst, kst + Lt::kTensorBytes, ti.n, rbase + 16 * kCallMT * st, lane,
-                                           wb[st], half_stride, qk, lane_off, lim);
+                                           wb[st], half_stride, lane_off, lim);
         const bool seg_last = (ti.flags & kSegLast) != 0;
         if (!kInStage || !seg_last) release(s);
         if (!seg_last) continue;

@@ -12,10 +12,14 @@
 // The array's size is fixed (PKV_STATIC_SCRATCH_BYTES); every GPU on which the
 // library is loaded holds it until the process exits.  All calls share it:
 // calls that overlap on the GPU (different streams without ordering, or
-// different host threads) race on it.  Nothing in it needs clearing between
-// calls: the only words that must start at zero (the per-sequence piece
-// counters) are cleared once, when the array is first set up on a device, and
-// every call leaves them at zero again.
+// different host threads) race on it.  It keeps whatever the previous call
+// left there.  The only words that must start at zero are the per-(sequence,
+// KV head) piece counters at its front, and where they sit depends on the
+// call's shape (a later call with more sequences or KV heads finds its
+// counters in bytes an earlier call filled with partial sums; a call whose
+// pipeline wait expired may leave counters non-zero).  So every call that
+// uses the array first clears its own counter bytes, in stream order on the
+// call's stream (one small memset; no allocation), and then launches.
 #include <cstdio>
 
 #include "pkv_internal.h"
@@ -54,8 +58,6 @@ extern "C" pkv_status paged_decode_attention_static_ws(const void* q, pkv_dtype 
         if (!g_scratch_addr[dev]) {  // once per device, with that device current
             void* p = nullptr;
             e = cudaGetSymbolAddress(&p, g_decode_scratch);
-            // the piece counters must start at zero; cleared in stream order
-            if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, PKV_STATIC_SCRATCH_BYTES, static_cast<cudaStream_t>(stream));
             if (e != cudaSuccess) {
                 pkv::set_last_error(e);
                 return PKV_ERR_CUDA;
@@ -63,6 +65,18 @@ extern "C" pkv_status paged_decode_attention_static_ws(const void* q, pkv_dtype 
             g_scratch_addr[dev] = p;
         }
         scratch = g_scratch_addr[dev];
+        // a rejected call enqueues nothing: check every argument before the memset
+        const pkv_status chk = pkv::decode_attention_check(
+            q, q_dtype, pool, layer, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, max_seq_len,
+            scale, split_tokens, algo, scratch, static_cast<size_t>(PKV_STATIC_SCRATCH_BYTES), out);
+        if (chk != PKV_OK) return chk;
+        // this call's counters must start at zero whatever earlier calls left
+        e = cudaMemsetAsync(scratch, 0, pkv::workspace_counter_bytes(num_seqs, pool->d.num_kv_heads),
+                            static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) {
+            pkv::set_last_error(e);
+            return PKV_ERR_CUDA;
+        }
     }
     return paged_decode_attention(q, q_dtype, pool, layer, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
                                   num_q_heads, max_seq_len, scale, split_tokens, algo, scratch,

@@ -35,6 +35,16 @@ constexpr int kTileTokens = 64;  // tokens one decode CTA stages per pipeline st
 int dtype_bytes(pkv_dtype t);
 int num_sms();  // SM count of the current device (cached)
 void set_last_error(cudaError_t e);
+// Bytes at the front of a decode workspace that hold the per-(sequence, KV
+// head) piece counters (int32 [num_seqs][num_kv_heads], rounded up to 256).
+size_t workspace_counter_bytes(int num_seqs, int num_kv_heads);
+// Every host-side check of paged_decode_attention with these arguments,
+// without enqueuing anything: PKV_OK when the call would be launched.
+pkv_status decode_attention_check(const void* q, pkv_dtype q_dtype, const pkv_pool* p, int32_t layer,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                  int32_t num_seqs, int32_t num_q_heads, int32_t max_seq_len, float scale,
+                                  int32_t split_tokens, pkv_algo algo, void* workspace, size_t workspace_bytes,
+                                  void* out);
 
 // ---------------------------------------------------------------- append
 cudaError_t launch_kv_append(const pkv_pool* pool, int layer, const void* k, const void* v,
@@ -83,6 +93,13 @@ struct DecodeArgs {
     int split_tokens, num_splits;
     float qk_scale_log2;      // scale * k_scale * log2(e)
     float v_scale;            // v_scale (FP8) or 1
+    // Test hook (pkv_set_first_wait_limit_for_testing): with test_wait_on,
+    // the consumers' first wait for a loaded stage in CTA test_wait_cta (its
+    // linear block index; every CTA when < 0) gives up after test_wait_polls
+    // polls, exactly as an expired wait does.  Zero-initialised: off.
+    int test_wait_on;
+    uint32_t test_wait_polls;
+    int test_wait_cta;
 };
 
 // Returns cudaErrorNotSupported when no kernel matches (dtype, D, query rows

@@ -1,24 +1,38 @@
-"""In-flight (continuous) batching over the paged KV cache.
+"""In-flight (continuous) batching over the paged KV cache: the host side of
+the decode hot path.
 
-"TensorRT-LLM, in depth", "In-flight batching and the scheduler": each
-iteration rebuilds the batch -- running requests contribute one decode token
-each (a request that cannot get a block for its next token is paused and
-retried later), then waiting requests are admitted with a prefill chunk after
-their cached prefix is matched, within two limits: max_batch_size requests
-and max_num_tokens tokens per iteration.  "How does TensorRT-LLM work?", "In-
-flight batching": a finished request leaves at once and its blocks return to
-the free pool.
+Policy, from "TensorRT-LLM, in depth", section "In-flight batching and the
+scheduler", and "How does TensorRT-LLM work?", section "In-flight batching":
+the batch is rebuilt before every forward pass under two caps, a number of
+requests and a number of tokens; requests already generating take priority
+over new ones; a request whose next token needs a block the pool cannot give
+waits for a later pass instead of failing; a new request first reuses the
+cached blocks of its longest matching prefix and may have its prompt cut
+into chunks across passes; a request that has finished leaves at once and
+its blocks go back to the pool.
 
-This module only plans iterations (which tokens go to which slots); the
-caller writes the planned tokens' K/V with ``kv_append`` and runs
-``paged_decode_attention`` for the decoding requests.  It is the host side of
-the decode hot path: no model, no sampling.
+Design.  A pass walks one queue of candidates in priority order -- the
+generating requests in the order they started, then the admitted-but-not-
+yet-generating and the new requests in arrival order -- and grants each what
+it asks for from one shared ``Budget`` (seats and tokens): one token for a
+generating request, as much of the remaining prompt as the budget allows for
+a prompt.  A grant that the pool cannot back with blocks either pauses the
+request (generating ones) or ends admission for the pass (prompts: later
+arrivals must not overtake an earlier one).  Where the pages leave a gap:
+if a pass would do nothing at all because every generating request is
+paused, the most recently started one releases its blocks and goes back to
+the front of the queue to be recomputed, so the loop always progresses.
+
+This module only plans (which token goes to which slot); the caller writes
+the planned tokens' K/V with ``kv_append`` and runs
+``paged_decode_attention`` for the generating requests.  No model, no
+sampling.
 """
 from __future__ import annotations
 
 from collections import deque
 from dataclasses import dataclass, field
-from typing import Deque, Dict, List, Optional, Sequence, Tuple
+from typing import Deque, Iterator, List, Optional, Tuple
 
 import numpy as np
 
@@ -33,7 +47,7 @@ class Request:
     prefilled: int = 0           # prompt tokens already in the cache (written or reused)
     reused: int = 0              # of which shared from cached blocks
     generated: int = 0           # decode tokens appended so far
-    admitted: bool = False
+    admitted: bool = False       # holds a sequence in the block manager
 
     @property
     def length(self) -> int:
@@ -42,6 +56,10 @@ class Request:
     @property
     def done(self) -> bool:
         return self.generated >= self.max_new_tokens
+
+    @property
+    def prompt_left(self) -> int:
+        return len(self.prompt) - self.prefilled
 
 
 @dataclass
@@ -57,13 +75,27 @@ class Iteration:
         return len(self.decode) + sum(len(s) for _, _, s in self.prefill)
 
 
+@dataclass
+class Budget:
+    """What one pass may still hand out."""
+    seats: int
+    tokens: int
+
+    def exhausted(self) -> bool:
+        return self.seats <= 0 or self.tokens <= 0
+
+    def take(self, tokens: int) -> None:
+        self.seats -= 1
+        self.tokens -= tokens
+
+
 class InFlightScheduler:
     def __init__(self, bm: BlockManager, max_batch_size: int, max_num_tokens: int):
         self.bm = bm
         self.max_batch_size = int(max_batch_size)
         self.max_num_tokens = int(max_num_tokens)
-        self.running: List[Request] = []     # prompt fully cached: decoding
-        self.waiting: Deque[Request] = deque()
+        self.running: List[Request] = []     # whole prompt cached: one token per pass
+        self.waiting: Deque[Request] = deque()  # prompt not (fully) cached yet, arrival order
         self.finished: List[Request] = []
         self.preempted = 0
 
@@ -73,55 +105,77 @@ class InFlightScheduler:
     def idle(self) -> bool:
         return not self.running and not self.waiting
 
+    # ------------------------------------------------------------ planning
+    def _queue(self) -> Iterator[Tuple[Request, bool]]:
+        """Candidates in priority order, each with whether it is generating."""
+        for r in list(self.running):
+            yield r, True
+        for r in list(self.waiting):
+            yield r, False
+
+    def _grant_token(self, r: Request, it: Iteration, budget: Budget) -> None:
+        """A generating request asks for the slot of its next token."""
+        slot = int(self.bm.decode_slots([r.rid])[0])
+        if slot < 0:  # no block for it this pass: it waits, costing nothing
+            it.paused.append(r)
+            return
+        it.decode.append((r, r.length, slot))
+        r.generated += 1
+        budget.take(1)
+
+    def _grant_prompt(self, r: Request, it: Iteration, budget: Budget) -> bool:
+        """A prompt asks for its next chunk; False when the pool cannot back
+        it (admission stops for this pass)."""
+        if not r.admitted:
+            self.bm.add(r.rid)
+            r.prefilled = r.reused = self.bm.match_prefix(r.rid, r.prompt)
+            r.admitted = True
+        n = min(r.prompt_left, budget.tokens)
+        first = r.prefilled
+        try:
+            slots = self.bm.grow(r.rid, n, token_ids=r.prompt[first:first + n])
+        except OutOfBlocks:
+            return False
+        it.prefill.append((r, first, slots))
+        r.prefilled += n
+        budget.take(n)
+        return True
+
     def plan(self) -> Iteration:
-        """Plan one iteration (the pages' schedule() sketch)."""
+        """Plan one forward pass."""
         it = Iteration()
-        batch, budget = 0, self.max_num_tokens
-        for r in self.running:                      # decoding requests: 1 token each
-            if batch == self.max_batch_size or budget == 0:
+        budget = Budget(self.max_batch_size, self.max_num_tokens)
+        admitting = True
+        for r, generating in self._queue():
+            if budget.exhausted():
                 break
-            pos = r.length
-            slot = int(self.bm.decode_slots([r.rid])[0])
-            if slot < 0:                            # out of blocks: pause, retry later
-                it.paused.append(r)
-                continue
-            r.generated += 1
-            it.decode.append((r, pos, slot))
-            batch += 1
-            budget -= 1
-        for r in list(self.waiting):                # new requests: prefill, maybe chunked
-            if batch == self.max_batch_size or budget == 0:
-                break
-            if not r.admitted:
-                self.bm.add(r.rid)
-                r.reused = r.prefilled = self.bm.match_prefix(r.rid, r.prompt)
-                r.admitted = True
-            chunk = min(len(r.prompt) - r.prefilled, budget)
-            try:
-                slots = self.bm.grow(r.rid, chunk, token_ids=r.prompt[r.prefilled:r.prefilled + chunk])
-            except OutOfBlocks:
-                break
-            it.prefill.append((r, r.prefilled, slots))
-            r.prefilled += chunk
-            batch += 1
-            budget -= chunk
-            if r.prefilled == len(r.prompt):        # whole prompt cached: decode from the next pass
+            if generating:
+                self._grant_token(r, it, budget)
+            elif admitting:
+                admitting = self._grant_prompt(r, it, budget)
+        # prompts cached in full this pass generate from the next one on
+        for r, _, _ in it.prefill:
+            if r.prompt_left == 0:
                 self.waiting.remove(r)
                 self.running.append(r)
         if it.num_tokens == 0 and it.paused:
-            # every running request is paused and nothing could be admitted:
-            # the newest running request gives its blocks back and starts over
-            # (recompute), so the others can make progress
-            victim = self.running.pop()
-            self.bm.free_sequence(victim.rid)
-            victim.prefilled = victim.reused = victim.generated = 0
-            victim.admitted = False
-            self.waiting.appendleft(victim)
-            self.preempted += 1
+            self._recompute_newest()
         return it
 
+    def _recompute_newest(self) -> None:
+        """Every generating request is stuck and nothing was admitted: the one
+        that started last gives its blocks back and re-enters the queue first,
+        to be prefilled again."""
+        victim = self.running.pop()
+        self.bm.free_sequence(victim.rid)
+        victim.prefilled = victim.reused = victim.generated = 0
+        victim.admitted = False
+        self.waiting.appendleft(victim)
+        self.preempted += 1
+
+    # ------------------------------------------------------------ after a pass
     def retire(self, it: Optional[Iteration] = None) -> List[Request]:
-        """After the pass: finished requests leave and free their blocks."""
+        """Finished requests leave and free their blocks."""
         done = [r for r in self.running if r.done]
         for r in done:
             self.running.remove(r)
@@ -132,6 +186,6 @@ class InFlightScheduler:
         return done
 
     def decode_view(self, it: Iteration, width: int):
-        """Tables and lengths of this pass's decoding requests (host tensors)."""
+        """Tables and lengths of this pass's generating requests (host tensors)."""
         rids = [r.rid for r, _, _ in it.decode]
         return rids, self.bm.block_tables(rids, width), self.bm.seq_lens(rids)

@@ -59,7 +59,8 @@ def test_fused_equals_two_launches(w, split):
 
 
 def test_fused_full_size_llama(record_property):
-    """The bench's decode step in one launch, at full size, on sampled sequences."""
+    """The benchmark's decode step (one launch: append + attention) at full
+    size, every sequence compared with the oracle."""
     w = wl.WORKLOADS["llama"]
     inst = wl.instance(w)
     batch = DecodeBatch(inst)
@@ -69,11 +70,41 @@ def test_fused_full_size_llama(record_property):
     out = pk.paged_decode_append_attention(q.cuda(), kn.cuda(), vn.cuda(), batch.pool, 0, tables.cuda(),
                                            lens.cuda(), int(lens.max()), w.scale)
     torch.cuda.synchronize()
-    seqs = [0, 7, 31, 63]
+    seqs = list(range(w.num_seqs))
     ref, _ = oracle_reference(w, inst.k_scale, inst.v_scale, 0, q, tables, lens.tolist(), seqs)
-    max_abs, max_rel = compare(out[seqs], ref, TOL["bf16"], "llama fused")
+    max_abs, max_rel = compare(out, ref, TOL["bf16"], "llama fused")
     record_property("max_abs_err", max_abs)
     record_property("max_rel_err", max_rel)
+    assert batch.pool.errors() == 0
+
+
+def test_fused_full_size_ragged_steps(record_property):
+    """The in-flight batch (256 sequences, 32-token blocks, 4 query heads per
+    KV head) for 8 fused decode steps, the block manager growing the tables
+    between them; every sequence compared with the oracle at the first and
+    the last step."""
+    w = wl.WORKLOADS["ragged"]
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    seqs = list(range(w.num_seqs))
+    ws = None
+    worst = (0.0, 0.0)
+    for step in range(w.steps):
+        batch.next_token_slots()
+        q, kn, vn = batch.step_inputs(0, step)
+        tables, lens = batch.tables(), batch.seq_lens()
+        if ws is None:
+            ws = pk.workspace_for(batch.pool, w.num_seqs, w.num_q_heads, int(inst.lens.max()) + w.steps)
+        out = pk.paged_decode_append_attention(q.cuda(), kn.cuda(), vn.cuda(), batch.pool, 0, tables.cuda(),
+                                               lens.cuda(), int(lens.max()), w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        if step in (0, w.steps - 1):
+            ref, _ = oracle_reference(w, 1.0, 1.0, 0, q, tables, lens.tolist(), seqs)
+            e = compare(out, ref, TOL["bf16"], "ragged fused step %d" % step)
+            worst = (max(worst[0], e[0]), max(worst[1], e[1]))
+        batch.bm.check()
+    record_property("max_abs_err", worst[0])
+    record_property("max_rel_err", worst[1])
     assert batch.pool.errors() == 0
 
 
