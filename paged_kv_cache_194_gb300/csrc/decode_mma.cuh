@@ -282,11 +282,42 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-// Two E4M3 codes (low byte first) -> f16x2 (exact).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-    __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
-    return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+// FP8 pools run both products on the E4M3 tensor-core path, with no
+// per-element conversion of the cache: mma m16n8k32 takes E4M3 operands and
+// accumulates in fp32.  K and V enter as stored; the query and the
+// probabilities, which the method keeps at higher precision, enter as two
+// E4M3 terms each, hi = e4m3(x) and lo = e4m3(x - hi), whose two MMAs
+// accumulate into one result (hi + lo carries about 8 significant bits,
+// as many as BF16).
+__device__ __forceinline__ void mma_e4m3(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// f16x2 x -> two E4M3x2 terms (element order kept, low element in the low
+// byte): hi = e4m3_rn(x), lo = e4m3_rn(x - hi).  x - hi is exact in f16 (hi
+// is x rounded to 4 significant bits, within a factor 2 of it).
+__device__ __forceinline__ void split_e4m3x2(uint32_t x, uint32_t& hi, uint32_t& lo) {
+    __half2_raw xr;
+    xr.x = static_cast<unsigned short>(x & 0xFFFFu);
+    xr.y = static_cast<unsigned short>(x >> 16);
+    const __nv_fp8x2_storage_t h = __nv_cvt_halfraw2_to_fp8x2(xr, __NV_SATFINITE, __NV_E4M3);
+    const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
+    __half2 xv, hv;
+    *reinterpret_cast<__half2_raw*>(&xv) = xr;
+    *reinterpret_cast<__half2_raw*>(&hv) = hb;
+    const __half2 r = __hsub2(xv, hv);
+    const __nv_fp8x2_storage_t l =
+        __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&r), __NV_SATFINITE, __NV_E4M3);
+    hi = static_cast<uint32_t>(h);
+    lo = static_cast<uint32_t>(l);
+}
+// Probabilities enter the E4M3 MMA scaled by 2^8 (they are <= 1; E4M3 holds
+// up to 448), undone in the output scale.
+constexpr float kFp8PScale = 256.f;
 
 // Byte offset of 16-byte chunk `chunk` of row `lr` inside a 128B-swizzled run
 // of rows whose first row sits on a 1024-byte boundary (and is a multiple of 8
@@ -318,16 +349,15 @@ struct Acc {
     float qk[NT][2];       // score scale (log2 domain) of this lane's two columns
 };
 
-// FP8 pools: the query enters the f16 MMA scaled by a power of two, 2^-e per
-// query row, chosen so that the row's largest |q| lands in [2^14, 2^15): a
-// BF16 query of any magnitude then converts to f16 exactly (neither
-// overflowing past 65504 nor losing bits to subnormals, except terms below
-// 2^-29 of the row's largest, which stay within f16's subnormal precision),
-// and 2^e is folded back into that row's score scale.
+// FP8 pools: each query row enters the E4M3 MMA scaled by a power of two,
+// 2^-e, chosen so that the row's largest |q| lands in [2^7, 2^8): a BF16
+// query of any magnitude then fits E4M3 (largest finite 448) and its f16
+// staging copy exactly, and small entries keep the E4M3 range below it;
+// 2^e is folded back into that row's score scale.
 __device__ __forceinline__ int q_row_exponent(float amax) {
     if (!(amax > 0.f)) return 0;  // zero (or NaN) row
     const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127;  // floor(log2) for normal amax
-    const int e = ex - 14;
+    const int e = ex - 7;
     return e < -110 ? -110 : (e > 110 ? 110 : e);  // keeps 2^e and 2^-e normal binary32
 }
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
@@ -362,7 +392,10 @@ __device__ __forceinline__ void acc_begin(Acc<NT>& s, const __nv_bfloat16* qs, i
                 s.bq[ks][j][1] = w[4];  // +8 elements
             }
             s.qk[j][0] = s.qk[j][1] = qk;
-        } else {  // head_dim order permuted like K's: chunk ks, bytes 4q..4q+3
+        } else {
+            // E4M3 B fragments of m16n8k32: k32 step kp, register h holds
+            // head dims 32 kp + 16 h + 4q .. +3 of row n (K's A fragments come
+            // from ldmatrix in natural order).  bq[2 kp] = hi terms, bq[2 kp + 1] = lo.
             // the row's largest |q|: this lane's 32 values, then the row's 4 lanes
             float amax = 0.f;
             if (n < col_end) {
@@ -378,14 +411,21 @@ __device__ __forceinline__ void acc_begin(Acc<NT>& s, const __nv_bfloat16* qs, i
             const int e = q_row_exponent(amax);
             const float f = pow2f(-e);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                if (n >= col_end) {
-                    s.bq[ks][j][0] = s.bq[ks][j][1] = 0u;
-                    continue;
+            for (int kp = 0; kp < 4; ++kp) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t hi = 0u, lo = 0u;
+                    if (n < col_end) {
+                        const __nv_bfloat16* p = qs + n * kD + 32 * kp + 16 * h + 4 * q;
+                        uint32_t h01, l01, h23, l23;
+                        split_e4m3x2(pack2<DT>(__bfloat162float(p[0]) * f, __bfloat162float(p[1]) * f), h01, l01);
+                        split_e4m3x2(pack2<DT>(__bfloat162float(p[2]) * f, __bfloat162float(p[3]) * f), h23, l23);
+                        hi = h01 | (h23 << 16);
+                        lo = l01 | (l23 << 16);
+                    }
+                    s.bq[2 * kp][j][h] = hi;
+                    s.bq[2 * kp + 1][j][h] = lo;
                 }
-                const __nv_bfloat16* p = qs + n * kD + ks * 16 + 4 * q;
-                s.bq[ks][j][0] = pack2<DT>(__bfloat162float(p[0]) * f, __bfloat162float(p[1]) * f);
-                s.bq[ks][j][1] = pack2<DT>(__bfloat162float(p[2]) * f, __bfloat162float(p[3]) * f);
             }
             // this lane's columns 2q, 2q+1 are the rows held by lanes 8q and 8q+4
             const float qrow = qk * pow2f(e);
@@ -478,24 +518,34 @@ __device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* 
             }
         }
     } else {
+        // one ldmatrix.x4 = the E4M3 A fragment of a k32 step (bytes 32 kp ..
+        // 32 kp + 31 of 16 token rows); hi and lo query terms accumulate apart
+        // (two independent chains) and are summed after the last step
+        float sl[MT][NT][4];
 #pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {  // two k-steps (chunks 2kp, 2kp+1) per ldmatrix.x4
+        for (int i = 0; i < MT; ++i)
+#pragma unroll
+            for (int j = 0; j < NT; ++j) sl[i][j][0] = sl[i][j][1] = sl[i][j][2] = sl[i][j][3] = 0.f;
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
 #pragma unroll
             for (int i = 0; i < MT; ++i) {
                 if (!live[i]) continue;
                 uint32_t r0, r1, r2, r3;
                 ldsm_x4(kb + wb[i] + lo.k[kp], r0, r1, r2, r3);
-                const uint32_t c0 = e4m3x2_to_f16x2(r0), c1 = e4m3x2_to_f16x2(r1);
-                const uint32_t c2 = e4m3x2_to_f16x2(r0 >> 16), c3 = e4m3x2_to_f16x2(r1 >> 16);
-                const uint32_t c4 = e4m3x2_to_f16x2(r2), c5 = e4m3x2_to_f16x2(r3);
-                const uint32_t c6 = e4m3x2_to_f16x2(r2 >> 16), c7 = e4m3x2_to_f16x2(r3 >> 16);
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    mma16816<DT>(sc[i][j], c0, c1, c2, c3, s.bq[2 * kp][j][0], s.bq[2 * kp][j][1]);
-                    mma16816<DT>(sc[i][j], c4, c5, c6, c7, s.bq[2 * kp + 1][j][0], s.bq[2 * kp + 1][j][1]);
+                    mma_e4m3(sc[i][j], r0, r1, r2, r3, s.bq[2 * kp][j][0], s.bq[2 * kp][j][1]);
+                    mma_e4m3(sl[i][j], r0, r1, r2, r3, s.bq[2 * kp + 1][j][0], s.bq[2 * kp + 1][j][1]);
                 }
             }
         }
+#pragma unroll
+        for (int i = 0; i < MT; ++i)
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sc[i][j][c] += sl[i][j][c];
     }
     // ---- online softmax (log2 domain) over the step's 16*MT rows, per column
     float sv[MT][NT][4];
@@ -573,18 +623,18 @@ __device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* 
         s.m[j][0] = nm[j][0];
         s.m[j][1] = nm[j][1];
     }
-    uint32_t pb[MT][NT][2];
-#pragma unroll
-    for (int i = 0; i < MT; ++i) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            pb[i][j][0] = movmatrix_t(pack2<DT>(p[i][j][0], p[i][j][1]));  // tokens 0-7 of m-tile i
-            pb[i][j][1] = movmatrix_t(pack2<DT>(p[i][j][2], p[i][j][3]));  // tokens 8-15
-        }
-    }
     // ---- O^T += V^T P^T; one V fragment feeds every n-tile
     const uint32_t vb0 = smem_u32(vst);
     if constexpr (DT == PKV_BF16) {
+        uint32_t pb[MT][NT][2];
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                pb[i][j][0] = movmatrix_t(pack2<DT>(p[i][j][0], p[i][j][1]));  // tokens 0-7 of m-tile i
+                pb[i][j][1] = movmatrix_t(pack2<DT>(p[i][j][2], p[i][j][3]));  // tokens 8-15
+            }
+        }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
 #pragma unroll
@@ -597,27 +647,62 @@ __device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* 
             }
         }
     } else {
-        // rows ta, ta+1 (ta = 2q) at offsets v[2c], v[2c+1]; rows ta+8, ta+9 are 8 rows (1024 B) further
+        static_assert(MT % 2 == 0, "an E4M3 k32 step spans two 16-token m-tiles");
+        // k-slot order within a 16-token m-tile: slots 4q .. 4q+3 hold tokens
+        // 2q, 2q+1, 2q+8, 2q+9 (the same order in P and in V, so every product
+        // pairs the right token); a k32 step covers m-tiles (i, i+1).
+        // P^T (scaled by 2^8) as hi / lo E4M3 B fragments per m-tile
+        uint32_t ph[MT][NT], pl[MT][NT];
+        const __half2 ps = __float2half2_rn(kFp8PScale);
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                uint32_t t0 = movmatrix_t(pack2<DT>(p[i][j][0], p[i][j][1]));  // (column r; tokens 2q, 2q+1)
+                uint32_t t1 = movmatrix_t(pack2<DT>(p[i][j][2], p[i][j][3]));  // (column r; tokens 2q+8, 2q+9)
+                __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&t0), ps);
+                __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&t1), ps);
+                uint32_t hi0, lo0, hi1, lo1;
+                split_e4m3x2(*reinterpret_cast<uint32_t*>(&h0), hi0, lo0);
+                split_e4m3x2(*reinterpret_cast<uint32_t*>(&h1), hi1, lo1);
+                ph[i][j] = hi0 | (hi1 << 16);
+                pl[i][j] = lo0 | (lo1 << 16);
+            }
+        }
+        // V^T A fragments: thread (r, q) reads the 4-byte word of head dims
+        // 32c + 4r .. +3 of tokens 2q, 2q+1, 2q+8, 2q+9 and transposes the 4x4
+        // bytes: dim 32c + 4r + i of those tokens is m-tile 2c (i = 0, 1: rows r,
+        // r+8) or 2c+1 (i = 2, 3) of O^T (see o_dim).
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
-            for (int i = 0; i < MT; ++i) {
-                if (!live[i]) continue;
-                const uint32_t vb_ = vb0 + wb[i];
-                const uint32_t w0 = lds32(vb_ + lo.v[2 * c]);
-                const uint32_t w1 = lds32(vb_ + lo.v[2 * c + 1]);
-                const uint32_t w8 = lds32<8 * kBoxRowBytes>(vb_ + lo.v[2 * c]);
-                const uint32_t w9 = lds32<8 * kBoxRowBytes>(vb_ + lo.v[2 * c + 1]);
-                const uint32_t x01 = __byte_perm(w0, w1, 0x5140), x23 = __byte_perm(w0, w1, 0x7362);
-                const uint32_t y01 = __byte_perm(w8, w9, 0x5140), y23 = __byte_perm(w8, w9, 0x7362);
-                const uint32_t e0 = e4m3x2_to_f16x2(x01), e1 = e4m3x2_to_f16x2(x01 >> 16);
-                const uint32_t e2 = e4m3x2_to_f16x2(y01), e3 = e4m3x2_to_f16x2(y01 >> 16);
-                const uint32_t f0 = e4m3x2_to_f16x2(x23), f1 = e4m3x2_to_f16x2(x23 >> 16);
-                const uint32_t f2 = e4m3x2_to_f16x2(y23), f3 = e4m3x2_to_f16x2(y23 >> 16);
+            for (int i0 = 0; i0 < MT; i0 += 2) {
+                if (!live[i0]) continue;
+                uint32_t R[2][4];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (u == 1 && !live[i0 + 1]) {
+                        R[1][0] = R[1][1] = R[1][2] = R[1][3] = 0u;
+                        continue;
+                    }
+                    const uint32_t vb_ = vb0 + wb[i0 + u];
+                    const uint32_t w0 = lds32(vb_ + lo.v[2 * c]);                         // token 2q
+                    const uint32_t w1 = lds32(vb_ + lo.v[2 * c + 1]);                     // token 2q+1
+                    const uint32_t w2 = lds32<8 * kBoxRowBytes>(vb_ + lo.v[2 * c]);       // token 2q+8
+                    const uint32_t w3 = lds32<8 * kBoxRowBytes>(vb_ + lo.v[2 * c + 1]);   // token 2q+9
+                    const uint32_t x01 = __byte_perm(w0, w1, 0x5140), x23 = __byte_perm(w0, w1, 0x7362);
+                    const uint32_t y01 = __byte_perm(w2, w3, 0x5140), y23 = __byte_perm(w2, w3, 0x7362);
+                    R[u][0] = __byte_perm(x01, y01, 0x5410);  // dim +0 of the 4 tokens
+                    R[u][1] = __byte_perm(x01, y01, 0x7632);  // dim +1
+                    R[u][2] = __byte_perm(x23, y23, 0x5410);  // dim +2
+                    R[u][3] = __byte_perm(x23, y23, 0x7632);  // dim +3
+                }
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    mma16816<DT>(s.o[2 * c][j], e0, e1, e2, e3, pb[i][j][0], pb[i][j][1]);
-                    mma16816<DT>(s.o[2 * c + 1][j], f0, f1, f2, f3, pb[i][j][0], pb[i][j][1]);
+                    mma_e4m3(s.o[2 * c][j], R[0][0], R[0][1], R[1][0], R[1][1], ph[i0][j], ph[i0 + 1][j]);
+                    mma_e4m3(s.o[2 * c + 1][j], R[0][2], R[0][3], R[1][2], R[1][3], ph[i0][j], ph[i0 + 1][j]);
+                    mma_e4m3(s.o[2 * c][j], R[0][0], R[0][1], R[1][0], R[1][1], pl[i0][j], pl[i0 + 1][j]);
+                    mma_e4m3(s.o[2 * c + 1][j], R[0][2], R[0][3], R[1][2], R[1][3], pl[i0][j], pl[i0 + 1][j]);
                 }
             }
         }
@@ -1059,6 +1144,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int col_end = HP == 1 ? nq : col0 + gh;
     const int rbase = wt * Lt::kRowsPerWarp;
     const float qk = a.qk_scale_log2;
+    // FP8: O accumulates probabilities scaled by kFp8PScale
+    const float vscale = DT == PKV_FP8_E4M3 ? a.v_scale / kFp8PScale : a.v_scale;
     const int bsz = a.block_size;
     const uint32_t half_stride = static_cast<uint32_t>(HP * bsz * kBoxRowBytes);
     // m-tile i of call k: rows rbase+16(k*kCallMT+i).. = block row/bs of the tile, rows row%bs.. of it
@@ -1156,7 +1243,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 float v, M, l;
                 merge_get<NQ, kWT>(mg, n, d, v, M, l);
                 out[out_row<HP>(a, ti.b, ti.h, n, gh) * kD + d] =
-                    __float2bfloat16_rn(l > 0.f ? v * (a.v_scale / l) : 0.f);
+                    __float2bfloat16_rn(l > 0.f ? v * (vscale / l) : 0.f);
             }
         } else if constexpr (!kBal) {
 #pragma unroll 4
@@ -1167,7 +1254,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const size_t prow = HP == 1 ? (static_cast<size_t>(ti.b) * a.num_queries + n / gh) * a.num_q_heads +
                                                   static_cast<size_t>(ti.h) * gh + n % gh
                                             : static_cast<size_t>(ti.b) * a.num_q_heads + static_cast<size_t>(HP * ti.h) * gh + n;
-                a.o_part[(prow * a.num_splits + fsplit) * kD + d] = l > 0.f ? v * (a.v_scale / l) : 0.f;
+                a.o_part[(prow * a.num_splits + fsplit) * kD + d] = l > 0.f ? v * (vscale / l) : 0.f;
                 if (d == 0) a.lse_part[prow * a.num_splits + fsplit] = l > 0.f ? M + log2f(l) : -INFINITY;
             }
         } else {
@@ -1178,7 +1265,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             for (int n = 0; n < nq; ++n) {
                 float v, M, l;
                 merge_get<NQ, kWT>(mg, n, d, v, M, l);
-                a.bal_o[(pbase + n) * kD + d] = l > 0.f ? v * (a.v_scale / l) : 0.f;
+                a.bal_o[(pbase + n) * kD + d] = l > 0.f ? v * (vscale / l) : 0.f;
                 if (d == 0) a.bal_lse[pbase + n] = l > 0.f ? M + log2f(l) : -INFINITY;
             }
             if constexpr (kInStage) release(s);
