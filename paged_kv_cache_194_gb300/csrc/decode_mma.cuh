@@ -153,8 +153,11 @@ struct Layout {
     static constexpr size_t kQOff = static_cast<size_t>(kStages) * kStageBytes;
     static constexpr size_t kInfoOff = kQOff + static_cast<size_t>(kStages) * kQBytes;
     static constexpr size_t kMlOff = kInfoOff + static_cast<size_t>(kStages) * sizeof(TileInfo);
-    static constexpr size_t kMlBytes = (static_cast<size_t>(kWT) * NQ * 2 + 4) * 4;
-    static constexpr size_t kMergeOBytes = static_cast<size_t>(kWT) * NQ * kD * 4;
+    // One consumer warp per KV head (HP heads, one token group): every warp
+    // owns whole rows, so segment ends need no merge area and no CTA-wide sync.
+    static constexpr bool kHeadPerWarp = HP > 1 && kWT == 1;
+    static constexpr size_t kMlBytes = kHeadPerWarp ? 16 : (static_cast<size_t>(kWT) * NQ * 2 + 4) * 4;
+    static constexpr size_t kMergeOBytes = kHeadPerWarp ? 0 : static_cast<size_t>(kWT) * NQ * kD * 4;
     static constexpr size_t kCtl = (2 * kStages + 1) * 8 + 16;  // barriers + abort word
     static constexpr size_t kBase = (kMlOff + kMlBytes + 15) / 16 * 16;
     static constexpr bool kMergeInStage = kBase + kMergeOBytes + kCtl + 1024 > kBudget;
@@ -164,7 +167,8 @@ struct Layout {
     static constexpr size_t kAlloc = kBytes + 1024;  // + alignment slack
     static_assert(kMergeOBytes <= static_cast<size_t>(kStageBytes), "the merge area must fit in a stage");
     static_assert(kNT * 8 * kWC * HP >= NQ && kCalls * kCallMT * 16 == kRowsPerWarp, "warp grid must cover the rows");
-    static_assert(HP == 1 || (HP == 2 && NQ <= 8), "KV-head pairs serve decode only");
+    static_assert(HP == 1 || (HP == 2 && NQ <= 8) || (HP == 4 && kHeadPerWarp && kNQH <= 8),
+                  "several KV heads per CTA serve decode only");
     static_assert(kAlloc <= kBudget, "shared memory budget");
 };
 
@@ -230,6 +234,16 @@ __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+// Two 16x16 E4M3 matrices, transposed: lanes 0-15 give the 16-byte rows of
+// the first, lanes 16-31 those of the second; lane (g, t) = (lane / 4,
+// lane % 4) receives bytes g and g + 8 of rows 4t .. 4t + 3 of each -- the
+// A fragment of mma m16n8k32 for a source stored k-major (rows = k).
+__device__ __forceinline__ void ldsm_x2_t_b8(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr)
                  : "memory");
@@ -329,12 +343,7 @@ __device__ __forceinline__ uint32_t swz(int lr, int chunk) {
 // Head-dim index held by O^T accumulator row `m` (0..15) of m-tile `mt`.
 template <int DT>
 __device__ __forceinline__ int o_dim(int mt, int m) {
-    if constexpr (DT == PKV_BF16) {
-        return mt * 16 + m;
-    } else {  // m-tiles (2j, 2j+1) rows (r, r+8) -> 32j + 4r + {0,1,2,3}
-        const int j = mt >> 1, r = m & 7;
-        return 32 * j + 4 * r + ((mt & 1) << 1) + (m >> 3);
-    }
+    return mt * 16 + m;
 }
 
 // ---------------------------------------------------------------- consumers
@@ -440,7 +449,7 @@ __device__ __forceinline__ void acc_begin(Acc<NT>& s, const __nv_bfloat16* qs, i
 // they depend only on the lane, so they are computed once.
 struct LaneOffsets {
     uint32_t k[4];  // K ldmatrix rows: chunk pair i (BF16: + half * half_stride)
-    uint32_t v[8];  // BF16: V ldmatrix.trans, chunk pair i (4 used); FP8: V bytes, (j, row ta / ta+1)
+    uint32_t v[4];  // BF16: V ldmatrix.trans, chunk pair i; FP8: v[0] = byte offset of this lane's V row, v[1] = its swizzle phase
 };
 
 template <int DT>
@@ -453,16 +462,14 @@ __device__ __forceinline__ LaneOffsets lane_offsets(int lane) {
         const int trow = (lane & 7) + ((lane >> 4) & 1) * 8;
 #pragma unroll
         for (int i = 0; i < 4; ++i) o.v[i] = swz(trow, 2 * i + ((lane >> 3) & 1));
-#pragma unroll
-        for (int i = 4; i < 8; ++i) o.v[i] = 0;
     } else {
-        const int r = lane >> 2, q = lane & 3;
-        const uint32_t inner = static_cast<uint32_t>((r & 3) * 4);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            o.v[2 * j] = swz(2 * q, 2 * j + (r >> 2)) + inner;
-            o.v[2 * j + 1] = swz(2 * q + 1, 2 * j + (r >> 2)) + inner;
-        }
+        // V rows for ldsm_x2_t_b8: source row i (= k-slot i) of an m-tile is
+        // token 2(i/4) + (i%4 & 1) + 8 (i%4 >> 1), the order P's B fragments
+        // use (see consume_tile); lanes 16-31 address the second m-tile.
+        const int i = lane & 15, row = 2 * (i >> 2) + (i & 1) + 8 * ((i & 3) >> 1);
+        o.v[0] = static_cast<uint32_t>(row * kBoxRowBytes);
+        o.v[1] = static_cast<uint32_t>(row & 7);
+        o.v[2] = o.v[3] = 0;
     }
     return o;
 }
@@ -669,40 +676,23 @@ __device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* 
                 pl[i][j] = lo0 | (lo1 << 16);
             }
         }
-        // V^T A fragments: thread (r, q) reads the 4-byte word of head dims
-        // 32c + 4r .. +3 of tokens 2q, 2q+1, 2q+8, 2q+9 and transposes the 4x4
-        // bytes: dim 32c + 4r + i of those tokens is m-tile 2c (i = 0, 1: rows r,
-        // r+8) or 2c+1 (i = 2, 3) of O^T (see o_dim).
+        // V^T A fragments straight from the staged rows: one transposing
+        // ldmatrix per 16 head dims (O^T m-tile c) and k32 step; the source rows
+        // follow the k-slot order above (lo.v[0]); a dead second m-tile's
+        // stale rows are replaced by zeros.
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int i0 = 0; i0 < MT; i0 += 2) {
+            if (!live[i0]) continue;
+            const uint32_t vrow = vb0 + (lane < 16 ? wb[i0] : wb[i0 + 1]) + lo.v[0];
 #pragma unroll
-            for (int i0 = 0; i0 < MT; i0 += 2) {
-                if (!live[i0]) continue;
-                uint32_t R[2][4];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    if (u == 1 && !live[i0 + 1]) {
-                        R[1][0] = R[1][1] = R[1][2] = R[1][3] = 0u;
-                        continue;
-                    }
-                    const uint32_t vb_ = vb0 + wb[i0 + u];
-                    const uint32_t w0 = lds32(vb_ + lo.v[2 * c]);                         // token 2q
-                    const uint32_t w1 = lds32(vb_ + lo.v[2 * c + 1]);                     // token 2q+1
-                    const uint32_t w2 = lds32<8 * kBoxRowBytes>(vb_ + lo.v[2 * c]);       // token 2q+8
-                    const uint32_t w3 = lds32<8 * kBoxRowBytes>(vb_ + lo.v[2 * c + 1]);   // token 2q+9
-                    const uint32_t x01 = __byte_perm(w0, w1, 0x5140), x23 = __byte_perm(w0, w1, 0x7362);
-                    const uint32_t y01 = __byte_perm(w2, w3, 0x5140), y23 = __byte_perm(w2, w3, 0x7362);
-                    R[u][0] = __byte_perm(x01, y01, 0x5410);  // dim +0 of the 4 tokens
-                    R[u][1] = __byte_perm(x01, y01, 0x7632);  // dim +1
-                    R[u][2] = __byte_perm(x23, y23, 0x5410);  // dim +2
-                    R[u][3] = __byte_perm(x23, y23, 0x7632);  // dim +3
-                }
+            for (int c = 0; c < 8; ++c) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x2_t_b8(vrow + ((static_cast<uint32_t>(c) ^ lo.v[1]) << 4), a0, a1, a2, a3);
+                if (!live[i0 + 1]) a2 = a3 = 0u;
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    mma_e4m3(s.o[2 * c][j], R[0][0], R[0][1], R[1][0], R[1][1], ph[i0][j], ph[i0 + 1][j]);
-                    mma_e4m3(s.o[2 * c + 1][j], R[0][2], R[0][3], R[1][2], R[1][3], ph[i0][j], ph[i0 + 1][j]);
-                    mma_e4m3(s.o[2 * c][j], R[0][0], R[0][1], R[1][0], R[1][1], pl[i0][j], pl[i0 + 1][j]);
-                    mma_e4m3(s.o[2 * c + 1][j], R[0][2], R[0][3], R[1][2], R[1][3], pl[i0][j], pl[i0 + 1][j]);
+                    mma_e4m3(s.o[c][j], a0, a1, a2, a3, ph[i0][j], ph[i0 + 1][j]);
+                    mma_e4m3(s.o[c][j], a0, a1, a2, a3, pl[i0][j], pl[i0 + 1][j]);
                 }
             }
         }
@@ -792,6 +782,137 @@ __device__ __forceinline__ size_t out_row(const DecodeArgs& a, int b, int h, int
         return (static_cast<size_t>(b) * a.q_total + a.q_first) * a.num_q_heads + static_cast<size_t>(HP * h) * gh + n;
 }
 
+// Segment end when each consumer warp owns one KV head of the unit (HP
+// heads per CTA, decode): the warp emits its own gh rows straight from its
+// registers -- a whole unit to the output, a piece of a shared (sequence, KV
+// head) to the workspace, and the warp that publishes a head's last piece
+// merges that head -- with no CTA-wide synchronisation, so the other warps
+// go on consuming.  Lane (r, q) holds columns col0 + 2q, +1 (rows r, r + 8 of
+// each O^T m-tile); vscale / l turns O into the normalised output.
+template <int DT, int NQ, bool kBal, int HP>
+__device__ __forceinline__ void head_epilogue(const DecodeArgs& a, const Acc<1>& s, const TileInfo& ti, int hp,
+                                              int col0, int col_end, int gh, int lane, float vscale, int fsplit) {
+    constexpr int kRows = NQ / HP;  // row bound of one head
+    const int r = lane >> 2, q = lane & 3;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    float inv[2], lse[2];
+    int n[2];
+    bool ok[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float l = s.l[0][h];
+        l += __shfl_xor_sync(0xFFFFFFFFu, l, 4);
+        l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
+        l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+        n[h] = col0 + 2 * q + h;
+        ok[h] = n[h] < col_end;
+        inv[h] = l > 0.f ? vscale / l : 0.f;
+        lse[h] = l > 0.f ? s.m[0][h] + log2f(l) : -INFINITY;
+    }
+    if (ti.flags & kSegWhole) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (!ok[h]) continue;
+            __nv_bfloat16* row = out + out_row<HP>(a, ti.b, ti.h, n[h], gh) * kD;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                row[o_dim<DT>(mt, r)] = __float2bfloat16_rn(s.o[mt][0][h] * inv[h]);
+                row[o_dim<DT>(mt, r + 8)] = __float2bfloat16_rn(s.o[mt][0][2 + h] * inv[h]);
+            }
+        }
+        return;
+    }
+    if constexpr (!kBal) {  // fixed splits: this split's partial rows
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (!ok[h]) continue;
+            const size_t prow = static_cast<size_t>(ti.b) * a.num_q_heads + static_cast<size_t>(HP * ti.h) * gh + n[h];
+            float* dst = a.o_part + (prow * a.num_splits + fsplit) * kD;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                dst[o_dim<DT>(mt, r)] = s.o[mt][0][h] * inv[h];
+                dst[o_dim<DT>(mt, r + 8)] = s.o[mt][0][2 + h] * inv[h];
+            }
+            if (r == 0) a.lse_part[prow * a.num_splits + fsplit] = lse[h];
+        }
+        return;
+    } else {
+        // a piece of a shared (sequence, KV head): O / l and the log-sum-exp
+        const int slot = (ti.flags & kCtaFirst) ? 0 : 1;
+        const size_t pbase = (static_cast<size_t>(blockIdx.x) * 2 + slot) * NQ;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (!ok[h]) continue;
+            float* dst = a.bal_o + (pbase + n[h]) * kD;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                dst[o_dim<DT>(mt, r)] = s.o[mt][0][h] * inv[h];
+                dst[o_dim<DT>(mt, r + 8)] = s.o[mt][0][2 + h] * inv[h];
+            }
+            if (r == 0) a.bal_lse[pbase + n[h]] = lse[h];
+        }
+        // Publish: every lane's writes are fenced, then one GPU-scope acq_rel
+        // atomic on this head's counter counts the piece (and, for the last one,
+        // orders the other pieces' writes before the reads below).
+        __threadfence();
+        __syncwarp();
+        int* counter = a.counters + static_cast<size_t>(ti.b) * a.num_kv_heads + HP * ti.h + hp;
+        int last = 0;
+        if (lane == 0) last = atom_add_acq_rel(counter, 1) == ti.pieces - 1 ? 1 : 0;
+        last = __shfl_sync(0xFFFFFFFFu, last, 0);
+        if (!last) return;
+        __threadfence();
+        // every piece is published: merge this head's rows, lane = 4-float
+        // chunk of head_dim, one online log-sum-exp merge per row; the loads of
+        // a piece are independent of the previous piece's arithmetic
+        const int rows = col_end - col0;
+        float M[kRows], z[kRows];
+        float4 acc[kRows];
+#pragma unroll
+        for (int g = 0; g < kRows; ++g) {
+            M[g] = -INFINITY;
+            z[g] = 0.f;
+            acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll 2
+        for (int j = 0; j < ti.pieces; ++j) {
+            const size_t pb = (static_cast<size_t>(ti.c_first + j) * 2 + (j == 0 ? ti.s_first : 0)) * NQ + col0;
+            float lj[kRows];
+            float4 o4[kRows];
+#pragma unroll
+            for (int g = 0; g < kRows; ++g) {
+                if (g >= rows) continue;
+                lj[g] = __ldcg(a.bal_lse + pb + g);
+                o4[g] = __ldcg(reinterpret_cast<const float4*>(a.bal_o + (pb + g) * kD) + lane);
+            }
+#pragma unroll
+            for (int g = 0; g < kRows; ++g) {
+                if (g >= rows || lj[g] == -INFINITY) continue;  // a piece with no token for this row
+                const float Mn = fmaxf(M[g], lj[g]);
+                const float sc = exp2f(M[g] - Mn), w = exp2f(lj[g] - Mn);
+                z[g] = z[g] * sc + w;
+                acc[g].x = fmaf(w, o4[g].x, acc[g].x * sc);
+                acc[g].y = fmaf(w, o4[g].y, acc[g].y * sc);
+                acc[g].z = fmaf(w, o4[g].z, acc[g].z * sc);
+                acc[g].w = fmaf(w, o4[g].w, acc[g].w * sc);
+                M[g] = Mn;
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < kRows; ++g) {
+            if (g >= rows) continue;
+            const float iz = z[g] > 0.f ? 1.f / z[g] : 0.f;
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[g].x * iz, acc[g].y * iz);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[g].z * iz, acc[g].w * iz);
+            uint2 pk;
+            pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(out + out_row<HP>(a, ti.b, ti.h, col0 + g, gh) * kD + 4 * lane) = pk;
+        }
+        if (lane == 0) *counter = 0;  // ready for the next call
+    }
+}
+
 // Fused append (decode), done by the producer warp: the rows [K, V] x [HP
 // heads] x [chunks] of a unit's newest token, lane `lane` owning output chunks
 // lane + 32 j.  prefetch() issues the input loads when a segment that ends
@@ -846,14 +967,23 @@ struct NewRows {
 };
 
 // ---------------------------------------------------------------- producer
+// The pool block ids of tile ti, one per lane (lane k: block k of the tile;
+// -1 past the tile).  The producer loads them before it waits for a free
+// stage, so the block table's latency overlaps that wait.
+__device__ __forceinline__ int tile_blocks(const DecodeArgs& a, const int32_t* table, const TileInfo& ti, int lane) {
+    const int bs = a.block_size;
+    const int nblk = (ti.n + bs - 1) / bs;  // <= 32 (a tile holds at most 128 tokens)
+    const int j = ti.tok0 / bs + lane;
+    return (lane < nblk && j < a.max_blocks) ? __ldg(table + j) : -1;
+}
+
 // Stage s <- tile ti: tile info, the query rows at a segment's first tile,
 // and one TMA box per KV block (K and V).  All 32 producer lanes call it
-// (they share the block-table window); lane 0 issues.
+// (lane k holds block k's id, from tile_blocks); lane 0 issues.
 template <int DT, int NQ, int HP>
 __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
-                                            uint8_t* smem, uint64_t* full, int s, const TileInfo& ti,
-                                            const int32_t* table, int& cache, int& cache_base, int lane, int gh,
-                                            NewRows<DT, HP>& nr, bool append) {
+                                            uint8_t* smem, uint64_t* full, int s, const TileInfo& ti, int myblk,
+                                            int lane, int gh, NewRows<DT, HP>& nr, bool append) {
     using Lt = Layout<DT, NQ, HP>;
     const int bs = a.block_size;
     uint8_t* kst = smem + s * Lt::kStageBytes;
@@ -882,13 +1012,7 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorM
     }
     const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
     for (int k = 0; k < nblk; ++k) {
-        const int j = ti.tok0 / bs + k;  // block index within the sequence
-        if (cache_base < 0 || j - cache_base >= 32 || j < cache_base) {
-            cache_base = j & ~31;
-            const int idx = cache_base + lane;
-            cache = idx < a.max_blocks ? table[idx] : -1;
-        }
-        int blk = __shfl_sync(0xFFFFFFFFu, cache, j - cache_base);
+        int blk = __shfl_sync(0xFFFFFFFFu, myblk, k);
         if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks)) {
             if (lane == 0 && a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
             blk = 0;  // read an in-bounds block; the flag marks the output invalid
@@ -992,7 +1116,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
     if (warp == kCWarps) {
         // ------------------------------------------------------------ producer
-        int cache = -1, cache_base = -1;
         long long k = 0;  // stages issued
         bool ok = true;
         auto acquire = [&](long long kk) -> int {  // stage for the kk-th issue, after it is free
@@ -1045,11 +1168,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 NewRows<DT, HP> nr;
                 bool app = false;  // this CTA appends the current unit's newest token
                 for (long long g = g0; g < g1 && ok; ++g, ++k) {
-                    const int s = acquire(k);
-                    if (!ok) break;
                     const long long pstart = cum + static_cast<long long>(h) * nt, pend = pstart + nt;
                     if (g == g0 || t == 0) {  // a new segment: who shares this (sequence, KV head)
-                        if constexpr (NQ <= 8) {  // fused append: the segment holds the unit's last tile
+                        if constexpr (NQ <= 8 || HP > 1) {  // fused append: the segment holds the unit's last tile
                             app = a.new_k != nullptr && pend <= g1 && a.lens[b] == L;
                             if (app) nr.prefetch(a, b, h, lane);
                         }
@@ -1066,8 +1187,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     ti.flags = ((g == g0 || t == 0) ? kSegFirst : 0) | ((g == g1 - 1 || t == nt - 1) ? kSegLast : 0) |
                                ((pstart >= g0 && pend <= g1) ? kSegWhole : 0) | (pstart <= g0 ? kCtaFirst : 0) |
                                (g == g1 - 1 ? kCtaLast : 0);
-                    issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh, nr,
-                                            app && t == nt - 1);
+                    const int myblk = tile_blocks(a, table, ti, lane);
+                    const int s = acquire(k);
+                    if (!ok) break;
+                    issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, myblk, lane, gh, nr, app && t == nt - 1);
                     if (++t == nt) {  // next (sequence, KV head)
                         t = 0;
                         if (++h == Hkv) {
@@ -1082,7 +1205,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                             if (b < B) {
                                 nt = (L + kTT - 1) / kTT;
                                 table = a.tables + static_cast<size_t>(b) * a.max_blocks;
-                                cache_base = -1;
                             }
                         }
                     }
@@ -1093,13 +1215,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             const int ntiles = (t_end - t_begin + kTT - 1) / kTT;
             NewRows<DT, HP> nr;
             bool app = false;
-            if constexpr (NQ <= 8) {  // fused append: this split holds the newest position
+            if constexpr (NQ <= 8 || HP > 1) {  // fused append: this split holds the newest position
                 app = a.new_k != nullptr && t_end == fL && a.lens[fb_] == fL;
                 if (app) nr.prefetch(a, fb_, fh_, lane);
             }
             for (int t = 0; t < ntiles && ok; ++t, ++k) {
-                const int s = acquire(k);
-                if (!ok) break;
                 TileInfo ti;
                 ti.b = fb_;
                 ti.h = fh_;
@@ -1111,8 +1231,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 ti.pieces = 1;
                 ti.c_first = 0;
                 ti.s_first = 0;
-                issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, table, cache, cache_base, lane, gh, nr,
-                                        app && t == ntiles - 1);
+                const int myblk = tile_blocks(a, table, ti, lane);
+                const int s = acquire(k);
+                if (!ok) break;
+                issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, myblk, lane, gh, nr, app && t == ntiles - 1);
             }
         }
         if (ok && k == 0) {  // a CTA without tiles: tell the consumers
@@ -1197,6 +1319,17 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
     };
 
+    if constexpr (kBal) {
+        // zero the rows of sequences with nothing visible (and report bad
+        // lengths once), while the first tiles are in flight
+        const int per_seq = a.num_queries * a.num_q_heads;
+        for (int b = blockIdx.x; b < a.num_seqs; b += gridDim.x) {
+            if (visible_len(a, b, threadIdx.x == 0) == 0) {
+                __nv_bfloat16* o = out + (static_cast<size_t>(b) * a.q_total + a.q_first) * a.num_q_heads * kD;
+                for (int i = threadIdx.x; i < per_seq * kD; i += kCWarps * 32) o[i] = __float2bfloat16_rn(0.f);
+            }
+        }
+    }
     // test hook: this CTA's first stage wait may be cut short (an expired wait on demand)
     const bool short_first = a.test_wait_on != 0 && (a.test_wait_cta < 0 || a.test_wait_cta == cta_linear());
     for (long long k = 0;; ++k) {
@@ -1229,6 +1362,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const bool seg_last = (ti.flags & kSegLast) != 0;
         if (!kInStage || !seg_last) release(s);
         if (!seg_last) continue;
+        if constexpr (Lt::kHeadPerWarp) {
+            head_epilogue<DT, NQ, kBal, HP>(a, acc, ti, hp, col0, col_end, gh, lane, vscale, fsplit);
+            if (ti.flags & kCtaLast) break;
+            continue;
+        } else {
 
         // ---- segment end: merge the token groups, emit
         if constexpr (kInStage) {  // the stage becomes the merge area once every warp is done reading it
@@ -1350,15 +1488,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             if (!csync()) break;  // the dedicated merge area is reused by the next segment
         }
         if (ti.flags & kCtaLast) break;
-    }
-    if (aborted || *abort_flag) return;
-    if constexpr (kBal) {  // zero the rows of sequences with nothing visible (and report bad lengths once)
-        const int per_seq = a.num_queries * a.num_q_heads;
-        for (int b = blockIdx.x; b < a.num_seqs; b += gridDim.x) {
-            if (visible_len(a, b, threadIdx.x == 0) == 0) {
-                __nv_bfloat16* o = out + (static_cast<size_t>(b) * a.q_total + a.q_first) * a.num_q_heads * kD;
-                for (int i = threadIdx.x; i < per_seq * kD; i += kCWarps * 32) o[i] = __float2bfloat16_rn(0.f);
-            }
         }
     }
 }
@@ -1410,6 +1539,13 @@ template <int DT, bool kBal>
 cudaError_t launch_rows(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
     const int rows = a.num_queries * (a.num_q_heads / a.num_kv_heads);
     if constexpr (DT == PKV_BF16) {
+        if (a.heads_per_cta == 4) {  // four KV heads, one consumer warp each: 4 * rows columns
+            if (a.num_queries != 1 || a.num_kv_heads % 4 != 0) return cudaErrorNotSupported;
+            if (rows <= 1) return launch_nq<DT, 4, kBal, 4>(a, tk, tv, stream);
+            if (rows <= 2) return launch_nq<DT, 8, kBal, 4>(a, tk, tv, stream);
+            if (rows <= 4) return launch_nq<DT, 16, kBal, 4>(a, tk, tv, stream);
+            return cudaErrorNotSupported;
+        }
         if (a.heads_per_cta == 2) {  // a KV-head pair: 2 * rows columns
             if (a.num_queries != 1 || a.num_kv_heads % 2 != 0) return cudaErrorNotSupported;
             if (rows <= 1) return launch_nq<DT, 2, kBal, 2>(a, tk, tv, stream);

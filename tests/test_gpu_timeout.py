@@ -94,7 +94,11 @@ def test_every_cta_gives_up(kv):
     out, dt = _call(w, batch, q, tables, lens, max_len, 0, ws, polls=0, cta=-1)
     assert dt < 5.0
     assert batch.pool.errors() & pk.ERRBIT_TIMEOUT
-    assert torch.isnan(out.float()).all()  # nothing was written
+    # nothing was written except the zero rows of the empty sequence, which
+    # every launch writes before its pipeline starts
+    empty = torch.tensor([L == 0 for L in LENS])
+    assert torch.all(out[empty] == 0)
+    assert torch.isnan(out[~empty].float()).all()
     assert int(ws[:4 * w.num_seqs * w.num_kv_heads].count_nonzero()) == 0  # no piece was published
     batch.pool.clear_errors()
     out2, _ = _call(w, batch, q, tables, lens, max_len, 0, ws)
