@@ -82,14 +82,11 @@ bool tc_balanced(int num_seqs, int num_kv_heads, int64_t rows) {
            static_cast<int64_t>(num_seqs) * num_kv_heads < bal_ctas();
 }
 // Rows of one balanced-schedule partial slot: the template row bound of the
-// largest launch (for decode, the 2 or 4 KV heads of a CTA: 2 * gh rows
-// bound by 8, or 4 x the bound of gh).
+// largest launch (a KV-head pair's 2 * gh rows for decode).
 int bal_rows(int gh, int C) {
-    int r = row_bound(mma_chunk(gh, C) * gh);
+    const int r = row_bound(mma_chunk(gh, C) * gh);
     const int pair = (C == 1 && 2 * gh <= 8) ? row_bound(2 * gh) : 0;
-    const int quad = (C == 1 && gh <= 4) ? 4 * row_bound(gh) : 0;
-    if (pair > r) r = pair;
-    return quad > r ? quad : r;
+    return r > pair ? r : pair;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -169,21 +166,6 @@ bool ensure_tmaps(pkv_pool* p) {
                     ok2 = r == CUDA_SUCCESS;
                 }
                 p->tmap_pair = ok2 ? 1 : 0;
-            }
-            // Boxes of four adjacent KV heads of a block: 16 KB per box at
-            // 16-token blocks, one box per tensor and pipeline stage.
-            p->tmap_quad = 0;
-            if (d.block_size == 16 && d.num_kv_heads % 4 == 0) {
-                const cuuint32_t box4[3] = {64, static_cast<cuuint32_t>(4 * d.block_size), 2};
-                bool ok4 = true;
-                for (int i = 0; i < 2 && ok4; ++i) {
-                    CUresult r = enc(i == 0 ? &p->tmap_k4 : &p->tmap_v4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                                     i == 0 ? d.k_base : d.v_base, dims3, strides3, box4, estr3,
-                                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-                    ok4 = r == CUDA_SUCCESS;
-                }
-                p->tmap_quad = ok4 ? 1 : 0;
             }
             return true;
         }
@@ -505,17 +487,13 @@ pkv_status attention_call(const void* q, pkv_dtype q_dtype, const pkv_pool* p, i
             a.lse_part = reinterpret_cast<float*>(body + round_up(rows * p->d.head_dim * sizeof(float), 256));
         }
     }
-    // Decode on BF16 pools of 16-token blocks: one CTA serves four adjacent
-    // KV heads, one consumer warp each, so a block of all four arrives as one
-    // 16 KB box and segment ends need no CTA-wide merge; two heads (8 KB
-    // boxes) when the KV-head count is not a multiple of 4 or the group is
-    // larger.  (Per-box cost dominates at 4 KB.)
-    const bool dec16 = use_mma && num_queries == 1 && p->tmap_3d == 1;
-    const bool quad = dec16 && p->tmap_quad == 1 && gh <= 4;
-    const bool pair = !quad && dec16 && p->tmap_pair == 1 && 2 * gh <= 8;
-    a.heads_per_cta = quad ? 4 : (pair ? 2 : 1);
-    const void* tk = quad ? &p->tmap_k4 : (pair ? &p->tmap_k2 : &p->tmap_k);
-    const void* tv = quad ? &p->tmap_v4 : (pair ? &p->tmap_v2 : &p->tmap_v);
+    // Decode on BF16 pools of 16-token blocks: one CTA serves two adjacent KV
+    // heads, so each block arrives as one 8 KB box instead of two 4 KB ones
+    // (per-box cost dominates at 4 KB).
+    const bool pair = use_mma && num_queries == 1 && p->tmap_pair == 1 && p->tmap_3d == 1 && 2 * gh <= 8;
+    a.heads_per_cta = pair ? 2 : 1;
+    const void* tk = pair ? &p->tmap_k2 : &p->tmap_k;
+    const void* tv = pair ? &p->tmap_v2 : &p->tmap_v;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (use_tc) {  // the balanced schedule (bal_max_ctas > 0) or one CTA per row tile
         a.heads_per_cta = 1;

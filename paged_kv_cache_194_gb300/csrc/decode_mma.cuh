@@ -153,11 +153,8 @@ struct Layout {
     static constexpr size_t kQOff = static_cast<size_t>(kStages) * kStageBytes;
     static constexpr size_t kInfoOff = kQOff + static_cast<size_t>(kStages) * kQBytes;
     static constexpr size_t kMlOff = kInfoOff + static_cast<size_t>(kStages) * sizeof(TileInfo);
-    // One consumer warp per KV head (HP heads, one token group): every warp
-    // owns whole rows, so segment ends need no merge area and no CTA-wide sync.
-    static constexpr bool kHeadPerWarp = HP > 1 && kWT == 1;
-    static constexpr size_t kMlBytes = kHeadPerWarp ? 16 : (static_cast<size_t>(kWT) * NQ * 2 + 4) * 4;
-    static constexpr size_t kMergeOBytes = kHeadPerWarp ? 0 : static_cast<size_t>(kWT) * NQ * kD * 4;
+    static constexpr size_t kMlBytes = (static_cast<size_t>(kWT) * NQ * 2 + 4) * 4;
+    static constexpr size_t kMergeOBytes = static_cast<size_t>(kWT) * NQ * kD * 4;
     static constexpr size_t kCtl = (2 * kStages + 1) * 8 + 16;  // barriers + abort word
     static constexpr size_t kBase = (kMlOff + kMlBytes + 15) / 16 * 16;
     static constexpr bool kMergeInStage = kBase + kMergeOBytes + kCtl + 1024 > kBudget;
@@ -167,8 +164,7 @@ struct Layout {
     static constexpr size_t kAlloc = kBytes + 1024;  // + alignment slack
     static_assert(kMergeOBytes <= static_cast<size_t>(kStageBytes), "the merge area must fit in a stage");
     static_assert(kNT * 8 * kWC * HP >= NQ && kCalls * kCallMT * 16 == kRowsPerWarp, "warp grid must cover the rows");
-    static_assert(HP == 1 || (HP == 2 && NQ <= 8) || (HP == 4 && kHeadPerWarp && kNQH <= 8),
-                  "several KV heads per CTA serve decode only");
+    static_assert(HP == 1 || (HP == 2 && NQ <= 8), "KV-head pairs serve decode only");
     static_assert(kAlloc <= kBudget, "shared memory budget");
 };
 
@@ -329,9 +325,9 @@ __device__ __forceinline__ void split_e4m3x2(uint32_t x, uint32_t& hi, uint32_t&
     hi = static_cast<uint32_t>(h);
     lo = static_cast<uint32_t>(l);
 }
-// Probabilities enter the E4M3 MMA scaled by 2^8 (they are <= 1; E4M3 holds
-// up to 448), undone in the output scale.
-constexpr float kFp8PScale = 256.f;
+// Probabilities enter the E4M3 MMA scaled by 2^kFp8PLog2 (they are <= 1;
+// E4M3 holds up to 448).
+constexpr float kFp8PLog2 = 8.f;
 
 // Byte offset of 16-byte chunk `chunk` of row `lr` inside a 128B-swizzled run
 // of rows whose first row sits on a 1024-byte boundary (and is a multiple of 8
@@ -528,11 +524,15 @@ __device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* 
         // one ldmatrix.x4 = the E4M3 A fragment of a k32 step (bytes 32 kp ..
         // 32 kp + 31 of 16 token rows); hi and lo query terms accumulate apart
         // (two independent chains) and are summed after the last step
-        float sl[MT][NT][4];
+        // four independent accumulator chains per m-tile: hi / lo terms x
+        // head-dim halves (each two k32 steps long)
+        float sl[MT][NT][4], sc2[MT][NT][4], sl2[MT][NT][4];
 #pragma unroll
         for (int i = 0; i < MT; ++i)
 #pragma unroll
-            for (int j = 0; j < NT; ++j) sl[i][j][0] = sl[i][j][1] = sl[i][j][2] = sl[i][j][3] = 0.f;
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sl[i][j][c] = sc2[i][j][c] = sl2[i][j][c] = 0.f;
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
 #pragma unroll
@@ -542,8 +542,9 @@ __device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* 
                 ldsm_x4(kb + wb[i] + lo.k[kp], r0, r1, r2, r3);
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    mma_e4m3(sc[i][j], r0, r1, r2, r3, s.bq[2 * kp][j][0], s.bq[2 * kp][j][1]);
-                    mma_e4m3(sl[i][j], r0, r1, r2, r3, s.bq[2 * kp + 1][j][0], s.bq[2 * kp + 1][j][1]);
+                    mma_e4m3(kp < 2 ? sc[i][j] : sc2[i][j], r0, r1, r2, r3, s.bq[2 * kp][j][0], s.bq[2 * kp][j][1]);
+                    mma_e4m3(kp < 2 ? sl[i][j] : sl2[i][j], r0, r1, r2, r3, s.bq[2 * kp + 1][j][0],
+                             s.bq[2 * kp + 1][j][1]);
                 }
             }
         }
@@ -552,8 +553,12 @@ __device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* 
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) sc[i][j][c] += sl[i][j][c];
+                for (int c = 0; c < 4; ++c) sc[i][j][c] = (sc[i][j][c] + sl[i][j][c]) + (sc2[i][j][c] + sl2[i][j][c]);
     }
+    // FP8: probabilities (and with them l and O) carry a factor 2^kPLog2, so
+    // that they fill E4M3's range (they are <= 1 before it; E4M3 holds up to
+    // 448); it cancels in O / l and is taken out of each log-sum-exp.
+    constexpr float kPLog2 = DT == PKV_FP8_E4M3 ? kFp8PLog2 : 0.f;
     // ---- online softmax (log2 domain) over the step's 16*MT rows, per column
     float sv[MT][NT][4];
     float x[NT][2];
@@ -597,10 +602,10 @@ __device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* 
     for (int i = 0; i < MT; ++i) {
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-            p[i][j][0] = exp2f(sv[i][j][0] - bb[j][0]);
-            p[i][j][1] = exp2f(sv[i][j][1] - bb[j][1]);
-            p[i][j][2] = exp2f(sv[i][j][2] - bb[j][0]);
-            p[i][j][3] = exp2f(sv[i][j][3] - bb[j][1]);
+            p[i][j][0] = exp2f(sv[i][j][0] - bb[j][0] + kPLog2);
+            p[i][j][1] = exp2f(sv[i][j][1] - bb[j][1] + kPLog2);
+            p[i][j][2] = exp2f(sv[i][j][2] - bb[j][0] + kPLog2);
+            p[i][j][3] = exp2f(sv[i][j][3] - bb[j][1] + kPLog2);
         }
     }
     // rescale only when some running max moved (the factor is exactly 1
@@ -660,18 +665,15 @@ __device__ __forceinline__ void consume_tile(Acc<NT>& s, uint8_t* kst, uint8_t* 
         // pairs the right token); a k32 step covers m-tiles (i, i+1).
         // P^T (scaled by 2^8) as hi / lo E4M3 B fragments per m-tile
         uint32_t ph[MT][NT], pl[MT][NT];
-        const __half2 ps = __float2half2_rn(kFp8PScale);
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 uint32_t t0 = movmatrix_t(pack2<DT>(p[i][j][0], p[i][j][1]));  // (column r; tokens 2q, 2q+1)
                 uint32_t t1 = movmatrix_t(pack2<DT>(p[i][j][2], p[i][j][3]));  // (column r; tokens 2q+8, 2q+9)
-                __half2 h0 = __hmul2(*reinterpret_cast<__half2*>(&t0), ps);
-                __half2 h1 = __hmul2(*reinterpret_cast<__half2*>(&t1), ps);
                 uint32_t hi0, lo0, hi1, lo1;
-                split_e4m3x2(*reinterpret_cast<uint32_t*>(&h0), hi0, lo0);
-                split_e4m3x2(*reinterpret_cast<uint32_t*>(&h1), hi1, lo1);
+                split_e4m3x2(t0, hi0, lo0);
+                split_e4m3x2(t1, hi1, lo1);
                 ph[i][j] = hi0 | (hi1 << 16);
                 pl[i][j] = lo0 | (lo1 << 16);
             }
@@ -780,137 +782,6 @@ __device__ __forceinline__ size_t out_row(const DecodeArgs& a, int b, int h, int
                static_cast<size_t>(h) * gh + n % gh;
     else
         return (static_cast<size_t>(b) * a.q_total + a.q_first) * a.num_q_heads + static_cast<size_t>(HP * h) * gh + n;
-}
-
-// Segment end when each consumer warp owns one KV head of the unit (HP
-// heads per CTA, decode): the warp emits its own gh rows straight from its
-// registers -- a whole unit to the output, a piece of a shared (sequence, KV
-// head) to the workspace, and the warp that publishes a head's last piece
-// merges that head -- with no CTA-wide synchronisation, so the other warps
-// go on consuming.  Lane (r, q) holds columns col0 + 2q, +1 (rows r, r + 8 of
-// each O^T m-tile); vscale / l turns O into the normalised output.
-template <int DT, int NQ, bool kBal, int HP>
-__device__ __forceinline__ void head_epilogue(const DecodeArgs& a, const Acc<1>& s, const TileInfo& ti, int hp,
-                                              int col0, int col_end, int gh, int lane, float vscale, int fsplit) {
-    constexpr int kRows = NQ / HP;  // row bound of one head
-    const int r = lane >> 2, q = lane & 3;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    float inv[2], lse[2];
-    int n[2];
-    bool ok[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        float l = s.l[0][h];
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 4);
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 8);
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 16);
-        n[h] = col0 + 2 * q + h;
-        ok[h] = n[h] < col_end;
-        inv[h] = l > 0.f ? vscale / l : 0.f;
-        lse[h] = l > 0.f ? s.m[0][h] + log2f(l) : -INFINITY;
-    }
-    if (ti.flags & kSegWhole) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (!ok[h]) continue;
-            __nv_bfloat16* row = out + out_row<HP>(a, ti.b, ti.h, n[h], gh) * kD;
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                row[o_dim<DT>(mt, r)] = __float2bfloat16_rn(s.o[mt][0][h] * inv[h]);
-                row[o_dim<DT>(mt, r + 8)] = __float2bfloat16_rn(s.o[mt][0][2 + h] * inv[h]);
-            }
-        }
-        return;
-    }
-    if constexpr (!kBal) {  // fixed splits: this split's partial rows
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (!ok[h]) continue;
-            const size_t prow = static_cast<size_t>(ti.b) * a.num_q_heads + static_cast<size_t>(HP * ti.h) * gh + n[h];
-            float* dst = a.o_part + (prow * a.num_splits + fsplit) * kD;
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                dst[o_dim<DT>(mt, r)] = s.o[mt][0][h] * inv[h];
-                dst[o_dim<DT>(mt, r + 8)] = s.o[mt][0][2 + h] * inv[h];
-            }
-            if (r == 0) a.lse_part[prow * a.num_splits + fsplit] = lse[h];
-        }
-        return;
-    } else {
-        // a piece of a shared (sequence, KV head): O / l and the log-sum-exp
-        const int slot = (ti.flags & kCtaFirst) ? 0 : 1;
-        const size_t pbase = (static_cast<size_t>(blockIdx.x) * 2 + slot) * NQ;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (!ok[h]) continue;
-            float* dst = a.bal_o + (pbase + n[h]) * kD;
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                dst[o_dim<DT>(mt, r)] = s.o[mt][0][h] * inv[h];
-                dst[o_dim<DT>(mt, r + 8)] = s.o[mt][0][2 + h] * inv[h];
-            }
-            if (r == 0) a.bal_lse[pbase + n[h]] = lse[h];
-        }
-        // Publish: every lane's writes are fenced, then one GPU-scope acq_rel
-        // atomic on this head's counter counts the piece (and, for the last one,
-        // orders the other pieces' writes before the reads below).
-        __threadfence();
-        __syncwarp();
-        int* counter = a.counters + static_cast<size_t>(ti.b) * a.num_kv_heads + HP * ti.h + hp;
-        int last = 0;
-        if (lane == 0) last = atom_add_acq_rel(counter, 1) == ti.pieces - 1 ? 1 : 0;
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        if (!last) return;
-        __threadfence();
-        // every piece is published: merge this head's rows, lane = 4-float
-        // chunk of head_dim, one online log-sum-exp merge per row; the loads of
-        // a piece are independent of the previous piece's arithmetic
-        const int rows = col_end - col0;
-        float M[kRows], z[kRows];
-        float4 acc[kRows];
-#pragma unroll
-        for (int g = 0; g < kRows; ++g) {
-            M[g] = -INFINITY;
-            z[g] = 0.f;
-            acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll 2
-        for (int j = 0; j < ti.pieces; ++j) {
-            const size_t pb = (static_cast<size_t>(ti.c_first + j) * 2 + (j == 0 ? ti.s_first : 0)) * NQ + col0;
-            float lj[kRows];
-            float4 o4[kRows];
-#pragma unroll
-            for (int g = 0; g < kRows; ++g) {
-                if (g >= rows) continue;
-                lj[g] = __ldcg(a.bal_lse + pb + g);
-                o4[g] = __ldcg(reinterpret_cast<const float4*>(a.bal_o + (pb + g) * kD) + lane);
-            }
-#pragma unroll
-            for (int g = 0; g < kRows; ++g) {
-                if (g >= rows || lj[g] == -INFINITY) continue;  // a piece with no token for this row
-                const float Mn = fmaxf(M[g], lj[g]);
-                const float sc = exp2f(M[g] - Mn), w = exp2f(lj[g] - Mn);
-                z[g] = z[g] * sc + w;
-                acc[g].x = fmaf(w, o4[g].x, acc[g].x * sc);
-                acc[g].y = fmaf(w, o4[g].y, acc[g].y * sc);
-                acc[g].z = fmaf(w, o4[g].z, acc[g].z * sc);
-                acc[g].w = fmaf(w, o4[g].w, acc[g].w * sc);
-                M[g] = Mn;
-            }
-        }
-#pragma unroll
-        for (int g = 0; g < kRows; ++g) {
-            if (g >= rows) continue;
-            const float iz = z[g] > 0.f ? 1.f / z[g] : 0.f;
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[g].x * iz, acc[g].y * iz);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[g].z * iz, acc[g].w * iz);
-            uint2 pk;
-            pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-            pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-            *reinterpret_cast<uint2*>(out + out_row<HP>(a, ti.b, ti.h, col0 + g, gh) * kD + 4 * lane) = pk;
-        }
-        if (lane == 0) *counter = 0;  // ready for the next call
-    }
 }
 
 // Fused append (decode), done by the producer warp: the rows [K, V] x [HP
@@ -1170,7 +1041,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 for (long long g = g0; g < g1 && ok; ++g, ++k) {
                     const long long pstart = cum + static_cast<long long>(h) * nt, pend = pstart + nt;
                     if (g == g0 || t == 0) {  // a new segment: who shares this (sequence, KV head)
-                        if constexpr (NQ <= 8 || HP > 1) {  // fused append: the segment holds the unit's last tile
+                        if constexpr (NQ <= 8) {  // fused append: the segment holds the unit's last tile
                             app = a.new_k != nullptr && pend <= g1 && a.lens[b] == L;
                             if (app) nr.prefetch(a, b, h, lane);
                         }
@@ -1215,7 +1086,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             const int ntiles = (t_end - t_begin + kTT - 1) / kTT;
             NewRows<DT, HP> nr;
             bool app = false;
-            if constexpr (NQ <= 8 || HP > 1) {  // fused append: this split holds the newest position
+            if constexpr (NQ <= 8) {  // fused append: this split holds the newest position
                 app = a.new_k != nullptr && t_end == fL && a.lens[fb_] == fL;
                 if (app) nr.prefetch(a, fb_, fh_, lane);
             }
@@ -1266,8 +1137,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int col_end = HP == 1 ? nq : col0 + gh;
     const int rbase = wt * Lt::kRowsPerWarp;
     const float qk = a.qk_scale_log2;
-    // FP8: O accumulates probabilities scaled by kFp8PScale
-    const float vscale = DT == PKV_FP8_E4M3 ? a.v_scale / kFp8PScale : a.v_scale;
+    // (O and l carry the same probability scale, which cancels in O / l)
+    const float vscale = a.v_scale;
+    // log-sum-exp of a piece: max + log2(l), less the probability scale
+    constexpr float kLseBias = DT == PKV_FP8_E4M3 ? kFp8PLog2 : 0.f;
     const int bsz = a.block_size;
     const uint32_t half_stride = static_cast<uint32_t>(HP * bsz * kBoxRowBytes);
     // m-tile i of call k: rows rbase+16(k*kCallMT+i).. = block row/bs of the tile, rows row%bs.. of it
@@ -1362,11 +1235,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const bool seg_last = (ti.flags & kSegLast) != 0;
         if (!kInStage || !seg_last) release(s);
         if (!seg_last) continue;
-        if constexpr (Lt::kHeadPerWarp) {
-            head_epilogue<DT, NQ, kBal, HP>(a, acc, ti, hp, col0, col_end, gh, lane, vscale, fsplit);
-            if (ti.flags & kCtaLast) break;
-            continue;
-        } else {
 
         // ---- segment end: merge the token groups, emit
         if constexpr (kInStage) {  // the stage becomes the merge area once every warp is done reading it
@@ -1393,7 +1261,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                                                   static_cast<size_t>(ti.h) * gh + n % gh
                                             : static_cast<size_t>(ti.b) * a.num_q_heads + static_cast<size_t>(HP * ti.h) * gh + n;
                 a.o_part[(prow * a.num_splits + fsplit) * kD + d] = l > 0.f ? v * (vscale / l) : 0.f;
-                if (d == 0) a.lse_part[prow * a.num_splits + fsplit] = l > 0.f ? M + log2f(l) : -INFINITY;
+                if (d == 0) a.lse_part[prow * a.num_splits + fsplit] = l > 0.f ? M + log2f(l) - kLseBias : -INFINITY;
             }
         } else {
             // partial of a (sequence, KV head) shared with other CTAs
@@ -1404,7 +1272,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 float v, M, l;
                 merge_get<NQ, kWT>(mg, n, d, v, M, l);
                 a.bal_o[(pbase + n) * kD + d] = l > 0.f ? v * (vscale / l) : 0.f;
-                if (d == 0) a.bal_lse[pbase + n] = l > 0.f ? M + log2f(l) : -INFINITY;
+                if (d == 0) a.bal_lse[pbase + n] = l > 0.f ? M + log2f(l) - kLseBias : -INFINITY;
             }
             if constexpr (kInStage) release(s);
             // Publish: after the consumer barrier one GPU-scope acq_rel atomic by
@@ -1488,7 +1356,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             if (!csync()) break;  // the dedicated merge area is reused by the next segment
         }
         if (ti.flags & kCtaLast) break;
-        }
     }
 }
 
@@ -1539,13 +1406,6 @@ template <int DT, bool kBal>
 cudaError_t launch_rows(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
     const int rows = a.num_queries * (a.num_q_heads / a.num_kv_heads);
     if constexpr (DT == PKV_BF16) {
-        if (a.heads_per_cta == 4) {  // four KV heads, one consumer warp each: 4 * rows columns
-            if (a.num_queries != 1 || a.num_kv_heads % 4 != 0) return cudaErrorNotSupported;
-            if (rows <= 1) return launch_nq<DT, 4, kBal, 4>(a, tk, tv, stream);
-            if (rows <= 2) return launch_nq<DT, 8, kBal, 4>(a, tk, tv, stream);
-            if (rows <= 4) return launch_nq<DT, 16, kBal, 4>(a, tk, tv, stream);
-            return cudaErrorNotSupported;
-        }
         if (a.heads_per_cta == 2) {  // a KV-head pair: 2 * rows columns
             if (a.num_queries != 1 || a.num_kv_heads % 2 != 0) return cudaErrorNotSupported;
             if (rows <= 1) return launch_nq<DT, 2, kBal, 2>(a, tk, tv, stream);

@@ -23,9 +23,6 @@ struct pkv_pool {
     int tmap_pair;           // 1: tmap_k2 / tmap_v2 are ready (3D boxes of two adjacent KV heads of a block)
     CUtensorMap tmap_k2;
     CUtensorMap tmap_v2;
-    int tmap_quad;           // 1: tmap_k4 / tmap_v4 are ready (3D boxes of four adjacent KV heads of a block)
-    CUtensorMap tmap_k4;
-    CUtensorMap tmap_v4;
     int tmap_half;           // 1: tmap_kh / tmap_vh are ready (3D boxes of one 64-column half of a block)
     CUtensorMap tmap_kh;
     CUtensorMap tmap_vh;
@@ -81,7 +78,7 @@ struct DecodeArgs {
     // Decode: q_total = num_queries = 1, q_first = len_trim = 0.
     int num_queries;
     int q_total, q_first, len_trim;
-    int heads_per_cta;        // tensor-core design: 1, or 2 / 4 (adjacent KV heads share a CTA; decode, 16-token blocks)
+    int heads_per_cta;        // tensor-core design: 1, or 2 (adjacent KV heads share a CTA; decode, 16-token blocks)
     // Fused append (tensor-core decode): the newest token of sequence b
     // (position seq_lens[b] - 1) has rows new_k / new_v [B][Hkv][D] of dtype
     // new_dtype (PKV_BF16 or PKV_F32); the CTA whose tile holds that position

@@ -24,9 +24,9 @@ def _w(name, G, Hkv, bs, kv, ind, lens, qd=""):
 
 CASES = [
     _w("bf16_pair_g4_bs16", 4, 2, 16, "bf16", "bf16", EDGE),         # KV-head pairs
-    _w("bf16_quad_g1_bs16", 1, 4, 16, "bf16", "bf16", (1, 16, 17, 90, 0)),  # four KV heads per CTA
-    _w("bf16_quad_g4_bs16", 4, 8, 16, "bf16", "bf16", EDGE),
-    _w("bf16_quad_g2_from_f32_bs16", 2, 4, 16, "bf16", "f32", (33, 1, 400), qd="bf16"),
+    _w("bf16_pairs_hkv4_g1_bs16", 1, 4, 16, "bf16", "bf16", (1, 16, 17, 90, 0)),
+    _w("bf16_pairs_hkv8_g4_bs16", 4, 8, 16, "bf16", "bf16", EDGE),
+    _w("bf16_pairs_g2_from_f32_bs16", 2, 4, 16, "bf16", "f32", (33, 1, 400), qd="bf16"),
     _w("bf16_pair_g1_bs16", 1, 2, 16, "bf16", "bf16", (1, 16, 17, 90, 0)),
     _w("bf16_g2_bs32", 2, 3, 32, "bf16", "bf16", (1, 31, 32, 33, 700, 0)),
     _w("bf16_from_f32_g8_bs16", 8, 1, 16, "bf16", "f32", (40, 100, 1), qd="bf16"),

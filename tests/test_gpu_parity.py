@@ -45,10 +45,10 @@ SMALL = [
     _w("pair_g1_bs16", 1, 4, 128, 16, "bf16", "bf16", (1, 16, 33, 200, 0, 511)),
     _w("pair_g2_bs16", 2, 2, 128, 16, "bf16", "bf16", EDGE_LENS),
     _w("pair_g3_bs16", 3, 2, 128, 16, "bf16", "bf16", (2, 17, 64, 129, 700)),
-    # four KV heads per CTA, one consumer warp each (16-token blocks, KV heads a multiple of 4)
-    _w("quad_g4_bs16", 4, 4, 128, 16, "bf16", "bf16", EDGE_LENS),
-    _w("quad_g2_bs16", 2, 8, 128, 16, "bf16", "bf16", (1, 16, 17, 250, 0, 2049)),
-    _w("quad_g3_bs16", 3, 4, 128, 16, "bf16", "bf16", (2, 17, 64, 129, 700)),
+    # several KV-head pairs per sequence (4 and 8 KV heads)
+    _w("pairs_hkv4_g4_bs16", 4, 4, 128, 16, "bf16", "bf16", EDGE_LENS),
+    _w("pairs_hkv8_g2_bs16", 2, 8, 128, 16, "bf16", "bf16", (1, 16, 17, 250, 0, 2049)),
+    _w("pairs_hkv4_g3_bs16", 3, 4, 128, 16, "bf16", "bf16", (2, 17, 64, 129, 700)),
 ]
 
 
