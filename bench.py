@@ -82,7 +82,7 @@ def _profile_traffic(kernel_tag: str, src_hash: str):
 KERNEL_SOURCES = {"simt": ("decode_simt.cu", "device_common.cuh", "pkv_internal.h"),
                   "mma": ("decode_mma.cuh", "decode_mma.cu", "decode_mma_bf16.cu", "decode_mma_fp8.cu",
                           "device_common.cuh", "pkv_internal.h"),
-                  "tc": ("attention_tc.cu", "device_common.cuh", "pkv_internal.h")}
+                  "tc": ("attention_tc.cu", "tc_common.cuh", "device_common.cuh", "pkv_internal.h")}
 
 
 def kernel_hash(algo: str) -> str:
