@@ -342,16 +342,20 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
             }
             const uint32_t dst0 = sbase + kKVOff + s * kStageBytes + (is_v ? 2 * kHalfBytes : 0);
             if (lane == 0) bar_expect_tx(B(full0 + s), static_cast<uint32_t>(nblk * bs * 128 * 2));
-            for (int kb = 0; kb < nblk; ++kb) {
-                int blk = __shfl_sync(0xFFFFFFFFu, cache, idx0 + kb - cache_base);
-                if (lane == 0 && static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks)) {
-                    if (a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
-                    blk = 0;  // read an in-bounds block; the flag marks the output invalid
-                }
-                if (lane == 0) {
+            __syncwarp();
+            // One copy instruction for the whole tile: lane 2 kb + hf copies
+            // half hf of block kb (issuing a copy costs a few hundred cycles,
+            // about the same for one lane or eight).
+            {
+                const int kb = lane >> 1, hf = lane & 1;
+                int blk = __shfl_sync(0xFFFFFFFFu, cache, (idx0 + kb - cache_base) & 31);
+                if (kb < nblk) {
+                    if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks)) {
+                        if (a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
+                        blk = 0;  // read an in-bounds block; the flag marks the output invalid
+                    }
                     const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + w.h) * bs);
-                    for (int hf = 0; hf < 2; ++hf)
-                        tma_3d(dst0 + hf * kHalfBytes + kb * bs * 128, map, 0, y, hf, B(full0 + s));
+                    tma_3d(dst0 + hf * kHalfBytes + kb * bs * 128, map, 0, y, hf, B(full0 + s));
                 }
             }
         }

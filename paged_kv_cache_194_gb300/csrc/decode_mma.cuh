@@ -882,28 +882,33 @@ __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorM
         }
     }
     const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
-    for (int k = 0; k < nblk; ++k) {
-        int blk = __shfl_sync(0xFFFFFFFFu, myblk, k);
+    if (append) {  // the block holding the unit's newest position takes its new row before the copies
+        const int blk = __shfl_sync(0xFFFFFFFFu, myblk, nblk - 1);
+        if (static_cast<unsigned>(blk) < static_cast<unsigned>(a.num_blocks)) nr.write(a, ti.h, blk, (ti.L - 1) % bs, lane);
+    }
+    __syncwarp();  // (and the expected bytes are posted before any copy lands)
+    // One copy instruction for the whole stage: lane l copies box l of the
+    // (block, K or V, half) list.  Issuing a copy costs a few hundred cycles,
+    // about the same for one lane or several, so one lane issuing them in
+    // turn held the ring back.  A box holds the block's rows of the HP
+    // adjacent KV heads; with 3D boxes, both 128-byte halves of every row.
+    constexpr int kBoxes = 1;  // per block and tensor with 3D boxes
+    const int bpb = (Lt::kHalves == 2 && a.tma_3d) ? kBoxes : Lt::kHalves;
+    const int k = lane / (2 * bpb), r = lane % (2 * bpb), tv = r / bpb, hf = r % bpb;
+    int blk = __shfl_sync(0xFFFFFFFFu, myblk, k & 31);
+    if (k < nblk) {  // nblk * 2 * bpb <= 32: a tile holds at most 128 tokens, blocks hold 16 or more
         if (static_cast<unsigned>(blk) >= static_cast<unsigned>(a.num_blocks)) {
-            if (lane == 0 && a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
+            if (a.err) atomicOr(a.err, PKV_ERRBIT_BLOCK_ID);
             blk = 0;  // read an in-bounds block; the flag marks the output invalid
-        } else if (append && k == nblk - 1) {  // the block holding the unit's newest position
-            nr.write(a, ti.h, blk, (ti.L - 1) % bs, lane);
-            __syncwarp();
         }
-        if (lane == 0) {  // a box holds the block's rows of the HP adjacent KV heads
-            const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + HP * ti.h) * bs);
-            const uint32_t off = k * Lt::kHalves * HP * bs * kBoxRowBytes;
-            if (Lt::kHalves == 2 && a.tma_3d) {  // one box: both 128-byte halves of every row
-                tma_load_3d(smem_u32(kst + off), tmk, 0, y, 0, fb);
-                tma_load_3d(smem_u32(vst + off), tmv, 0, y, 0, fb);
-            } else {
-                for (int hf = 0; hf < Lt::kHalves; ++hf) {  // (never with HP = 2: the host requires 3D boxes)
-                    const uint32_t o2 = off + hf * HP * bs * kBoxRowBytes;
-                    tma_load_2d(smem_u32(kst + o2), tmk, hf * 64, y, fb);
-                    tma_load_2d(smem_u32(vst + o2), tmv, hf * 64, y, fb);
-                }
-            }
+        const int y = static_cast<int>(((layer_blk0 + blk) * a.num_kv_heads + HP * ti.h) * bs);
+        const uint32_t off = k * Lt::kHalves * HP * bs * kBoxRowBytes;
+        uint8_t* dst = tv ? vst : kst;
+        const CUtensorMap* map = tv ? tmv : tmk;
+        if (Lt::kHalves == 2 && a.tma_3d) {
+            tma_load_3d(smem_u32(dst + off), map, 0, y, 0, fb);
+        } else {  // (never with HP = 2: the host requires 3D boxes)
+            tma_load_2d(smem_u32(dst + off + hf * HP * bs * kBoxRowBytes), map, hf * 64, y, fb);
         }
     }
 }
