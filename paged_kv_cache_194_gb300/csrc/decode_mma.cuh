@@ -956,8 +956,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int Hu = a.num_kv_heads / HP;             // KV-head units per sequence
 
     // Launched as a programmatic dependent of the previous kernel in the
-    // stream (the append): nothing is read before that grid has finished.
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // stream (the append, or the previous decode step).  The next kernel may
+    // be scheduled at once: it waits for this grid before it touches what
+    // this grid writes, so its CTAs take over SMs as ours leave and run
+    // their prologue meanwhile.  The fixed schedule waits here; the balanced
+    // one first cuts its range from the sequence lengths (which no kernel of
+    // this library writes), then waits: before anything else is read or any
+    // global memory written.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    if constexpr (!kBal) asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
     // fixed schedule: this CTA's one segment
     int fb_ = 0, fh_ = 0, fsplit = 0, t_begin = 0, t_end = 0, fL = 0;
@@ -1043,6 +1050,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 TileInfo ti;
                 NewRows<DT, HP> nr;
                 bool app = false;  // this CTA appends the current unit's newest token
+                asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the previous grid is done
                 for (long long g = g0; g < g1 && ok; ++g, ++k) {
                     const long long pstart = cum + static_cast<long long>(h) * nt, pend = pstart + nt;
                     if (g == g0 || t == 0) {  // a new segment: who shares this (sequence, KV head)
@@ -1198,6 +1206,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     };
 
     if constexpr (kBal) {
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the previous grid is done
         // zero the rows of sequences with nothing visible (and report bad
         // lengths once), while the first tiles are in flight
         const int per_seq = a.num_queries * a.num_q_heads;
