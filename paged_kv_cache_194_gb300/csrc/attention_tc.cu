@@ -556,16 +556,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                 l = l * alpha + lt;
                 tmem_st32(sa, pk);
             }
-            // PV completions, one barrier per score buffer.  A parity wait is only
-            // unambiguous when the barrier is at most one phase from the one
-            // awaited, so every phase is consumed: PV k - NSB here, which has
-            // finished already (S k, just read, was issued after it, and MMAs
-            // complete in order).  PV k cannot finish before this softmax
-            // signals P k.  So only a rescale of O waits for the PV before it.
-            if (k >= Lt::kNSB && !bar_wait_warp(B(Lt::kPvDone + s), ((k / Lt::kNSB) - 1) & 1)) {
-                ok = false;
-                break;
-            }
+            // PV completions, one barrier per score buffer.  A parity wait is
+            // unambiguous while the barrier is at most one phase past the one
+            // awaited.  Here every PV before S k has finished (S k, just read,
+            // was issued after them, and MMAs complete in order), and PV k + 1
+            // cannot finish before this softmax signals P k + 1: so the waits
+            // below for PV k - 1 (a rescale of O) and PV k (the segment end)
+            // see their phase, or the one before it, and need no other wait.
             const bool any_rescale = busy && __any_sync(0xFFFFFFFFu, rescale);
             if (any_rescale) {  // O is stable from PV k - 1 until P k is signalled
                 if (!bar_wait_warp(B(Lt::kPvDone + (k - 1) % Lt::kNSB), ((k - 1) / Lt::kNSB) & 1)) {
