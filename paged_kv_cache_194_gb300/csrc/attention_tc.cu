@@ -318,7 +318,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         // so K loads run a tile ahead of V loads.
         const bool is_v = warp == 6;
         const CUtensorMap* map = is_v ? &tmv : &tmk;
-        const int full0 = is_v ? Lt::kVFull : Lt::kKFull, empty0 = is_v ? Lt::kVEmpty : Lt::kKEmpty;
+        // With as many stages as score buffers, stage s is freed by the same
+        // completion that signals score buffer s (S done for K, PV done for
+        // V): the producers wait on those barriers and the MMA thread issues
+        // two commits per tile fewer (a commit costs about what an MMA does
+        // to issue).
+        constexpr bool kSame = kNS == Lt::kNSB;
+        const int full0 = is_v ? Lt::kVFull : Lt::kKFull;
+        const int empty0 = is_v ? (kSame ? Lt::kPvDone : Lt::kVEmpty) : (kSame ? Lt::kSFull : Lt::kKEmpty);
         const int bs = a.block_size;
         const int64_t layer_blk0 = static_cast<int64_t>(a.layer) * a.num_blocks;
         // Block-table entries cache_base .. cache_base + 31 of sequence cache_b,
@@ -406,7 +413,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                                  sdesc(kst + (ks >> 2) * kHalfBytes + kin, 16), idesc(kTok, 0), ks > 0 ? 1u : 0u);
                     }
                     mma_commit(B(Lt::kSFull + ns % NSB));
-                    mma_commit(B(Lt::kKEmpty + st));  // K of this stage no longer needed
+                    if constexpr (kNS != NSB) mma_commit(B(Lt::kKEmpty + st));  // K of this stage no longer needed
                     ws.next(a);
                     ++ns;
                 }
@@ -433,7 +440,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                     mma_bf16_ta(tmem + Lt::kOCol, pb + 8 * ks, sdesc(vst + ks * 16 * 128, kHalfBytes), idesc(kDim, 1),
                                 (!first || ks > 0) ? 1u : 0u);
                 mma_commit(B(Lt::kPvDone + k % NSB));
-                mma_commit(B(Lt::kVEmpty + k % kNS));
+                if constexpr (kNS != NSB) mma_commit(B(Lt::kVEmpty + k % kNS));
             }
             if (!ok) fail();
             mma_commit(B(kDone));  // completes once every MMA issued above has finished
