@@ -115,6 +115,7 @@ constexpr int kSegLast = 2;   // last tile of a segment (merge and emit)
 constexpr int kSegWhole = 4;  // the segment is the whole sequence
 constexpr int kCtaFirst = 8;  // the segment holds the CTA's first tile
 constexpr int kEnd = 16;      // no tiles at all (a CTA that owns none)
+constexpr int kLenRegs = 8;   // sequence lengths per producer lane held in registers by the balanced cut
 constexpr int kCtaLast = 32;  // the CTA's last tile
 
 // Shared memory of one CTA:
@@ -956,15 +957,12 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int Hu = a.num_kv_heads / HP;             // KV-head units per sequence
 
     // Launched as a programmatic dependent of the previous kernel in the
-    // stream (the append, or the previous decode step).  The next kernel may
-    // be scheduled at once: it waits for this grid before it touches what
-    // this grid writes, so its CTAs take over SMs as ours leave and run
-    // their prologue meanwhile.  The fixed schedule waits here; the balanced
-    // one first cuts its range from the sequence lengths (which no kernel of
-    // this library writes), then waits: before anything else is read or any
-    // global memory written.
+    // stream (the append, or the previous decode step): nothing is read
+    // before that grid has finished.  The next kernel may be scheduled at
+    // once: it too waits before it reads anything, so its CTAs take over SMs
+    // as ours leave.
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-    if constexpr (!kBal) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
     // fixed schedule: this CTA's one segment
     int fb_ = 0, fh_ = 0, fsplit = 0, t_begin = 0, t_end = 0, fL = 0;
@@ -1011,9 +1009,22 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         };
         if constexpr (kBal) {
             const int B = a.num_seqs, Hkv = Hu;
+            // The tiles of sequences lane, lane + 32, ... (batches up to 256):
+            // one round of independent loads for both passes below, instead
+            // of a dependent load per 32 sequences and pass.
+            int ntl[kLenRegs];
+#pragma unroll
+            for (int i = 0; i < kLenRegs; ++i) ntl[i] = seq_tiles<kTT>(a, 32 * i + lane);
+            auto tiles32 = [&](int b0) {  // the tiles of sequence b0 + lane
+                int v = 0;
+#pragma unroll
+                for (int i = 0; i < kLenRegs; ++i)
+                    if (b0 == 32 * i) v = ntl[i];
+                return b0 < 32 * kLenRegs ? v : seq_tiles<kTT>(a, b0 + lane);
+            };
             long long T = 0;
 #pragma unroll 4
-            for (int b0 = 0; b0 < B; b0 += 32) T += warp_sum_ll(seq_tiles<kTT>(a, b0 + lane));
+            for (int b0 = 0; b0 < B; b0 += 32) T += warp_sum_ll(tiles32(b0));
             T *= Hkv;
             // CTA c < P owns tiles [c*T/P, (c+1)*T/P); P <= T keeps every range non-empty
             const long long P = T < static_cast<long long>(gridDim.x) ? T : static_cast<long long>(gridDim.x);
@@ -1024,7 +1035,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 long long cum = 0;
                 int b = 0;
                 for (int b0 = 0; b0 < B; b0 += 32) {
-                    const long long u = static_cast<long long>(seq_tiles<kTT>(a, b0 + lane)) * Hkv;
+                    const long long u = static_cast<long long>(tiles32(b0)) * Hkv;
                     long long incl = u;
 #pragma unroll
                     for (int o = 1; o < 32; o <<= 1) {
@@ -1050,7 +1061,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 TileInfo ti;
                 NewRows<DT, HP> nr;
                 bool app = false;  // this CTA appends the current unit's newest token
-                asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the previous grid is done
                 for (long long g = g0; g < g1 && ok; ++g, ++k) {
                     const long long pstart = cum + static_cast<long long>(h) * nt, pend = pstart + nt;
                     if (g == g0 || t == 0) {  // a new segment: who shares this (sequence, KV head)
@@ -1206,7 +1216,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     };
 
     if constexpr (kBal) {
-        asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the previous grid is done
         // zero the rows of sequences with nothing visible (and report bad
         // lengths once), while the first tiles are in flight
         const int per_seq = a.num_queries * a.num_q_heads;

@@ -119,3 +119,29 @@ def test_fused_unsupported_designs():
     with pytest.raises(pk.PkvError):
         pk.paged_decode_append_attention(q.cuda(), kn.cuda(), vn.cuda(), batch.pool, 0, batch.tables().cuda(),
                                          batch.seq_lens().cuda(), 9, w.scale)
+
+
+def test_lengths_written_by_the_kernel_before():
+    """Decode calls back to back, each reading lengths that a kernel wrote
+    just before it on the same stream (no host synchronisation between
+    them): every call must match the oracle for the lengths it was given."""
+    w = CASES[2]
+    inst = wl.instance(w)
+    batch = DecodeBatch(inst)
+    slots = batch.next_token_slots()
+    q, kn, vn = batch.step_inputs(0)
+    pk.kv_append(batch.pool, 0, kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda())
+    tables, lens = batch.tables().cuda(), batch.seq_lens().cuda()
+    max_len = int(lens.max())
+    outs, used = [], []
+    for cut in (0, 1, 3, 0, 40):
+        lens_dev = torch.clamp(lens - cut, min=0).to(torch.int32)  # a kernel writes them
+        outs.append(pk.paged_decode_attention(q.cuda(), batch.pool, 0, tables, lens_dev, max_len, w.scale,
+                                              algo="mma"))
+        used.append(lens_dev)
+    torch.cuda.synchronize()
+    assert batch.pool.errors() == 0
+    for out, L in zip(outs, used):
+        ref, _ = oracle_reference(w, inst.k_scale, inst.v_scale, 0, q, tables.cpu(), L.cpu().tolist(),
+                                  list(range(w.num_seqs)))
+        compare(out, ref, TOL[w.kv_dtype], "lengths written by the kernel before")
