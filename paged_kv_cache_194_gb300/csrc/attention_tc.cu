@@ -384,6 +384,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
             // wait (for K, or for a Q the softmax stores only after scores not
             // yet issued) is left for later, so the PVs the softmax may be
             // waiting on still get issued.
+            // Operand descriptors.  Their address field holds the shared-memory
+            // address / 16, so the descriptor of base + off is the base's plus
+            // off / 16 (no carry: a CTA's shared addresses stay below 2^18):
+            // the issuing thread, which sets the pace, adds one constant per MMA.
+            const uint64_t dq = sdesc(sbase + kQOff, 16);
+            const uint64_t dk0 = sdesc(sbase + kKVOff, 16);
+            const uint64_t dv0 = sdesc(sbase + kKVOff + 2 * kHalfBytes, kHalfBytes);
             Walk<kBal> ws = w;
             int ns = 0;     // S issued
             int seg_s = 0;  // segments whose Q tile the S cursor has taken
@@ -404,13 +411,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                     }
                     if (q_new) ++seg_s;
                     fence_after();
-                    const uint32_t kst = sbase + kKVOff + st * kStageBytes;
+                    const uint64_t dk = dk0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
                     const uint32_t sb = tmem + static_cast<uint32_t>((ns % NSB) * kTok);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {  // K = head_dim in 16-wide steps
                         const uint32_t kin = (ks & 3) * 32;
-                        mma_bf16(sb, sdesc(sbase + kQOff + (ks >> 2) * kQHalf + kin, 16),
-                                 sdesc(kst + (ks >> 2) * kHalfBytes + kin, 16), idesc(kTok, 0), ks > 0 ? 1u : 0u);
+                        mma_bf16(sb, dq + (((ks >> 2) * kQHalf + kin) >> 4), dk + (((ks >> 2) * kHalfBytes + kin) >> 4),
+                                 idesc(kTok, 0), ks > 0 ? 1u : 0u);
                     }
                     mma_commit(B(Lt::kSFull + ns % NSB));
                     if constexpr (kNS != NSB) mma_commit(B(Lt::kKEmpty + st));  // K of this stage no longer needed
@@ -433,11 +440,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                 }
                 if (first) ++seg;
                 fence_after();
-                const uint32_t vst = sbase + kKVOff + (k % kNS) * kStageBytes + 2 * kHalfBytes;
+                const uint64_t dv = dv0 + static_cast<uint64_t>(((k % kNS) * kStageBytes) >> 4);
                 const uint32_t pb = tmem + static_cast<uint32_t>((k % NSB) * kTok);
 #pragma unroll
                 for (int ks = 0; ks < kTok / 16; ++ks)  // K = tokens in 16-wide steps: 8 TMEM columns of P each
-                    mma_bf16_ta(tmem + Lt::kOCol, pb + 8 * ks, sdesc(vst + ks * 16 * 128, kHalfBytes), idesc(kDim, 1),
+                    mma_bf16_ta(tmem + Lt::kOCol, pb + 8 * ks, dv + ((ks * 16 * 128) >> 4), idesc(kDim, 1),
                                 (!first || ks > 0) ? 1u : 0u);
                 mma_commit(B(Lt::kPvDone + k % NSB));
                 if constexpr (kNS != NSB) mma_commit(B(Lt::kVEmpty + k % kNS));
