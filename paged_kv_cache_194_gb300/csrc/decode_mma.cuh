@@ -28,7 +28,7 @@
 //    partials by their log-sum-exp and writes the output.
 //  * fixed splits (when the caller names a split size): one CTA per
 //    (split, KV head, sequence); partials go to the combine kernel.
-// CTA = 4 consumer warps + 1 producer warp.
+// CTA = 4 consumer warps + 1 producer warp (+ 1 publisher warp: balanced, FP8).
 //  * Producer: one lane walks the block table and issues, per stage, one TMA
 //    tile load (cp.async.bulk.tensor, 128-byte swizzle) per block of K and of
 //    V: for BF16 a 3D box {64 columns, bs rows, 2 halves} fetches a block's
@@ -59,6 +59,13 @@
 //    memory and the CTA writes the final rows or its fp32 partials.  When a
 //    dedicated merge area would cost the second CTA per SM, the merge uses the
 //    buffer of the segment's last stage, which is released only afterwards.
+//  * Publisher (balanced schedule, FP8 pools): at a segment's end the consumers only put
+//    their (m, l, O) into the segment's last stage and post a message; the
+//    publisher warp writes the rows or the partial, frees the stage, counts
+//    the piece and merges when it is the last.  A partial must be visible
+//    GPU-wide before it is counted, and that release waits behind the SM's
+//    copies in flight (microseconds mid-stream), so the consumers do not wait
+//    for it: they go on with the next segment.
 // Rows past the sequence end inside a loaded block are masked in S and zeroed
 // in V (uninitialised pool bytes could hold NaN patterns, and 0 * NaN = NaN).
 // Every mbarrier wait is bounded; on expiry the CTA flags PKV_ERRBIT_TIMEOUT,
@@ -80,7 +87,16 @@ cudaError_t launch_decode_mma_fp8(const DecodeArgs& a, const CUtensorMap& tk, co
 namespace {
 
 constexpr int kCWarps = 4;
-constexpr int kMmaThreads = (kCWarps + 1) * 32;
+// The balanced schedule over an FP8 pool adds a publisher warp (see
+// publisher()): there the consumers set the pace, and it takes the segment
+// ends off them.  Over BF16 the stream of copies sets the pace; three stages in
+// flight already cover the consumers' segment ends, and the publisher's
+// mid-stream release fence cost more than it saved (measured).
+template <int DT, bool kBal>
+constexpr bool kPubOf = kBal && DT == PKV_FP8_E4M3;
+// consumers + producer (+ publisher)
+template <bool kPub>
+constexpr int kThreadsOf = (kCWarps + (kPub ? 2 : 1)) * 32;
 constexpr int kBoxRowBytes = 128;          // one swizzled TMA row
 constexpr int kD = 128;                    // head_dim served by this design
 constexpr uint32_t kSpinLimit = 1u << 22;  // try_wait polls before a wait gives up
@@ -125,9 +141,13 @@ constexpr int kCtaLast = 32;  // the CTA's last tile
 //     128-byte swizzle phase of a row is its row index within the block, mod 8.
 //   q slots [kStages][NQ][128] BF16, tile info [kStages],
 //   merge m, l [kWT][NQ] + one flag word,
-//   merge O [kWT][NQ][128] fp32 (dedicated, or in the segment's last stage),
-//   barriers full[kStages], empty[kStages], consumer sync, abort word.
-template <int DT, int NQ, int HP = 1>
+//   with a publisher: merge m, l [kStages][kWT][NQ] (of a segment ending in that stage),
+//   merge O [kWT][NQ][128] fp32 (dedicated, or in the segment's last stage;
+//     always the stage with a publisher, which reads it while the consumers
+//     go on),
+//   barriers full[kStages], empty[kStages], consumer sync, abort word,
+//   with a publisher: message barriers [kStages], message ring [kStages], progress word.
+template <int DT, int NQ, int HP = 1, bool kPub = false>
 struct Layout {
     static constexpr int kHalves = MmaCfg<DT>::kHalves;
     static constexpr int kMT = MmaCfg<DT>::kMT;
@@ -155,10 +175,13 @@ struct Layout {
     static constexpr size_t kInfoOff = kQOff + static_cast<size_t>(kStages) * kQBytes;
     static constexpr size_t kMlOff = kInfoOff + static_cast<size_t>(kStages) * sizeof(TileInfo);
     static constexpr size_t kMlBytes = (static_cast<size_t>(kWT) * NQ * 2 + 4) * 4;
+    static constexpr size_t kStageMlOff = (kMlOff + kMlBytes + 15) / 16 * 16;
+    static constexpr size_t kStageMlBytes = kPub ? static_cast<size_t>(kWT) * NQ * 2 * 4 : 0;
     static constexpr size_t kMergeOBytes = static_cast<size_t>(kWT) * NQ * kD * 4;
-    static constexpr size_t kCtl = (2 * kStages + 1) * 8 + 16;  // barriers + abort word
-    static constexpr size_t kBase = (kMlOff + kMlBytes + 15) / 16 * 16;
-    static constexpr bool kMergeInStage = kBase + kMergeOBytes + kCtl + 1024 > kBudget;
+    // barriers + abort word (+ message barriers, ring and progress word)
+    static constexpr size_t kCtl = (2 * kStages + 1) * 8 + 16 + (kPub ? kStages * 8 + (kStages + 1) * 4 : 0);
+    static constexpr size_t kBase = (kStageMlOff + kStages * kStageMlBytes + 15) / 16 * 16;
+    static constexpr bool kMergeInStage = kPub || kBase + kMergeOBytes + kCtl + 1024 > kBudget;
     static constexpr size_t kMergeOff = kBase;  // dedicated merge O (unused when kMergeInStage)
     static constexpr size_t kBarOff = kBase + (kMergeInStage ? 0 : kMergeOBytes);
     static constexpr size_t kBytes = kBarOff + kCtl;
@@ -181,6 +204,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+// n arrivals at once (the publisher frees a stage for the 4 consumer warps)
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t n) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(n) : "memory");
 }
 // Bounded wait for the phase with the given parity to complete: at most
 // `polls` polls (0: give up without looking).  A pipeline wait passes the
@@ -852,11 +879,11 @@ __device__ __forceinline__ int tile_blocks(const DecodeArgs& a, const int32_t* t
 // Stage s <- tile ti: tile info, the query rows at a segment's first tile,
 // and one TMA box per KV block (K and V).  All 32 producer lanes call it
 // (lane k holds block k's id, from tile_blocks); lane 0 issues.
-template <int DT, int NQ, int HP>
+template <int DT, int NQ, int HP, bool kPub>
 __device__ __forceinline__ void issue_stage(const DecodeArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                             uint8_t* smem, uint64_t* full, int s, const TileInfo& ti, int myblk,
                                             int lane, int gh, NewRows<DT, HP>& nr, bool append) {
-    using Lt = Layout<DT, NQ, HP>;
+    using Lt = Layout<DT, NQ, HP, kPub>;
     const int bs = a.block_size;
     uint8_t* kst = smem + s * Lt::kStageBytes;
     uint8_t* vst = kst + Lt::kTensorBytes;
@@ -926,13 +953,168 @@ __device__ __forceinline__ int seq_tiles(const DecodeArgs& a, int b) {
     return b < a.num_seqs ? (visible_len(a, b, false) + kTT - 1) / kTT : 0;
 }
 
+// Publisher warp (balanced schedule, FP8 pools).  Message i is the i-th segment end of
+// the CTA: its stage holds the token groups' O, the stage's m/l slot their
+// m and l, and info[stage] the segment.  Messages are taken in order; each
+// keeps its stage until the publisher frees it, so at most kStages are
+// outstanding and a ring of kStages slots cannot be overrun.  Lane l owns
+// head-dim entries 4l..4l+3 of every row.
+template <int DT, int NQ, int HP>
+__device__ __forceinline__ void publisher(const DecodeArgs& a, uint8_t* smem, uint64_t* empty, uint64_t* msg_full,
+                                          const volatile int* msg_ring, const volatile int* progress,
+                                          volatile int* abort_flag, int lane, int gh, int nq) {
+    using Lt = Layout<DT, NQ, HP, true>;
+    constexpr int kStages = Lt::kStages;
+    constexpr int kWT = Lt::kWT;
+    constexpr float kLseBias = DT == PKV_FP8_E4M3 ? kFp8PLog2 : 0.f;
+    const float vscale = a.v_scale;
+    const TileInfo* info = reinterpret_cast<const TileInfo*>(smem + Lt::kInfoOff);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    struct Piece {
+        int b, h, pieces, c_first, s_first;
+    };
+    // every piece is published: out = sum_j 2^(lse_j - M) o_j / sum_j 2^(lse_j - M),
+    // accumulated piece by piece with the running maximum M
+    auto merge = [&](const Piece& pc) {
+        for (int n0 = 0; n0 < nq; n0 += 4) {
+            float4 acc[4];
+            float Mx[4], z[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                Mx[u] = -INFINITY;
+                z[u] = 0.f;
+            }
+#pragma unroll 2
+            for (int j = 0; j < pc.pieces; ++j) {
+                const size_t pb = (static_cast<size_t>(pc.c_first + j) * 2 + (j == 0 ? pc.s_first : 0)) * NQ;
+                float lj[4];
+                float4 oj[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int n = n0 + u < nq ? n0 + u : n0;
+                    lj[u] = __ldcg(a.bal_lse + pb + n);
+                    oj[u] = __ldcg(reinterpret_cast<const float4*>(a.bal_o + (pb + n) * kD) + lane);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (lj[u] == -INFINITY) continue;  // a piece with no token for this query
+                    const float Mn = fmaxf(Mx[u], lj[u]);
+                    const float c = exp2f(Mx[u] - Mn), w = exp2f(lj[u] - Mn);
+                    acc[u].x = fmaf(w, oj[u].x, acc[u].x * c);
+                    acc[u].y = fmaf(w, oj[u].y, acc[u].y * c);
+                    acc[u].z = fmaf(w, oj[u].z, acc[u].z * c);
+                    acc[u].w = fmaf(w, oj[u].w, acc[u].w * c);
+                    z[u] = fmaf(z[u], c, w);
+                    Mx[u] = Mn;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int n = n0 + u;
+                if (n >= nq) break;
+                const float iz = z[u] > 0.f ? 1.f / z[u] : 0.f;
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[u].x * iz, acc[u].y * iz);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[u].z * iz, acc[u].w * iz);
+                uint2 pk;
+                pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                reinterpret_cast<uint2*>(out + out_row<HP>(a, pc.b, pc.h, n, gh) * kD)[lane] = pk;
+            }
+        }
+        if (lane == 0) a.counters[static_cast<size_t>(pc.b) * a.num_kv_heads + pc.h] = 0;  // ready for the next call
+    };
+    for (long long i = 0;; ++i) {
+        const int r = static_cast<int>(i % kStages);
+        // The wait may span a whole segment: rounds of bounded polls, another
+        // round only while the consumers keep taking tiles.
+        bool got = false;
+        for (int seen = *progress;;) {
+            if (mbar_wait(smem_u32(&msg_full[r]), static_cast<uint32_t>((i / kStages) & 1), kSpinLimit, abort_flag)) {
+                got = true;
+                break;
+            }
+            const int now = *progress;
+            if (*abort_flag || now == seen) break;
+            seen = now;
+        }
+        if (!got) {
+            if (lane == 0 && !*abort_flag) {
+                *abort_flag = 1;
+                if (a.err) atomicOr(a.err, PKV_ERRBIT_TIMEOUT);
+            }
+            return;
+        }
+        const int s = msg_ring[r];
+        if (s < 0) return;  // a CTA without tiles
+        const TileInfo ti = info[s];
+        const float* mo = reinterpret_cast<const float*>(smem + static_cast<size_t>(s) * Lt::kStageBytes);
+        const float* mm = reinterpret_cast<const float*>(smem + Lt::kStageMlOff + s * Lt::kStageMlBytes);
+        const float* ml = mm + kWT * NQ;
+        const bool whole = (ti.flags & kSegWhole) != 0;
+        const size_t pbase = (static_cast<size_t>(blockIdx.x) * 2 + ((ti.flags & kCtaFirst) ? 0 : 1)) * NQ;
+        // the segment's rows: sum the token groups' O, scaled to the largest m
+#pragma unroll 4
+        for (int n = 0; n < nq; ++n) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWT; ++w) M = fmaxf(M, mm[w * NQ + n]);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            float l = 0.f;
+            if (M != -INFINITY) {  // else no token for this query in the segment
+#pragma unroll
+                for (int w = 0; w < kWT; ++w) {
+                    const float f = exp2f(mm[w * NQ + n] - M);  // token groups without rows: 2^-inf = 0
+                    const float4 o = reinterpret_cast<const float4*>(mo + (w * NQ + n) * kD)[lane];
+                    v.x += f * o.x;
+                    v.y += f * o.y;
+                    v.z += f * o.z;
+                    v.w += f * o.w;
+                    l += f * ml[w * NQ + n];
+                }
+            }
+            const float sc = l > 0.f ? vscale / l : 0.f;
+            if (whole) {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * sc, v.y * sc);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * sc, v.w * sc);
+                uint2 pk;
+                pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                reinterpret_cast<uint2*>(out + out_row<HP>(a, ti.b, ti.h, n, gh) * kD)[lane] = pk;
+            } else {
+                reinterpret_cast<float4*>(a.bal_o + (pbase + n) * kD)[lane] =
+                    make_float4(v.x * sc, v.y * sc, v.z * sc, v.w * sc);
+                if (lane == 0) a.bal_lse[pbase + n] = l > 0.f ? M + log2f(l) - kLseBias : -INFINITY;
+            }
+        }
+        // the merge area is read: the producer may refill the stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive_n(smem_u32(&empty[s]), kCWarps);
+        if (!whole) {
+            // Count the piece: one GPU-scope acq_rel atomic after the warp's
+            // writes (ordered before it by the __syncwarp above); the last
+            // piece's lanes read the others' writes after it.
+            int last = 0;
+            if (lane == 0)
+                last = (atom_add_acq_rel(a.counters + static_cast<size_t>(ti.b) * a.num_kv_heads + ti.h, 1) ==
+                        ti.pieces - 1)
+                           ? 1
+                           : 0;
+            __syncwarp();
+            if (__shfl_sync(0xFFFFFFFFu, last, 0)) merge(Piece{ti.b, ti.h, ti.pieces, ti.c_first, ti.s_first});
+        }
+        if (ti.flags & kCtaLast) return;
+    }
+}
+
 // kBal: balanced persistent schedule (grid = P CTAs); otherwise one CTA per
 // (split, KV head, sequence) with grid (num_splits, num_kv_heads, num_seqs).
 template <int DT, int NQ, bool kBal, int HP>
-__global__ void __launch_bounds__(kMmaThreads, Layout<DT, NQ, HP>::kMinBlocks)
+__global__ void __launch_bounds__(kThreadsOf<kPubOf<DT, kBal>>, Layout<DT, NQ, HP, kPubOf<DT, kBal>>::kMinBlocks)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const DecodeArgs a) {
-    using Lt = Layout<DT, NQ, HP>;
+    constexpr bool kPub = kPubOf<DT, kBal>;
+    using Lt = Layout<DT, NQ, HP, kPub>;
     constexpr int kStages = Lt::kStages;
     constexpr int kHalves = Lt::kHalves;
     constexpr int kTT = Lt::kTT;
@@ -949,6 +1131,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     uint64_t* empty = full + kStages;
     uint64_t* csync_bar = empty + kStages;  // the 4 consumer warps meet here at segment ends
     volatile int* abort_flag = reinterpret_cast<volatile int*>(csync_bar + 1);
+    // publisher: message i (a segment end) is the stage msg_ring[i % kStages], posted on msg_full[i % kStages]
+    uint64_t* msg_full = csync_bar + 3;
+    volatile int* msg_ring = reinterpret_cast<volatile int*>(msg_full + kStages);
+    volatile int* progress = msg_ring + kStages;  // tiles the consumers have taken
     const TileInfo* info = reinterpret_cast<const TileInfo*>(smem + Lt::kInfoOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -976,7 +1162,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         t_end = min(L, t_begin + a.split_tokens);
         if (t_begin >= t_end) {
             if (a.num_splits == 1) {  // nothing visible: zero output rows
-                for (int i = threadIdx.x; i < nq * kD; i += kMmaThreads)
+                for (int i = threadIdx.x; i < nq * kD; i += kThreadsOf<kPub>)
                     static_cast<__nv_bfloat16*>(a.out)[out_row<HP>(a, fb_, fh_, i / kD, gh) * kD + i % kD] =
                         __float2bfloat16_rn(0.f);
             }
@@ -991,6 +1177,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         mbar_init(smem_u32(csync_bar), kCWarps);
         *abort_flag = 0;
+        if constexpr (kPub) {
+            for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&msg_full[s]), kCWarps);
+            *progress = 0;
+        }
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     __syncthreads();
@@ -1084,7 +1274,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     const int myblk = tile_blocks(a, table, ti, lane);
                     const int s = acquire(k);
                     if (!ok) break;
-                    issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, myblk, lane, gh, nr, app && t == nt - 1);
+                    issue_stage<DT, NQ, HP, kPub>(a, &tmk, &tmv, smem, full, s, ti, myblk, lane, gh, nr, app && t == nt - 1);
                     if (++t == nt) {  // next (sequence, KV head)
                         t = 0;
                         if (++h == Hkv) {
@@ -1128,7 +1318,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 const int myblk = tile_blocks(a, table, ti, lane);
                 const int s = acquire(k);
                 if (!ok) break;
-                issue_stage<DT, NQ, HP>(a, &tmk, &tmv, smem, full, s, ti, myblk, lane, gh, nr, app && t == ntiles - 1);
+                issue_stage<DT, NQ, HP, kPub>(a, &tmk, &tmv, smem, full, s, ti, myblk, lane, gh, nr, app && t == ntiles - 1);
             }
         }
         if (ok && k == 0) {  // a CTA without tiles: tell the consumers
@@ -1149,6 +1339,12 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                 (void)mbar_wait(smem_u32(&full[kk % kStages]), static_cast<uint32_t>((kk / kStages) & 1));
         }
         return;
+    }
+    if constexpr (kPub) {
+        if (warp == kCWarps + 1) {
+            publisher<DT, NQ, HP>(a, smem, empty, msg_full, msg_ring, progress, abort_flag, lane, gh, nq);
+            return;
+        }
     }
 
     // ---------------------------------------------------------------- consumers
@@ -1210,9 +1406,19 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         return okw;
     };
     auto release = [&](int s) {
-        if constexpr (kInStage) fence_proxy_async();  // generic merge writes before the next TMA fill
+        // generic merge writes before the next TMA fill (with a publisher, a
+        // stage with merge writes is freed by it, after that fence)
+        if constexpr (kInStage && !kPub) fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    };
+    long long nmsg = 0;  // messages posted to the publisher
+    auto post = [&](int s) {  // message nmsg: stage s (-1: no tiles)
+        const int r = static_cast<int>(nmsg % kStages);
+        if (threadIdx.x == 0) msg_ring[r] = s;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&msg_full[r]));
+        ++nmsg;
     };
 
     if constexpr (kBal) {
@@ -1240,7 +1446,12 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             break;
         }
         const TileInfo ti = info[s];
-        if (ti.flags & kEnd) break;
+        if (ti.flags & kEnd) {
+            if constexpr (kPub) post(-1);
+            break;
+        }
+        if constexpr (kPub)
+            if (threadIdx.x == 0) *progress = static_cast<int>(k);
         uint8_t* kst = smem + s * Lt::kStageBytes;
         if (ti.flags & kSegFirst)
             acc_begin<DT, kNT>(acc, reinterpret_cast<const __nv_bfloat16*>(smem + Lt::kQOff + s * Lt::kQBytes), lane,
@@ -1262,6 +1473,14 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         // ---- segment end: merge the token groups, emit
         if constexpr (kInStage) {  // the stage becomes the merge area once every warp is done reading it
             if (!csync()) break;
+        }
+        if constexpr (kPub) {  // hand the merge area to the publisher and go on
+            const Merge<NQ, kWT> mg(kst, smem + Lt::kStageMlOff + s * Lt::kStageMlBytes);
+            merge_put<DT, NQ, kWT, kNT>(acc, mg, wt, col0, col_end, lane);
+            fence_proxy_async();  // generic merge writes before the stage's next TMA fill
+            post(s);
+            if (ti.flags & kCtaLast) break;
+            continue;
         }
         const Merge<NQ, kWT> mg(kInStage ? kst : smem + Lt::kMergeOff, smem + Lt::kMlOff);
         merge_put<DT, NQ, kWT, kNT>(acc, mg, wt, col0, col_end, lane);
@@ -1384,7 +1603,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
 template <int DT, int NQ, bool kBal, int HP = 1>
 cudaError_t launch_nq(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-    using Lt = Layout<DT, NQ, HP>;
+    constexpr bool kPub = kPubOf<DT, kBal>;
+    using Lt = Layout<DT, NQ, HP, kPub>;
     constexpr size_t smem = Lt::kAlloc;
     auto kern = decode_mma_kernel<DT, NQ, kBal, HP>;
     static int configured_mask = 0;
@@ -1399,7 +1619,7 @@ cudaError_t launch_nq(const DecodeArgs& a, const CUtensorMap& tk, const CUtensor
             e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kMmaThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreadsOf<kPub>, smem);
         if (e != cudaSuccess) return e;
         ctas_per_sm[dev] = occ > 0 ? occ : 1;
         configured_mask |= 1 << dev;
@@ -1413,7 +1633,7 @@ cudaError_t launch_nq(const DecodeArgs& a, const CUtensorMap& tk, const CUtensor
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kMmaThreads);
+    cfg.blockDim = dim3(kThreadsOf<kPub>);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
