@@ -327,11 +327,14 @@ def test_balanced_schedule_repeats_and_leaves_counters_zero(kv):
     assert batch.pool.errors() == 0
 
 
-def test_balanced_schedule_tiny_batch():
-    """Fewer tiles than CTAs: most CTAs own nothing."""
-    w = _w("balanced_tiny", 4, 1, 128, 16, "bf16", "bf16", (3, 70), seed=34)
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_balanced_schedule_tiny_batch(kv):
+    """Fewer tiles than CTAs: most CTAs own nothing (over FP8 their publisher
+    warp is told so by the consumers)."""
+    w = _w("balanced_tiny_" + kv, 4, 1, 128, 16, kv, "bf16", (3, 70), seed=34)
     inst = wl.instance(w)
     batch = DecodeBatch(inst)
     q, tables, lens, out = _run_step(batch, algo="mma")
-    ref, _ = oracle_reference(w, 1.0, 1.0, 0, q, tables, lens.tolist(), [0, 1])
-    compare(out, ref, TOL["bf16"], "balanced tiny")
+    ref, _ = oracle_reference(w, inst.k_scale, inst.v_scale, 0, q, tables, lens.tolist(), [0, 1])
+    compare(out, ref, TOL[kv], "balanced tiny " + kv)
+    assert batch.pool.errors() == 0
