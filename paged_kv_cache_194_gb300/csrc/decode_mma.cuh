@@ -1586,9 +1586,13 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                     *reinterpret_cast<uint2*>(out + out_row<HP>(a, ti.b, ti.h, n, gh) * kD + 4 * d4) = pk;
                 }
                 if (threadIdx.x == 0) *counter = 0;  // ready for the next call
+                // pass 2 read M and 1/z from the merge m/l area: a warp that
+                // runs ahead must not put its next segment there before every
+                // warp is through (nothing follows the CTA's last segment)
+                if (!(ti.flags & kCtaLast) && !csync()) break;
             }
-            // every consumer read the merge area before the second barrier, so
-            // the next segment may overwrite it without another barrier
+            // otherwise every consumer read the merge area before the second
+            // barrier, so the next segment may overwrite it without another
             if (ti.flags & kCtaLast) break;
             continue;
         }
